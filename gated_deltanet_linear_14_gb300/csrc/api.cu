@@ -1,0 +1,278 @@
+// C ABI of the GDN layer core: host-side validation, layouts and launches.
+// Every entry point checks its arguments completely before launching, so a
+// negative return means nothing was launched and nothing was written.
+#include <cmath>
+#include <cstring>
+
+#include "gdn.h"
+#include "kernels.h"
+
+namespace {
+
+using namespace gdn;
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t dsize(int32_t dt) { return dt == GDN_BF16 ? 2 : 4; }
+inline bool valid_dtype(int32_t dt) { return dt == GDN_F32 || dt == GDN_BF16; }
+
+gdn_status check_dims(const gdn_dims* d) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->num_k_heads <= 0 || d->num_v_heads <= 0 || d->head_k_dim <= 0 || d->head_v_dim <= 0 ||
+      d->conv_width <= 0 || d->max_candidates < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (!valid_dtype(d->io_dtype) || !valid_dtype(d->state_dtype) || !valid_dtype(d->out_dtype))
+    return GDN_ERR_INVALID_ARG;
+  if (d->num_v_heads % d->num_k_heads != 0) return GDN_ERR_UNSUPPORTED;
+  if (d->head_k_dim != d->head_v_dim) return GDN_ERR_UNSUPPORTED;
+  if (d->head_k_dim != 32 && d->head_k_dim != 64 && d->head_k_dim != 128) return GDN_ERR_UNSUPPORTED;
+  if (d->conv_width != 4) return GDN_ERR_UNSUPPORTED;
+  if (d->max_candidates > 8) return GDN_ERR_UNSUPPORTED;
+  if (d->num_v_heads > 4096 || d->num_k_heads > 4096) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+void layout(const gdn_dims* d, gdn_page_layout_t* L, int* rec_row_elems) {
+  const size_t C = 2 * (size_t)d->num_k_heads * d->head_k_dim + (size_t)d->num_v_heads * d->head_v_dim;
+  const size_t io = dsize(d->io_dtype), st = dsize(d->state_dtype);
+  const size_t rec_row = align_up((C + 2 * (size_t)d->num_v_heads) * io, 16) / io;
+  std::memset(L, 0, sizeof(*L));
+  L->state_offset = 0;
+  L->state_bytes = (size_t)d->num_v_heads * d->head_v_dim * d->head_k_dim * st;
+  L->window_offset = align_up(L->state_offset + L->state_bytes, kAlign);
+  L->window_bytes = (size_t)(d->conv_width - 1 + d->max_candidates) * C * io;
+  L->record_offset = align_up(L->window_offset + L->window_bytes, kAlign);
+  L->record_bytes = 2 * (size_t)d->max_candidates * rec_row * io;
+  L->flag_offset = align_up(L->record_offset + L->record_bytes, kAlign);
+  L->page_bytes = align_up(L->flag_offset + sizeof(uint32_t), kAlign);
+  if (rec_row_elems) *rec_row_elems = (int)rec_row;
+}
+
+void slot_layout(const gdn_dims* d, gdn_slot_layout_t* S) {
+  const size_t C = 2 * (size_t)d->num_k_heads * d->head_k_dim + (size_t)d->num_v_heads * d->head_v_dim;
+  const size_t state_bytes =
+      (size_t)d->num_v_heads * d->head_v_dim * d->head_k_dim * dsize(d->state_dtype);
+  const size_t window_bytes = (size_t)(d->conv_width - 1) * C * dsize(d->io_dtype);
+  S->state_offset = 0;
+  S->window_offset = align_up(state_bytes, kAlign);
+  S->slot_bytes = align_up(S->window_offset + window_bytes, kAlign);
+  S->pool_bytes = S->slot_bytes * (size_t)(d->max_candidates > 0 ? d->max_candidates : 1);
+}
+
+Geom make_geom(const gdn_dims* d) {
+  gdn_page_layout_t L;
+  int rec_row = 0;
+  layout(d, &L, &rec_row);
+  Geom G;
+  G.Hk = d->num_k_heads;
+  G.Hv = d->num_v_heads;
+  G.Dk = d->head_k_dim;
+  G.Dv = d->head_v_dim;
+  G.W = d->conv_width;
+  G.Kc = d->max_candidates;
+  G.C = 2 * G.Hk * G.Dk + G.Hv * G.Dv;
+  G.rec_row = rec_row;
+  G.page_bytes = L.page_bytes;
+  G.window_off = L.window_offset;
+  G.state_off = L.state_offset;
+  G.record_off = L.record_offset;
+  G.flag_off = L.flag_offset;
+  return G;
+}
+
+gdn_status check_batch(const gdn_batch* b, bool accepted_may_be_null) {
+  if (!b) return GDN_ERR_INVALID_ARG;
+  if (b->num_requests < 0 || b->num_rows < 0 || b->max_rows < 0 || b->num_pages < 0)
+    return GDN_ERR_INVALID_ARG;
+  if (b->num_requests > 65535) return GDN_ERR_UNSUPPORTED;
+  if (b->num_requests > 0 && (!b->row_start || !b->row_len || !b->page || !b->flags))
+    return GDN_ERR_INVALID_ARG;
+  if (!accepted_may_be_null && b->num_requests > 0 && !b->n_accepted) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+gdn_status check_params(const gdn_params* p, bool need_gates) {
+  if (!p) return GDN_ERR_INVALID_ARG;
+  if (need_gates && (!p->A_log || !p->dt_bias)) return GDN_ERR_INVALID_ARG;
+  if (p->gate_mode != 0 && p->gate_mode != 1) return GDN_ERR_INVALID_ARG;
+  if (!(p->norm_eps >= 0.0f) || !std::isfinite(p->norm_eps)) return GDN_ERR_INVALID_ARG;
+  if (std::isnan(p->scale)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+Batch make_batch(const gdn_batch* b) {
+  Batch B;
+  B.R = b->num_requests;
+  B.num_rows = b->num_rows;
+  B.max_rows = b->max_rows;
+  B.num_pages = b->num_pages;
+  B.row_start = b->row_start;
+  B.row_len = b->row_len;
+  B.page = b->page;
+  B.flags = b->flags;
+  B.n_accepted = b->n_accepted;
+  B.order = b->order;
+  return B;
+}
+
+Params make_params(const gdn_params* p, const gdn_dims* d) {
+  Params P;
+  P.A_log = p->A_log;
+  P.dt_bias = p->dt_bias;
+  P.conv_bias = p->conv_bias;
+  P.scale = (p->scale > 0.0f) ? p->scale : 1.0f / std::sqrt((float)d->head_k_dim);
+  P.eps = p->norm_eps;
+  P.gate_mode = p->gate_mode;
+  return P;
+}
+
+cudaError_t rule(int mode, const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
+                 const gdn_dims* d, const void* qkv, const void* a, const void* b, void* o,
+                 void* pages, int32_t* status, cudaStream_t s) {
+  const int io = d->io_dtype == GDN_BF16, st = d->state_dtype == GDN_BF16,
+            of = d->out_dtype == GDN_F32;
+  switch (d->head_k_dim) {
+    case 32: return launch_rule_d32(mode, G, B, P, SG, io, st, of, qkv, a, b, o, pages, status, s);
+    case 64: return launch_rule_d64(mode, G, B, P, SG, io, st, of, qkv, a, b, o, pages, status, s);
+    default: return launch_rule_d128(mode, G, B, P, SG, io, st, of, qkv, a, b, o, pages, status, s);
+  }
+}
+
+gdn_status rule_entry(int mode, const gdn_dims* dims, const gdn_batch* batch,
+                      const gdn_params* params, const void* qkv, const void* a, const void* b,
+                      void* o, void* pages, int32_t* status, gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, mode == 0)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  if (mode == 1 && dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!qkv || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  SlotGeom SG{};
+  if (rule(mode, G, B, P, SG, dims, qkv, a, b, o, pages, status, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t gdn_abi_version(void) { return (1 << 16) | 0; }
+
+gdn_status gdn_page_layout(const gdn_dims* dims, gdn_page_layout_t* out) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if (!out) return GDN_ERR_INVALID_ARG;
+  layout(dims, out, nullptr);
+  return GDN_OK;
+}
+
+gdn_status gdn_slot_layout(const gdn_dims* dims, gdn_slot_layout_t* out) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if (!out) return GDN_ERR_INVALID_ARG;
+  slot_layout(dims, out);
+  return GDN_OK;
+}
+
+gdn_status gdn_conv(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                    const void* x, const void* conv_w, void* y, int32_t y_dtype, void* pages,
+                    int32_t* status, gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, true)) != GDN_OK) return e;
+  if ((e = check_params(params, false)) != GDN_OK) return e;
+  if (!valid_dtype(y_dtype)) return GDN_ERR_INVALID_ARG;
+  if (y_dtype != GDN_F32 && y_dtype != dims->io_dtype) return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages || !conv_w) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!x || !y)) return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  if (launch_conv(G, B, P, dims->io_dtype == GDN_BF16, y_dtype == GDN_F32, x, conv_w, y, pages,
+                  status, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
+gdn_status gdn_seq(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                   const void* qkv, const void* a, const void* b, void* o, void* pages,
+                   int32_t* status, gdn_stream_t stream) {
+  return rule_entry(0, dims, batch, params, qkv, a, b, o, pages, status, stream);
+}
+
+gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                           const void* qkv, const void* a, const void* b, void* o, void* pages,
+                           int32_t* status, gdn_stream_t stream) {
+  return rule_entry(1, dims, batch, params, qkv, a, b, o, pages, status, stream);
+}
+
+gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                          const void* x, const void* conv_w, void* y, const void* a, const void* b,
+                          void* o, void* slots, int32_t* status, gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, false)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !slots || !conv_w) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!x || !y || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  gdn_slot_layout_t SL;
+  slot_layout(dims, &SL);
+  SlotGeom SG{SL.pool_bytes, SL.slot_bytes, SL.state_offset, SL.window_offset};
+  const cudaStream_t s = (cudaStream_t)stream;
+  const int io = dims->io_dtype == GDN_BF16;
+  if (launch_conv_slots(G, B, P, SG, io, x, conv_w, y, slots, status, s) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  if (rule(2, G, B, P, SG, dims, y, a, b, o, slots, status, s) != cudaSuccess) return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
+size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims, const gdn_batch* batch) {
+  if (check_dims(dims) != GDN_OK || check_batch(batch, true) != GDN_OK) return 0;
+  return 0;
+}
+
+gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                             const void* qkv, const void* a, const void* b, void* o, void* pages,
+                             void* workspace, size_t workspace_bytes, int32_t* status,
+                             gdn_stream_t stream) {
+  (void)qkv; (void)a; (void)b; (void)o; (void)pages; (void)workspace; (void)workspace_bytes;
+  (void)status; (void)stream;
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, true)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  return GDN_ERR_UNSUPPORTED;
+}
+
+const char* gdn_strerror(int32_t s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument (null pointer, negative count or bad enum)";
+    case GDN_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case GDN_ERR_LAUNCH: return "kernel launch failed";
+    case GDN_ERR_WORKSPACE: return "workspace too small";
+    case GDN_ERR_NO_DEVICE: return "no usable device";
+    case GDN_DEV_BAD_PAGE: return "device: page index out of range";
+    case GDN_DEV_BAD_ROWS: return "device: row range out of bounds";
+    case GDN_DEV_BAD_ACCEPTED: return "device: accepted count outside the record width";
+    case GDN_DEV_STALE_STEP: return "device: page step parity does not match the request";
+    case GDN_DEV_TOO_MANY_CANDIDATES: return "device: more candidate rows than max_candidates";
+    case GDN_DEV_RECORD_OPEN: return "device: plain rows on a page whose spec record is open";
+    case GDN_DEV_BAD_FLAG: return "device: corrupt page flag word (or FRESH with SPEC)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

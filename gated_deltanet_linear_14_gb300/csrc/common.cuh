@@ -1,0 +1,249 @@
+// Device-side helpers shared by the GDN kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+typedef __nv_bfloat16 bf16;
+
+// ------------------------------------------------------------------ layout
+
+// Everything a kernel needs to address one layer's rows and pages.
+struct Geom {
+  int Hk, Hv, Dk, Dv, W, Kc;
+  int C;              // 2*Hk*Dk + Hv*Dv
+  int rec_row;        // record row stride in elements (16-byte padded)
+  size_t page_bytes, window_off, state_off, record_off, flag_off;
+};
+
+struct Batch {
+  int R, num_rows, max_rows, num_pages;
+  const int32_t* row_start;
+  const int32_t* row_len;
+  const int32_t* page;
+  const uint32_t* flags;
+  const int32_t* n_accepted;
+  const int32_t* order;
+};
+
+// Slot pool geometry of the slot-per-candidate layout.
+struct SlotGeom {
+  size_t pool_bytes, slot_bytes, state_off, window_off;
+};
+
+struct Params {
+  const float* A_log;
+  const float* dt_bias;
+  const float* conv_bias;
+  float scale;
+  float eps;
+  int gate_mode;
+};
+
+// Flag word: bit 0 live slot, bit 1 parity, bits 2..7 width, 8..31 counter.
+__device__ __forceinline__ int flag_live(uint32_t f) { return (int)(f & 1u); }
+__device__ __forceinline__ int flag_parity(uint32_t f) { return (int)((f >> 1) & 1u); }
+__device__ __forceinline__ int flag_width(uint32_t f) { return (int)((f >> 2) & 63u); }
+__device__ __forceinline__ uint32_t make_flag(int live, int parity, int width) {
+  return (uint32_t)live | ((uint32_t)parity << 1) | ((uint32_t)width << 2);
+}
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+// Per-request facts every kernel checks the same way.
+struct Req {
+  int r, start, len, page;
+  uint32_t flags;
+  bool fresh, spec;
+  int err;  // 0 or a gdn_status device code
+};
+
+__device__ __forceinline__ Req load_req(const Batch& B, int slot) {
+  Req q;
+  q.r = B.order ? B.order[slot] : slot;
+  q.err = 0;
+  if (q.r < 0 || q.r >= B.R) {
+    q.err = GDN_DEV_BAD_ROWS;
+    q.r = 0;
+    q.start = q.len = q.page = 0;
+    q.flags = 0;
+    q.fresh = q.spec = false;
+    return q;
+  }
+  q.start = B.row_start[q.r];
+  q.len = B.row_len[q.r];
+  q.page = B.page[q.r];
+  q.flags = B.flags[q.r];
+  q.fresh = (q.flags & GDN_REQ_FRESH) != 0;
+  q.spec = (q.flags & GDN_REQ_SPEC) != 0;
+  if (q.page < 0 || q.page >= B.num_pages) q.err = GDN_DEV_BAD_PAGE;
+  else if (q.start < 0 || q.len < 0 || q.len > B.max_rows ||
+           (long long)q.start + q.len > (long long)B.num_rows)
+    q.err = GDN_DEV_BAD_ROWS;
+  return q;
+}
+
+__device__ __forceinline__ char* page_ptr(const Geom& G, void* pages, int p) {
+  return reinterpret_cast<char*>(pages) + (size_t)p * G.page_bytes;
+}
+
+// Speculative request facts read from the page flag (validated).
+struct SpecState {
+  int live, parity, width, accepted;  // accepted = -1 when nothing to replay
+  int err;
+};
+
+__device__ __forceinline__ SpecState spec_state(const Geom& G, const Batch& B, const Req& q,
+                                                uint32_t flag) {
+  SpecState s;
+  s.live = flag_live(flag);
+  s.parity = flag_parity(flag);
+  s.width = flag_width(flag);
+  s.accepted = -1;
+  s.err = 0;
+  const int want = (q.flags & GDN_REQ_PARITY) ? 1 : 0;
+  if (s.width > G.Kc) s.err = GDN_DEV_BAD_FLAG;
+  else if (s.parity != want) s.err = GDN_DEV_STALE_STEP;
+  else if (q.len > G.Kc) s.err = GDN_DEV_TOO_MANY_CANDIDATES;
+  else if (s.width > 0) {
+    const int a = B.n_accepted ? B.n_accepted[q.r] : -1;
+    if (a < 0 || a >= s.width) s.err = GDN_DEV_BAD_ACCEPTED;
+    else s.accepted = a;
+  }
+  return s;
+}
+
+// ------------------------------------------------------------ dtype access
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(bf16 x) { return __bfloat162float(x); }
+
+template <class T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// Load N consecutive elements (N * sizeof(T) a multiple of 8 bytes, pointer
+// aligned to min(16, N * sizeof(T))) into fp32 registers.
+template <class T, int N>
+__device__ __forceinline__ void load_f(const T* p, float* out) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  static_assert(BYTES % 8 == 0, "vector load of at least 8 bytes");
+  if constexpr (BYTES >= 16) {
+#pragma unroll
+    for (int v = 0; v < BYTES / 16; ++v) {
+      uint4 u = reinterpret_cast<const uint4*>(p)[v];
+      const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+      for (int i = 0; i < 16 / (int)sizeof(T); ++i) out[v * (16 / sizeof(T)) + i] = to_f(e[i]);
+    }
+  } else {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    const T* e = reinterpret_cast<const T*>(&u);
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = to_f(e[i]);
+  }
+}
+
+template <class T, int N>
+__device__ __forceinline__ void store_f(T* p, const float* in) {
+  constexpr int BYTES = N * (int)sizeof(T);
+  static_assert(BYTES % 8 == 0, "vector store of at least 8 bytes");
+  if constexpr (BYTES >= 16) {
+#pragma unroll
+    for (int v = 0; v < BYTES / 16; ++v) {
+      uint4 u;
+      T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+      for (int i = 0; i < 16 / (int)sizeof(T); ++i) e[i] = from_f<T>(in[v * (16 / sizeof(T)) + i]);
+      reinterpret_cast<uint4*>(p)[v] = u;
+    }
+  } else {
+    uint2 u;
+    T* e = reinterpret_cast<T*>(&u);
+#pragma unroll
+    for (int i = 0; i < N; ++i) e[i] = from_f<T>(in[i]);
+    *reinterpret_cast<uint2*>(p) = u;
+  }
+}
+
+// Round-trip through the storage type (what a store followed by a load
+// returns).
+template <class T>
+__device__ __forceinline__ float through(float x) { return to_f(from_f<T>(x)); }
+
+// ----------------------------------------------------------- own exp, SiLU
+//
+// The conv's SiLU must be reproducible bit for bit by a plain CPU program, so
+// it does not use the CUDA math library. exp is computed with Cody and
+// Waite's argument reduction (Cody & Waite, "Software Manual for the
+// Elementary Functions", 1980): x = n ln2 + r, n = round-to-even(x log2 e),
+// ln2 split into a 12-bit-trimmed high part and a low correction; e^r from
+// the Taylor series through r^7 (coefficients 1/k!), Horner's rule with
+// fused multiply-adds; scaling by 2^n as two exact power-of-two factors.
+// x >= 88.5 gives +inf and x <= -87 gives 0.
+__host__ __device__ constexpr float recip_factorial(int k) {
+  double f = 1.0;
+  for (int i = 2; i <= k; ++i) f *= i;
+  return (float)(1.0 / f);
+}
+
+// ln 2 = 0.693147180559945309417...; its float value is 0x3F317218. The high
+// part keeps that pattern with the low 12 mantissa bits cleared (0x3F317000),
+// the low part is ln 2 minus the high part, rounded to float.
+__device__ __forceinline__ float own_exp(float x) {
+  constexpr double kLn2 = 0.693147180559945309417232121458176568;
+  const float log2e = (float)(1.0 / kLn2);
+  const float ln2_hi = __uint_as_float(0x3F317000u);
+  const float ln2_lo = (float)(kLn2 - (double)0.693115234375);  // 0x3F317000 == 0.693115234375
+  if (x >= 88.5f) return __int_as_float(0x7f800000);
+  if (x <= -87.0f) return 0.0f;
+  const float t = __fmul_rn(x, log2e);
+  const float n = rintf(t);
+  float r = __fmaf_rn(-n, ln2_hi, x);
+  r = __fmaf_rn(-n, ln2_lo, r);
+  float p = recip_factorial(7);
+  p = __fmaf_rn(p, r, recip_factorial(6));
+  p = __fmaf_rn(p, r, recip_factorial(5));
+  p = __fmaf_rn(p, r, recip_factorial(4));
+  p = __fmaf_rn(p, r, recip_factorial(3));
+  p = __fmaf_rn(p, r, recip_factorial(2));
+  p = __fmaf_rn(p, r, recip_factorial(1));
+  p = __fmaf_rn(p, r, recip_factorial(0));
+  const int ni = (int)n;
+  const int h1 = ni / 2;
+  const int h2 = ni - h1;
+  const float s1 = __int_as_float((h1 + 127) << 23);
+  const float s2 = __int_as_float((h2 + 127) << 23);
+  return __fmul_rn(__fmul_rn(p, s1), s2);
+}
+
+__device__ __forceinline__ float own_silu(float z) {
+  const float e = own_exp(-z);
+  return __fdiv_rn(z, __fadd_rn(1.0f, e));
+}
+
+// ----------------------------------------------------------------- gates
+
+// g (log decay) and beta from the raw inputs, fp32, CUDA math library.
+__device__ __forceinline__ void gates(const Params& P, int h, float a_in, float b_in,
+                                      float& alpha, float& beta) {
+  if (P.gate_mode == 1) {
+    alpha = expf(a_in);
+    beta = b_in;
+    return;
+  }
+  const float x = __fadd_rn(a_in, P.dt_bias[h]);
+  const float sp = (x > 20.0f) ? x : log1pf(expf(x));
+  const float g = -__fmul_rn(expf(P.A_log[h]), sp);
+  alpha = expf(g);
+  beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
+}
+
+}  // namespace gdn

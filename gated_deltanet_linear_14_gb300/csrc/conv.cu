@@ -1,0 +1,224 @@
+// Causal depthwise conv + SiLU over the step's packed rows (sm_103a).
+//
+// r9700-stack v0.2.3, section 1 (r9k_gdn_conv: one launch over the batch's
+// own rows); v0.2.4, "A defect found and fixed before the tag" (the window
+// rolls by the candidate count read from the record); vllm.cpp PR #155,
+// "What changed" (the width-4 specialisation, one channel group per thread).
+//
+// Design (HBM-bound streaming):
+//   * a thread owns one 16-byte vector of channels (8 bf16 or 4 fp32) and a
+//     tile of TR consecutive rows of one request; the W-1 previous columns
+//     live in registers and slide down the tile, so every input element is
+//     read once (plus W-1 halo rows per tile);
+//   * grid = (channel tiles, row tiles, requests); empty row tiles exit;
+//   * the conv window of a page is read ONLY by row tile 0 of the request,
+//     and that same thread also writes the new window (from its registers
+//     and the read-only input rows). No other block touches the window, so a
+//     long request split over many blocks cannot race on it (the hazard
+//     vllm.cpp's exact-chunk conv has, where one block reads the initial
+//     window and another writes the final one).
+//   * accumulation is fp32 in a fixed order: bias (or 0), then taps
+//     j = 0..W-1 oldest first, each a fused multiply-add; SiLU uses the
+//     library's own exp. The CPU fp32 conv reproduces this bit for bit.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+
+constexpr int kConvThreads = 128;
+constexpr int kConvRows = 32;  // rows per tile (>= W-1)
+
+template <class IO, class YT, int W, bool SLOTS>
+__global__ void __launch_bounds__(kConvThreads)
+conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
+            const IO* __restrict__ w, YT* __restrict__ y, void* pages, int32_t* status) {
+  constexpr int V = 16 / (int)sizeof(IO);  // channels per thread
+  constexpr int H = W - 1;
+  const bool reporter = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
+
+  Batch Bi = B;
+  Bi.order = nullptr;  // the conv has no scheduling order
+  const Req q = load_req(Bi, blockIdx.z);
+  if (q.err) {
+    if (reporter) report(status, q.err);
+    return;
+  }
+  const int t0 = blockIdx.y * kConvRows;
+  if (t0 > 0 && t0 >= q.len) return;
+
+  char* pg = nullptr;
+  const IO* hist_src = nullptr;  // history column 0 (oldest), or null for zeros
+  IO* win = nullptr;
+  IO* rec_out = nullptr;         // record slot receiving conv'd candidate rows
+  char* pool = nullptr;
+  if constexpr (!SLOTS) {
+    pg = page_ptr(G, pages, q.page);
+    win = reinterpret_cast<IO*>(pg + G.window_off);
+    const uint32_t flag = *reinterpret_cast<const uint32_t*>(pg + G.flag_off);
+    if (q.spec) {
+      SpecState ss = spec_state(G, B, q, flag);
+      if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
+      if (ss.err) {
+        if (reporter) report(status, ss.err);
+        return;
+      }
+      const int base = (ss.width > 0) ? ss.accepted + 1 : 0;
+      hist_src = win + (size_t)base * G.C;
+      rec_out = reinterpret_cast<IO*>(pg + G.record_off) + (size_t)(1 - ss.live) * G.Kc * G.rec_row;
+    } else if (!q.fresh) {
+      if (flag_width(flag) != 0) {
+        if (reporter) report(status, GDN_DEV_RECORD_OPEN);
+        return;
+      }
+      hist_src = win;
+    }
+  } else {
+    const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
+    if (src < 0 || src >= G.Kc) {
+      if (reporter) report(status, GDN_DEV_BAD_ACCEPTED);
+      return;
+    }
+    if (q.len > G.Kc) {
+      if (reporter) report(status, GDN_DEV_TOO_MANY_CANDIDATES);
+      return;
+    }
+    pool = reinterpret_cast<char*>(pages) + (size_t)q.page * SG.pool_bytes;
+    hist_src = reinterpret_cast<const IO*>(pool + (size_t)src * SG.slot_bytes + SG.window_off);
+  }
+
+  const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
+  if (c0 >= G.C) return;
+
+  // taps and bias
+  float wt[W][V];
+  {
+    float tmp[W * V];
+#pragma unroll
+    for (int i = 0; i < W * V; i += 16 / (int)sizeof(IO)) load_f<IO, 16 / sizeof(IO)>(w + (size_t)c0 * W + i, tmp + i);
+#pragma unroll
+    for (int v = 0; v < V; ++v)
+#pragma unroll
+      for (int j = 0; j < W; ++j) wt[j][v] = tmp[v * W + j];
+  }
+  float bias[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) bias[v] = P.conv_bias ? P.conv_bias[c0 + v] : 0.0f;
+
+  // history for the tile's first row: sequence positions t0-H .. t0-1
+  float h[H][V];
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const int pos = t0 - H + j;
+    if (pos >= 0) {
+      load_f<IO, V>(x + (size_t)(q.start + pos) * G.C + c0, h[j]);
+    } else if (hist_src) {
+      load_f<IO, V>(hist_src + (size_t)(H + pos) * G.C + c0, h[j]);
+    } else {
+#pragma unroll
+      for (int v = 0; v < V; ++v) h[j][v] = 0.0f;
+    }
+  }
+
+  const int t_end = min(q.len, t0 + kConvRows);
+  for (int t = t0; t < t_end; ++t) {
+    float xv[V];
+    load_f<IO, V>(x + (size_t)(q.start + t) * G.C + c0, xv);
+    float yv[V];
+#pragma unroll
+    for (int v = 0; v < V; ++v) {
+      float acc = bias[v];
+#pragma unroll
+      for (int j = 0; j < H; ++j) acc = __fmaf_rn(wt[j][v], h[j][v], acc);
+      acc = __fmaf_rn(wt[H][v], xv[v], acc);
+      yv[v] = own_silu(acc);
+    }
+    store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
+#pragma unroll
+    for (int j = 0; j < H - 1; ++j)
+#pragma unroll
+      for (int v = 0; v < V; ++v) h[j][v] = h[j + 1][v];
+#pragma unroll
+    for (int v = 0; v < V; ++v) h[H - 1][v] = xv[v];
+    if constexpr (!SLOTS) {
+      if (rec_out) store_f<IO, V>(rec_out + (size_t)t * G.rec_row + c0, yv);
+    } else {
+      // window after candidate t goes to slot t
+      IO* wdst = reinterpret_cast<IO*>(pool + (size_t)t * SG.slot_bytes + SG.window_off);
+#pragma unroll
+      for (int j = 0; j < H; ++j) store_f<IO, V>(wdst + (size_t)j * G.C + c0, h[j]);
+    }
+  }
+
+  if constexpr (!SLOTS) {
+    if (blockIdx.y != 0) return;
+    // The window channels [c0, c0+V) are read and written only by this
+    // thread, so the initial history can be read again here.
+    if (q.spec) {
+      // columns 0..H-1 keep the history this step started from; the raw
+      // candidates follow, so the next step can roll by its accepted count
+      float hw[H][V];
+#pragma unroll
+      for (int j = 0; j < H; ++j) load_f<IO, V>(hist_src + (size_t)j * G.C + c0, hw[j]);
+#pragma unroll
+      for (int j = 0; j < H; ++j) store_f<IO, V>(win + (size_t)j * G.C + c0, hw[j]);
+      for (int t = 0; t < q.len; ++t) {
+        float xv[V];
+        load_f<IO, V>(x + (size_t)(q.start + t) * G.C + c0, xv);
+        store_f<IO, V>(win + (size_t)(H + t) * G.C + c0, xv);
+      }
+    } else {
+      // last H columns of [history; rows], oldest first. Column j comes from
+      // sequence position len-H+j, which is a history column when negative;
+      // for j < H those history columns sit at index >= j, so reading them
+      // in increasing j before overwriting column j is safe.
+#pragma unroll
+      for (int j = 0; j < H; ++j) {
+        const int pos = q.len - H + j;
+        float col[V];
+        if (pos >= 0) {
+          load_f<IO, V>(x + (size_t)(q.start + pos) * G.C + c0, col);
+        } else if (hist_src) {
+          load_f<IO, V>(hist_src + (size_t)(H + pos) * G.C + c0, col);
+        } else {
+#pragma unroll
+          for (int v = 0; v < V; ++v) col[v] = 0.0f;
+        }
+        store_f<IO, V>(win + (size_t)j * G.C + c0, col);
+      }
+    }
+  }
+}
+
+template <class IO, class YT, bool SLOTS>
+static cudaError_t launch_conv_t(const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
+                                 const void* x, const void* w, void* y, void* pages,
+                                 int32_t* status, cudaStream_t stream) {
+  constexpr int V = 16 / (int)sizeof(IO);
+  const int ctiles = (G.C + kConvThreads * V - 1) / (kConvThreads * V);
+  const int rtiles = B.max_rows > 0 ? (B.max_rows + kConvRows - 1) / kConvRows : 1;
+  dim3 grid(ctiles, rtiles, B.R);
+  conv_kernel<IO, YT, 4, SLOTS><<<grid, kConvThreads, 0, stream>>>(
+      G, B, P, SG, static_cast<const IO*>(x), static_cast<const IO*>(w), static_cast<YT*>(y),
+      pages, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv(const Geom& G, const Batch& B, const Params& P, int io_bf16, int y_f32,
+                        const void* x, const void* w, void* y, void* pages, int32_t* status,
+                        cudaStream_t stream) {
+  SlotGeom SG{};
+  if (io_bf16) {
+    if (y_f32) return launch_conv_t<bf16, float, false>(G, B, P, SG, x, w, y, pages, status, stream);
+    return launch_conv_t<bf16, bf16, false>(G, B, P, SG, x, w, y, pages, status, stream);
+  }
+  return launch_conv_t<float, float, false>(G, B, P, SG, x, w, y, pages, status, stream);
+}
+
+cudaError_t launch_conv_slots(const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
+                              int io_bf16, const void* x, const void* w, void* y, void* slots,
+                              int32_t* status, cudaStream_t stream) {
+  if (io_bf16) return launch_conv_t<bf16, bf16, true>(G, B, P, SG, x, w, y, slots, status, stream);
+  return launch_conv_t<float, float, true>(G, B, P, SG, x, w, y, slots, status, stream);
+}
+
+}  // namespace gdn

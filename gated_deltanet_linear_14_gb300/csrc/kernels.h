@@ -1,0 +1,36 @@
+// Launchers implemented by the kernel translation units (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace gdn {
+
+cudaError_t launch_conv(const Geom& G, const Batch& B, const Params& P, int io_bf16, int y_f32,
+                        const void* x, const void* w, void* y, void* pages, int32_t* status,
+                        cudaStream_t stream);
+
+cudaError_t launch_conv_slots(const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
+                              int io_bf16, const void* x, const void* w, void* y, void* slots,
+                              int32_t* status, cudaStream_t stream);
+
+// mode: 0 = token-by-token rule (plain requests), 1 = one-page verify (SPEC
+// requests), 2 = slot-per-candidate layout (every request).
+cudaError_t launch_rule(int mode, const Geom& G, const Batch& B, const Params& P,
+                        const SlotGeom& SG, int io_bf16, int state_bf16, int out_f32,
+                        const void* qkv, const void* a, const void* b, void* o, void* pages,
+                        int32_t* status, cudaStream_t stream);
+
+// per head dimension (one translation unit each)
+cudaError_t launch_rule_d32(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
+                            int, int, int, const void*, const void*, const void*, void*, void*,
+                            int32_t*, cudaStream_t);
+cudaError_t launch_rule_d64(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
+                            int, int, int, const void*, const void*, const void*, void*, void*,
+                            int32_t*, cudaStream_t);
+cudaError_t launch_rule_d128(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
+                             int, int, int, const void*, const void*, const void*, void*, void*,
+                             int32_t*, cudaStream_t);
+
+}  // namespace gdn

@@ -208,11 +208,17 @@ class SlotSim:
     the last accepted one).
 
     ``state_round`` models a bf16 state page: every stored slot is rounded.
+    ``row_store`` models the storage dtype of conv'd rows: with it set, the
+    conv runs in the fp32 mirror (``conv_f32``) and its output is passed
+    through ``row_store`` (e.g. ``round_bf16``) before the recurrence, which
+    is where the method keeps conv'd rows in the io dtype (the record holds
+    them so; the r9700-stack v0.2.4 notes, "What it does"). Without it the
+    conv is fp64 and unrounded.
     """
 
     def __init__(self, R, Hk, Hv, Dk, Dv, W, conv_w, A_log, dt_bias, S0=None,
                  hist0=None, scale=None, eps=1e-6, gate_mode=0, conv_bias=None,
-                 state_round=None, threads=None):
+                 state_round=None, row_store=None, threads=None):
         self.R, self.Hk, self.Hv, self.Dk, self.Dv, self.W = R, Hk, Hv, Dk, Dv, W
         self.C = 2 * Hk * Dk + Hv * Dv
         self.conv_w = np.asarray(conv_w, np.float64)
@@ -221,6 +227,7 @@ class SlotSim:
         self.dt_bias = np.asarray(dt_bias, np.float64)
         self.scale, self.eps, self.gate_mode = scale, eps, gate_mode
         self.state_round = state_round
+        self.row_store = row_store
         self.threads = threads
         S0 = np.zeros((R, Hv, Dk, Dv)) if S0 is None else np.asarray(S0, np.float64)
         hist0 = (np.zeros((R, W - 1, self.C)) if hist0 is None
@@ -255,7 +262,12 @@ class SlotSim:
         for i in range(n):
             # candidate i of every request: one row each, windows and states
             # carried from candidate i-1 (or the resumed slot)
-            y, hist = conv_f64(x[:, i], hist, self.conv_w, one, ones, bias=self.conv_bias)
+            if self.row_store is None:
+                y, hist = conv_f64(x[:, i], hist, self.conv_w, one, ones, bias=self.conv_bias)
+            else:
+                y, hist = conv_f32(x[:, i], hist, self.conv_w, one, ones, bias=self.conv_bias)
+                y = self.row_store(y)
+                hist = hist.astype(np.float64)
             o, S = gdn_f64(y, a[:, i], b[:, i], self.A_log, self.dt_bias, one, ones,
                            self.Hk, self.Hv, self.Dk, self.Dv, S0=S, scale=self.scale,
                            eps=self.eps, gate_mode=self.gate_mode, threads=self.threads)

@@ -1,0 +1,204 @@
+"""gdn_seq against the fp64 token-by-token oracle.
+
+The bar (from the method's statement): relative error <= 1e-4 per tensor
+(||x - ref||_2 / ||ref||_2) with an fp32 state and fp32 outputs. Both sides
+read the same rows: conv'd q/k/v drawn directly as N(0,1) in the io dtype
+(kernel-only parity), or, end to end, the conv's io-dtype rows, which the
+oracle obtains from its own fp32 conv mirror rounded to the io dtype.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_14_gb300 as gdn
+import oracle
+import synth
+from tests.gpu_util import Layer, bits, f64, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+def oracle_seq(d, qkv, a, b, start, ln, S0, gate_mode=0):
+    sh = d["shapes"]
+    return oracle.gdn_f64(qkv, a, b, d["A_log"], d["dt_bias"], start, ln, sh.Hk, sh.Hv, sh.Dk,
+                          sh.Dv, S0=S0, gate_mode=gate_mode)
+
+
+def gpu_seq(d, rows, start, ln, S0, fresh, state=gdn.GDN_F32, out=gdn.GDN_F32, order=None,
+            gate_mode=0, calls=None):
+    sh, io = d["shapes"], d["io"]
+    R = len(ln)
+    L = Layer(sh, io, d["A_log"], d["dt_bias"], d["conv_w"], state=state, out=out, num_pages=R,
+              gate_mode=gate_mode)
+    L.seed(range(R), S0=S0)
+    flags = np.where(np.asarray(fresh), gdn.GDN_REQ_FRESH, 0)
+    qkv, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    B = L.batch(start, ln, flags=flags, order=order)
+    o = L.seq(B, qkv, a, b)
+    L.ok()
+    S = torch.stack([L.pool.state_math(r) for r in range(R)])
+    return o, S, L
+
+
+def check(o, S, o_ref, S_ref, tol=TOL):
+    eo, es = rel(f64(o), o_ref), rel(f64(S), S_ref)
+    assert eo <= tol and es <= tol, (eo, es)
+    return eo, es
+
+
+def test_tiny_fp32_rows():
+    d = synth.tiny()
+    rows = {"x": d["x"], "a": d["a"], "b": d["b"]}
+    o, S, _ = gpu_seq(d, rows, d["row_start"], d["row_len"], d["S0"], d["fresh"])
+    o_ref, S_ref = oracle_seq(d, d["x"].value, d["a"].value, d["b"].value, d["row_start"],
+                              d["row_len"], d["S0"])
+    check(o, S, o_ref, S_ref)
+
+
+def test_decode_batch_full_size():
+    """64 requests x 1 token at 16/32 heads, Dk = Dv = 128, fp32 state."""
+    d = synth.decode()
+    rows = {"x": d["x"], "a": d["a"], "b": d["b"]}
+    o, S, _ = gpu_seq(d, rows, d["row_start"], d["row_len"], d["S0"], d["fresh"])
+    o_ref, S_ref = oracle_seq(d, d["x"].value, d["a"].value, d["b"].value, d["row_start"],
+                              d["row_len"], d["S0"])
+    check(o, S, o_ref, S_ref)
+    for r in (0, 17, 63):  # per request too
+        assert rel(f64(o[r]), o_ref[r]) <= TOL
+
+
+@pytest.mark.parametrize("shape", [(16, 32, 128), (4, 8, 64), (2, 2, 32), (2, 6, 64)])
+def test_varlen_prefills_shuffled_order(shape):
+    Hk, Hv, D = shape
+    sh = synth.Shapes(Hk=Hk, Hv=Hv, Dk=D, Dv=D)
+    rng = np.random.default_rng(7 + D)
+    lengths = [45, 1, 400, 7, 64, 65, 0, 130]
+    R = len(lengths)
+    order = rng.permutation(R)
+    start, ln, T = synth.pack(lengths, order)
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    S0 = synth.state(rng, R, sh)
+    fresh = np.array([i % 3 == 0 for i in range(R)])
+    S0[fresh] = 0.0
+    longest_first = np.argsort(-np.asarray(lengths), kind="stable")
+    o, S, _ = gpu_seq(d, rows, start, ln, S0, fresh, order=longest_first)
+    o_ref, S_ref = oracle_seq(d, rows["x"].value, rows["a"].value, rows["b"].value, start, ln, S0)
+    check(o, S, o_ref, S_ref)
+    for r in range(R):
+        if ln[r]:
+            sl = slice(start[r], start[r] + ln[r])
+            assert rel(f64(o[sl]), o_ref[sl]) <= TOL
+
+
+def test_split_and_carry_and_decode_kernel_bitwise():
+    """T rows in one call == two calls with the state carried == T one-row
+    calls (the decode path), bit for bit, outputs and state."""
+    d = synth.decode(R=2)
+    sh = d["shapes"]
+    rng = np.random.default_rng(21)
+    T = 37
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    qkv, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    S0 = d["S0"][:1]
+
+    def run(splits):
+        L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], num_pages=1)
+        L.seed([0], S0=S0)
+        outs = []
+        for s0, s1 in zip(splits[:-1], splits[1:]):
+            B = L.batch([s0], [s1 - s0], num_rows=T)
+            outs.append(L.seq(B, qkv, a, b)[s0:s1])
+            L.ok()
+        return torch.cat(outs), L.pool.state(0).clone()
+
+    o1, S1 = run([0, T])
+    o2, S2 = run([0, 11, T])
+    o3, S3 = run(list(range(T + 1)))
+    assert np.array_equal(bits(o1), bits(o2)) and np.array_equal(bits(S1), bits(S2))
+    assert np.array_equal(bits(o1), bits(o3)) and np.array_equal(bits(S1), bits(S3))
+    o_ref, S_ref = oracle.gdn_f64(rows["x"].value, rows["a"].value, rows["b"].value, d["A_log"],
+                                  d["dt_bias"], [0], [T], sh.Hk, sh.Hv, sh.Dk, sh.Dv, S0=S0)
+    assert rel(f64(o1), o_ref) <= TOL
+    assert rel(f64(S1.transpose(-1, -2)), S_ref[0]) <= TOL
+
+
+def test_bf16_outputs_within_one_ulp_of_rounded_oracle():
+    d = synth.decode()
+    rows = {"x": d["x"], "a": d["a"], "b": d["b"]}
+    o, S, _ = gpu_seq(d, rows, d["row_start"], d["row_len"], d["S0"], d["fresh"],
+                      out=gdn.GDN_BF16)
+    o_ref, _ = oracle_seq(d, d["x"].value, d["a"].value, d["b"].value, d["row_start"],
+                          d["row_len"], d["S0"])
+    def ordered(b):  # bf16 bit patterns -> integers in value order
+        b = np.asarray(b).astype(np.int32) & 0xFFFF
+        return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    ref_bits = ordered(synth.bf16_bits(o_ref.astype(np.float32)))
+    got_bits = ordered(bits(o))
+    # same sign, at most one unit in the last bf16 place apart
+    assert np.all(np.abs(got_bits - ref_bits) <= 1)
+    flips = np.mean(got_bits != ref_bits)
+    assert flips < 0.05, flips
+
+
+def test_bf16_state_rounds_once_per_call():
+    """A bf16 page is read to fp32, advanced, and rounded once when stored:
+    the result is the oracle's state rounded to bf16, up to the rounding of
+    an fp32 value that is itself within 1e-4."""
+    d = synth.decode(R=8)
+    rows = {"x": d["x"], "a": d["a"], "b": d["b"]}
+    S0 = oracle.round_bf16(d["S0"]).astype(np.float32)
+    o, S, _ = gpu_seq(d, rows, d["row_start"], d["row_len"], S0, d["fresh"], state=gdn.GDN_BF16)
+    o_ref, S_ref = oracle_seq(d, d["x"].value, d["a"].value, d["b"].value, d["row_start"],
+                              d["row_len"], S0)
+    assert rel(f64(o), o_ref) <= TOL                 # outputs come from fp32 registers
+    assert rel(f64(S), oracle.round_bf16(S_ref)) <= 2e-3  # at most a bf16 flip here and there
+    assert rel(f64(S), S_ref) <= 4e-3                # bf16 storage: 2^-9 relative
+
+
+def test_gate_mode_precomputed_g_beta():
+    d = synth.decode(R=4)
+    rng = np.random.default_rng(9)
+    sh = d["shapes"]
+    T = 20
+    start, ln, _ = synth.pack([5, 5, 5, 5])
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    g = synth.as_io(-np.abs(rng.standard_normal((T, sh.Hv))) * 0.7, synth.BF16)
+    beta = synth.as_io(rng.uniform(0, 1, (T, sh.Hv)), synth.BF16)
+    rows["a"], rows["b"] = g, beta
+    o, S, _ = gpu_seq(d, rows, start, ln, d["S0"][:4], np.zeros(4, bool), gate_mode=1)
+    o_ref, S_ref = oracle_seq(d, rows["x"].value, g.value, beta.value, start, ln, d["S0"][:4],
+                              gate_mode=1)
+    check(o, S, o_ref, S_ref)
+
+
+def test_batch_composition_and_reruns_are_bitwise_identical():
+    """A request's result does not depend on the rest of the batch or on the
+    run; identical requests in lockstep equal the request alone."""
+    d = synth.decode(R=1)
+    sh = d["shapes"]
+    rng = np.random.default_rng(33)
+    T1 = 9
+    rows1 = synth.rows(rng, T1, sh, synth.BF16)
+    S01 = d["S0"][:1]
+    o_alone, S_alone, _ = gpu_seq(d, rows1, [0], [T1], S01, [False])
+    # four copies of it among other requests, packed in a scrambled order
+    others = synth.rows(rng, 30, sh, synth.BF16)
+    X = np.concatenate([others["x"].value[:10], rows1["x"].value, rows1["x"].value,
+                        others["x"].value[10:], rows1["x"].value, rows1["x"].value])
+    A = np.concatenate([others["a"].value[:10], rows1["a"].value, rows1["a"].value,
+                        others["a"].value[10:], rows1["a"].value, rows1["a"].value])
+    Bv = np.concatenate([others["b"].value[:10], rows1["b"].value, rows1["b"].value,
+                         others["b"].value[10:], rows1["b"].value, rows1["b"].value])
+    big = {k: synth.as_io(v, synth.BF16) for k, v in (("x", X), ("a", A), ("b", Bv))}
+    start = [10, 10 + T1, 40, 40 + T1, 0, 28]
+    ln = [T1, T1, T1, T1, 10, 2]
+    S0 = np.concatenate([S01] * 4 + [d["S0"][:1] * 2, d["S0"][:1] * 3])
+    for rep in range(2):
+        o, S, _ = gpu_seq(d, big, start, ln, S0, [False] * 6, order=[5, 3, 0, 4, 1, 2])
+        for r in range(4):
+            assert np.array_equal(bits(o[start[r]:start[r] + T1]), bits(o_alone))
+            assert np.array_equal(bits(S[r]), bits(S_alone[0]))

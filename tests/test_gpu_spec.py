@@ -1,0 +1,318 @@
+"""Speculative-decode verify with one page per request.
+
+* bit-identical to the slot-per-candidate layout (gdn_spec_slots) under
+  random acceptance, over 20 steps, with fp32 and bf16 state pages;
+* within 1e-4 of the fp64 slot simulation of the oracle (fp32 state);
+* identical requests in lockstep equal the same request alone;
+* commit closes the record and plain rows continue from it;
+* a mixed step (prefills + spec requests, one conv launch) through a row map;
+* device-side error codes leave the offending page untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_14_gb300 as gdn
+import oracle
+import synth
+from tests.gpu_util import Layer, bits, f64, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SPEC = gdn.GDN_REQ_SPEC
+PAR = gdn.GDN_REQ_PARITY
+TOL = 1e-4
+
+
+def spec_flags(step, R):
+    return np.full(R, SPEC | (PAR if step % 2 else 0), np.int64)
+
+
+def make_layers(d, R, state, slots=True):
+    sh = d["shapes"]
+    L1 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
+               num_pages=R)
+    L2 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
+               num_pages=R, slots=slots) if slots else None
+    hist = to_dev(d["hist0"])[:R]
+    S0 = d["S0"][:R]
+    if state == gdn.GDN_BF16:
+        S0 = oracle.round_bf16(S0).astype(np.float32)
+    L1.seed(range(R), S0=S0, hist=hist)
+    if L2 is not None:
+        for r in range(R):
+            L2.slots.state(r, 0).copy_(torch.from_numpy(S0[r]).transpose(-1, -2))
+            L2.slots.window(r, 0).copy_(hist[r])
+    return L1, L2, S0
+
+
+def one_page_step(L, start, ln, flags, acc, x, a, b):
+    B = L.batch(start, ln, flags=flags, n_accepted=acc)
+    y = L.conv(B, x)
+    o = L.verify(B, y, a, b)
+    return y, o
+
+
+def step_rows(d, s, R, n):
+    rows = d["step_rows"][s]
+    sl = slice(0, R * n)
+    return to_dev(rows["x"])[sl], to_dev(rows["a"])[sl], to_dev(rows["b"])[sl]
+
+
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_one_page_bit_identical_to_slot_layout_20_steps(state):
+    d = synth.spec()
+    R, n, steps = d["R"], d["n"], d["steps"]
+    start, ln = d["row_start"], d["row_len"]
+    L1, L2, _ = make_layers(d, R, state)
+    for s in range(steps):
+        x, a, b = step_rows(d, s, R, n)
+        acc = d["accepted"][s]
+        y1, o1 = one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        B2 = L2.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc)
+        y2, o2 = L2.spec_slots(B2, x, a, b)
+        L1.ok()
+        L2.ok()
+        assert np.array_equal(bits(y1), bits(y2)), f"conv rows differ at step {s}"
+        assert np.array_equal(bits(o1), bits(o2)), f"outputs differ at step {s}"
+    # commit the last step's acceptance and compare the checkpoint with the slot
+    acc = d["accepted"][steps]
+    zero = np.zeros(R, np.int32)
+    B = L1.batch(start, zero, flags=spec_flags(steps, R), n_accepted=acc, num_rows=int(start[-1]) + n)
+    L1.conv(B, x)
+    L1.verify(B, y1, a, b)
+    L1.ok()
+    for r in range(R):
+        assert np.array_equal(bits(L1.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
+        assert np.array_equal(bits(L1.pool.window(r)[:3]), bits(L2.slots.window(r, int(acc[r]))))
+        assert int(L1.pool.flag(r).item()) & 0xFC == 0     # record closed (width 0)
+
+
+def test_one_page_matches_oracle_slot_simulation():
+    d = synth.spec()
+    R_all, n = d["R"], d["n"]
+    R, steps = 4, 6
+    sh = d["shapes"]
+    start, ln = d["row_start"][:R], d["row_len"][:R]
+    L1, _, S0 = make_layers(d, R, gdn.GDN_F32, slots=False)
+    sim = oracle.SlotSim(R, sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, d["conv_w"].value, d["A_log"],
+                         d["dt_bias"], S0=S0, hist0=d["hist0"].value[:R],
+                         row_store=oracle.round_bf16)
+    for s in range(steps):
+        rows = d["step_rows"][s]
+        x, a, b = step_rows(d, s, R, n)
+        acc = d["accepted"][s][:R]
+        y, o = one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        L1.ok()
+        xs = rows["x"].value[: R * n].reshape(R, n, -1)
+        As = rows["a"].value[: R * n].reshape(R, n, -1)
+        Bs = rows["b"].value[: R * n].reshape(R, n, -1)
+        y_ref, o_ref = sim.step(xs, As, Bs, acc)
+        # the conv'd rows are bit-exact against the fp32 mirror
+        assert np.array_equal(bits(y), synth.bf16_bits(y_ref.reshape(R * n, -1)).view(np.int16))
+        assert rel(f64(o), o_ref.reshape(R * n, sh.Hv, sh.Dv)) <= TOL
+    del R_all
+
+
+def test_lockstep_identical_requests_equal_request_alone():
+    d = synth.spec(R=8, steps=5)
+    n, steps = d["n"], d["steps"]
+    twin = [1, 3, 4, 6]
+    # requests in `twin` are copies of request 1: same rows, state, window, acceptance
+    for s in range(steps):
+        for k in ("x", "a", "b"):
+            t = d["step_rows"][s][k]
+            st = t.store.reshape(8, n, -1)
+            st[twin] = st[1]
+            t.store[:] = st.reshape(t.store.shape)
+        d["accepted"][s][twin] = d["accepted"][s][1]
+    d["S0"][twin] = d["S0"][1]
+    d["hist0"].store[twin] = d["hist0"].store[1]
+    d["hist0"].value[twin] = d["hist0"].value[1]
+    start, ln = d["row_start"], d["row_len"]
+    L, _, _ = make_layers(d, 8, gdn.GDN_F32, slots=False)
+    # the same request alone, as request 0 of a batch of one, on page 0
+    d1 = dict(d)
+    d1["S0"] = d["S0"][1:2]
+    h1 = synth.Tensor(d["hist0"].store[1:2], d["hist0"].value[1:2], d["hist0"].dtype)
+    d1["hist0"] = h1
+    La, _, _ = make_layers(d1, 1, gdn.GDN_F32, slots=False)
+    for s in range(steps):
+        x, a, b = step_rows(d, s, 8, n)
+        _, o = one_page_step(L, start, ln, spec_flags(s, 8), d["accepted"][s], x, a, b)
+        _, oa = one_page_step(La, [0], [n], spec_flags(s, 1), d["accepted"][s][1:2],
+                              x[n:2 * n], a[n:2 * n], b[n:2 * n])
+        L.ok()
+        La.ok()
+        for r in twin:
+            assert np.array_equal(bits(o[r * n:(r + 1) * n]), bits(oa))
+
+
+def test_commit_then_plain_decode_continues():
+    """Commit (zero new candidates) closes the record; plain rows then run
+    from the committed state, and plain rows on an open record are refused."""
+    d = synth.spec(R=2, steps=2)
+    sh, n = d["shapes"], d["n"]
+    start, ln = d["row_start"], d["row_len"]
+    L, _, S0 = make_layers(d, 2, gdn.GDN_F32, slots=False)
+    x, a, b = step_rows(d, 0, 2, n)
+    one_page_step(L, start, ln, spec_flags(0, 2), d["accepted"][0], x, a, b)
+    L.ok()
+    # plain rows while the record is open: refused, page untouched
+    before = L.pool.buf.clone()
+    rng = np.random.default_rng(5)
+    rows = synth.rows(rng, 2, sh, synth.BF16)
+    xp, ap, bp = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    Bp = L.batch([0, 1], [1, 1])
+    L.conv(Bp, xp)
+    assert L.status_code() == gdn.CODES["GDN_DEV_RECORD_OPEN"]
+    L.reset_status()
+    L.seq(Bp, xp, ap, bp)
+    assert L.status_code() == gdn.CODES["GDN_DEV_RECORD_OPEN"]
+    L.reset_status()
+    assert torch.equal(before, L.pool.buf)
+    # commit with acceptance [2, 5]
+    acc = np.array([2, 5], np.int32)
+    Bc = L.batch(start, [0, 0], flags=spec_flags(1, 2), n_accepted=acc, num_rows=2 * n)
+    L.conv(Bc, x)
+    L.verify(Bc, x, a, b)
+    L.ok()
+    # then one plain decode token through conv + rule
+    y = L.conv(Bp, xp)
+    o = L.seq(Bp, y, ap, bp)
+    L.ok()
+    # oracle: accepted history (rows 0..acc of step 0) then the decode row
+    for r in range(2):
+        xs = np.concatenate([d["step_rows"][0]["x"].value[r * n: r * n + acc[r] + 1],
+                             rows["x"].value[r:r + 1]])
+        As = np.concatenate([d["step_rows"][0]["a"].value[r * n: r * n + acc[r] + 1],
+                             rows["a"].value[r:r + 1]])
+        Bs = np.concatenate([d["step_rows"][0]["b"].value[r * n: r * n + acc[r] + 1],
+                             rows["b"].value[r:r + 1]])
+        yy, _ = oracle.conv_f32(xs, d["hist0"].value[r:r + 1], d["conv_w"].value, [0], [len(xs)])
+        yy = oracle.round_bf16(yy)
+        o_ref, S_ref = oracle.gdn_f64(yy, As, Bs, d["A_log"], d["dt_bias"], [0], [len(xs)],
+                                      sh.Hk, sh.Hv, sh.Dk, sh.Dv, S0=S0[r:r + 1])
+        assert rel(f64(o[r]), o_ref[-1]) <= TOL
+        assert rel(f64(L.pool.state_math(r)), S_ref[0]) <= TOL
+
+
+def test_mixed_prefill_and_spec_step_through_row_map():
+    for shuffled in (False, True):
+        d = synth.mixed(shuffled=shuffled)
+        sh, n, ns, npf = d["shapes"], d["n"], d["n_spec"], d["n_prefill"]
+        R = d["R"]
+        L = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=R)
+        spec = d["is_spec"]
+        S0 = d["S0"]
+        L.seed(range(R), S0=S0, hist=to_dev(d["hist0"]))
+        # one earlier spec step seeds the spec requests' records
+        pr = d["prev_rows"]
+        st0, ln0, _ = synth.pack([n] * ns)
+        one_page_step(L, st0, ln0, spec_flags(0, ns), np.zeros(ns, np.int32), to_dev(pr["x"]),
+                      to_dev(pr["a"]), to_dev(pr["b"]))
+        L.ok()
+        # the mixed step: one conv launch over every row, then rule + verify
+        flags = np.where(spec, SPEC | PAR, gdn.GDN_REQ_FRESH)
+        acc = np.where(spec, np.concatenate([d["prev_accepted"], np.zeros(npf, np.int32)]), 0)
+        lengths = d["row_len"]
+        order = np.argsort(-lengths, kind="stable")
+        B = L.batch(d["row_start"], lengths, flags=flags, n_accepted=acc, order=order)
+        x, a, b = to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"])
+        y = L.conv(B, x)
+        o = L.seq(B, y, a, b)
+        o2 = L.verify(B, y, a, b)
+        L.ok()
+        row_is_spec = np.zeros(d["T"], bool)
+        for r in range(R):
+            row_is_spec[d["row_start"][r]: d["row_start"][r] + lengths[r]] = spec[r]
+        o = torch.where(torch.from_numpy(row_is_spec).cuda()[:, None, None], o2, o)
+        # prefills: fp32 conv mirror from a zero window, bf16 rows, fp64 rule
+        for r in np.nonzero(~spec)[0][:3]:
+            sl = slice(d["row_start"][r], d["row_start"][r] + lengths[r])
+            yy, _ = oracle.conv_f32(d["x"].value[sl], np.zeros((1, 3, sh.C)), d["conv_w"].value,
+                                    [0], [lengths[r]])
+            o_ref, S_ref = oracle.gdn_f64(oracle.round_bf16(yy), d["a"].value[sl],
+                                          d["b"].value[sl], d["A_log"], d["dt_bias"], [0],
+                                          [lengths[r]], sh.Hk, sh.Hv, sh.Dk, sh.Dv)
+            assert rel(f64(o[sl]), o_ref) <= TOL
+            assert rel(f64(L.pool.state_math(r)), S_ref[0]) <= TOL
+        # spec requests: the oracle's slot simulation over both steps
+        k = 3
+        sim = oracle.SlotSim(k, sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, d["conv_w"].value, d["A_log"],
+                             d["dt_bias"], S0=S0[:k], hist0=d["hist0"].value[:k],
+                             row_store=oracle.round_bf16)
+        sim.step(pr["x"].value[:k * n].reshape(k, n, -1), pr["a"].value[:k * n].reshape(k, n, -1),
+                 pr["b"].value[:k * n].reshape(k, n, -1), np.zeros(k, np.int32))
+        xs = np.stack([d["x"].value[d["row_start"][r]: d["row_start"][r] + n] for r in range(k)])
+        As = np.stack([d["a"].value[d["row_start"][r]: d["row_start"][r] + n] for r in range(k)])
+        Bs = np.stack([d["b"].value[d["row_start"][r]: d["row_start"][r] + n] for r in range(k)])
+        _, o_ref = sim.step(xs, As, Bs, d["prev_accepted"][:k])
+        for r in range(k):
+            sl = slice(d["row_start"][r], d["row_start"][r] + n)
+            assert rel(f64(o[sl]), o_ref[r]) <= TOL
+
+
+def _at_step_one(d):
+    """Four spec pages after one verify step (record width 8, parity 1)."""
+    L, _, _ = make_layers(d, 4, gdn.GDN_F32, slots=False)
+    x, a, b = step_rows(d, 0, 4, d["n"])
+    one_page_step(L, d["row_start"], d["row_len"], spec_flags(0, 4), d["accepted"][0], x, a, b)
+    L.ok()
+    return L
+
+
+def _page(L, p):
+    lay = L.pool.layout
+    return L.pool.buf[p * lay.page_bytes:(p + 1) * lay.page_bytes].clone()
+
+
+@pytest.mark.parametrize("name", ["GDN_DEV_STALE_STEP", "GDN_DEV_BAD_ACCEPTED",
+                                  "GDN_DEV_BAD_FLAG"])
+def test_device_errors_skip_only_the_offending_request(name):
+    d = synth.spec(R=4, steps=2)
+    n = d["n"]
+    start, ln = d["row_start"], d["row_len"]
+    L = _at_step_one(d)
+    x, a, b = step_rows(d, 1, 4, n)
+    flags = spec_flags(1, 4)
+    acc = d["accepted"][1].copy()
+    if name == "GDN_DEV_STALE_STEP":
+        flags[2] = SPEC                      # parity 0, the page expects 1
+    elif name == "GDN_DEV_BAD_ACCEPTED":
+        acc[2] = 8                           # the record holds 8 rows: 0..7
+    else:
+        flags[2] |= gdn.GDN_REQ_FRESH        # FRESH together with SPEC
+    before = _page(L, 2)
+    others = [_page(L, p) for p in (0, 1, 3)]
+    B = L.batch(start, ln, flags=flags, n_accepted=acc)
+    y = L.conv(B, x)
+    assert L.status_code() == gdn.CODES[name]
+    L.verify(B, y, a, b)
+    assert L.status_code() == gdn.CODES[name]
+    assert torch.equal(before, _page(L, 2))
+    # the other requests completed their step
+    for p, old in zip((0, 1, 3), others):
+        assert not torch.equal(old, _page(L, p))
+        assert (int(L.pool.flag(p).item()) >> 1) & 1 == 0      # parity advanced to 0
+
+
+def test_device_errors_page_index_and_candidate_count():
+    d = synth.spec(R=4, steps=2)
+    n = d["n"]
+    start, ln = d["row_start"], d["row_len"]
+    L = _at_step_one(d)
+    x, a, b = step_rows(d, 1, 4, n)
+    B = L.batch(start, ln, flags=spec_flags(1, 4), n_accepted=d["accepted"][1], page=[0, 1, 7, 3])
+    L.conv(B, x)
+    assert L.status_code() == gdn.CODES["GDN_DEV_BAD_PAGE"]
+    L.reset_status()
+    # 9 candidates for request 0 (rows 0..8 exist: request 1 starts at row 8)
+    lens = ln.copy()
+    lens[0] = 9
+    B = L.batch(start, lens, flags=spec_flags(1, 4), n_accepted=d["accepted"][1])
+    L.conv(B, x)
+    assert L.status_code() == gdn.CODES["GDN_DEV_TOO_MANY_CANDIDATES"]
+    L.reset_status()
+    L.verify(B, x, a, b)
+    assert L.status_code() == gdn.CODES["GDN_DEV_TOO_MANY_CANDIDATES"]
