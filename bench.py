@@ -1,0 +1,681 @@
+"""Benchmark of the GB300 Gated DeltaNet layer core.
+
+One step = one pass of the layer core over one batch: the causal conv +
+SiLU (gdn_conv) and the fused post-conv + gated delta rule (gdn_seq). The
+headline workload is the decode batch: 64 requests x 1 token, 16 q/k heads,
+32 value heads, Dk = Dv = 128 (8192 conv channels), bf16 rows, fp32 state.
+
+Metric: GDN tokens/s per layer, plus the state-traffic HBM GB/s of the rule
+kernel against the measured HBM peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--no-extra]
+
+Under torchrun each rank runs its own replica on its own GPU (requests are
+independent: weak scaling, no data-path collective); the ranks meet only in a
+barrier around the timed region and a max-reduction of the elapsed time.
+``--impl reference`` times the CPU oracle on the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "GDN tokens/s per layer and state-traffic HBM GB/s vs GB300 peak (1 GPU)"
+WORKLOAD = ("decode: 64 requests x 1 token, Hk=16 Hv=32 Dk=Dv=128 (C=8192), W=4, "
+            "bf16 rows, fp32 state")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+POOLS = 4  # rotating page pools: 4 x ~135 MB > the 129 MB L2
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ measurement
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi SM clock and throttle reasons, sampled every 100 ms."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self._stop = threading.Event()
+        self._thread = None
+
+    def _run(self):
+        try:
+            proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                     "--format=csv,noheader,nounits", "-lms", "100"],
+                                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        try:
+            while not self._stop.is_set():
+                line = proc.stdout.readline()
+                if not line:
+                    break
+                self.rows.append([s.strip() for s in line.split(",")])
+        finally:
+            proc.terminate()
+            try:
+                proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                proc.kill()
+
+    def __enter__(self):
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        self._thread.join(timeout=10)
+
+    def summary(self):
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in self.rows:
+            if len(r) < 9:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- our arm
+
+class Decode:
+    """The decode step on POOLS rotating copies of the 64-request batch."""
+
+    def __init__(self, device, pools=POOLS, R=64):
+        import torch
+
+        import gated_deltanet_linear_14_gb300 as gdn
+        from gated_deltanet_linear_14_gb300.pages import PagePool
+
+        self.gdn, self.torch = gdn, torch
+        d = synth.decode(R=R)
+        self.d = d
+        sh = d["shapes"]
+        self.R, self.sh = R, sh
+        self.dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 0, gdn.GDN_BF16, gdn.GDN_F32,
+                                  gdn.GDN_BF16)
+
+        def put(a, dtype=None):
+            a = np.ascontiguousarray(a if dtype is None else np.asarray(a, dtype))
+            t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).to(device)
+            return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+        self.put = put
+        self.A_log, self.dt_bias = put(d["A_log"]), put(d["dt_bias"])
+        self.params = gdn.make_params(self.A_log, self.dt_bias)
+        self.conv_w = put(d["conv_w"].store)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.pools = []
+        S_page = torch.from_numpy(d["S0"]).transpose(-1, -2).contiguous().to(device)
+        hist = put(d["hist0"].store)
+        for _ in range(pools):
+            pool = PagePool(self.dims, R, device=device)
+            for r in range(R):
+                pool.state(r).copy_(S_page[r])
+                pool.window(r).copy_(hist[r])
+            self.pools.append(pool)
+        self.x = put(d["x"].store)
+        self.a = put(d["a"].store)
+        self.b = put(d["b"].store)
+        self.y = torch.empty(R, sh.C, dtype=torch.bfloat16, device=device)
+        self.o = torch.empty(R, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+        ints = [put(np.asarray(v, np.int32)) for v in
+                (d["row_start"], d["row_len"], np.arange(R), np.zeros(R))]
+        self._ints = ints
+        self.batch = gdn.make_batch(R, R, 1, R, *ints)
+        # host-side buffers of the end-to-end leg (pinned)
+        self.h_x = torch.empty_like(self.x, device="cpu").pin_memory()
+        self.h_a = torch.empty_like(self.a, device="cpu").pin_memory()
+        self.h_b = torch.empty_like(self.b, device="cpu").pin_memory()
+        self.h_o = torch.empty_like(self.o, device="cpu").pin_memory()
+        self.h_x.copy_(self.x.cpu())
+        self.h_a.copy_(self.a.cpu())
+        self.h_b.copy_(self.b.cpu())
+
+    # bytes the rule kernel must move per launch (decode)
+    def rule_bytes(self):
+        sh, R = self.sh, self.R
+        state = 2 * R * sh.Hv * sh.Dk * sh.Dv * 4            # read + write fp32 state
+        rows = R * (2 * sh.Hk * sh.Dk + sh.Hv * sh.Dv) * 2   # conv'd q|k|v rows (bf16)
+        gates = 2 * R * sh.Hv * 2                            # a, b
+        out = R * sh.Hv * sh.Dv * 2                          # o (bf16)
+        return state + rows + gates + out, state
+
+    def conv_bytes(self):
+        sh, R = self.sh, self.R
+        return R * sh.C * 2 * 2 + R * 2 * (sh.W - 1) * sh.C * 2 + sh.C * sh.W * 2
+
+    def launch(self, i, ev=None):
+        gdn = self.gdn
+        pool = self.pools[i % len(self.pools)]
+        if ev is not None:
+            ev[0].record()
+        gdn.gdn_conv(self.dims, self.batch, self.params, self.x, self.conv_w, self.y,
+                     gdn.GDN_BF16, pool.buf, self.status)
+        if ev is not None:
+            ev[1].record()
+        gdn.gdn_seq(self.dims, self.batch, self.params, self.y, self.a, self.b, self.o, pool.buf,
+                    self.status)
+        if ev is not None:
+            ev[2].record()
+
+    def launch_e2e(self, i):
+        """The same step through host buffers: H2D inputs, step, D2H output."""
+        self.x.copy_(self.h_x, non_blocking=True)
+        self.a.copy_(self.h_a, non_blocking=True)
+        self.b.copy_(self.h_b, non_blocking=True)
+        self.launch(i)
+        self.h_o.copy_(self.o, non_blocking=True)
+
+    def e2e_bytes(self):
+        h2d = sum(t.numel() * t.element_size() for t in (self.h_x, self.h_a, self.h_b))
+        return h2d, self.h_o.numel() * self.h_o.element_size()
+
+    def check(self):
+        code = int(self.status.item())
+        if code != 0:
+            raise RuntimeError(f"device status {self.gdn.STATUS.get(code, code)}")
+
+
+def time_steps(fn, K, torch):
+    """K back-to-back calls of fn(i), CUDA events on the current stream."""
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record()
+    for i in range(K):
+        fn(i)
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    peaks, peak_src = load_peaks()
+    wl = Decode(device)
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        wl.launch(i)
+    torch.cuda.synchronize()
+    wl.check()
+
+    # timed region: K steps, per-kernel events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        elapsed = time_steps(lambda i: wl.launch(W + i, evs[i]), K, torch)
+        wall = time.perf_counter() - t0
+    torch.cuda.synchronize()
+    barrier(world)
+    wl.check()
+    conv_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    rule_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    elapsed_max = reduce_max(elapsed, world)
+
+    # end-to-end through host buffers
+    for i in range(W):
+        wl.launch_e2e(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e = time_steps(lambda i: wl.launch_e2e(i), K, torch)
+    e2e_max = reduce_max(e2e, world)
+    h2d, d2h = wl.e2e_bytes()
+
+    tokens = wl.R * K * world
+    rule_bytes, state_bytes = wl.rule_bytes()
+    rule_s = statistics.mean(rule_ms) / 1e3
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved = rule_bytes / rule_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": tokens / elapsed_max,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": elapsed_max / K * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) rows, N(0,0.02) fp32 state, random-init layer)",
+        "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
+                   "l2": f"{POOLS} rotating page pools ({POOLS * wl.pools[0].buf.numel() / 2**20:.0f} "
+                         "MiB) exceed the 129 MB L2"},
+        "state_gbs": state_bytes / rule_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": traffic_from_profile("rule_decode"),
+                     "kernel": "rule_kernel (gdn_seq, decode)",
+                     "algorithmic_bytes_per_launch": rule_bytes,
+                     "launch_ms": rule_s * 1e3, "peak_source": f"{peak_src} hbm_gbs (burst)"},
+        "kernels_ms": {"gdn_conv": statistics.mean(conv_ms), "gdn_seq": statistics.mean(rule_ms)},
+        "e2e": {"value": tokens / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max / K * 1e3},
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+        "wall_s": wall,
+    }
+    if not args.no_extra:
+        line["workloads"] = extra_workloads(device, peaks, args)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+    return line
+
+
+def traffic_from_profile(name):
+    """DRAM bytes per launch from a committed ncu summary, if one is current."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        data = json.load(f)
+    v = data.get(name)
+    return None if v is None else v.get("dram_bytes_per_launch")
+
+
+def extra_workloads(device, peaks, args):
+    """The other workloads of the layer core, each timed the same way."""
+    out = {}
+    for name, fn in (("spec_verify_fp32_state", lambda: bench_spec(device, peaks, "f32")),
+                     ("spec_verify_bf16_state", lambda: bench_spec(device, peaks, "bf16")),
+                     ("mixed_prefill_spec", lambda: bench_mixed(device, peaks)),
+                     ("long_prefill_token_by_token", lambda: bench_long_seq(device, peaks)),
+                     ("conv_long_rows", lambda: bench_conv_long(device, peaks))):
+        try:
+            out[name] = fn()
+        except Exception as e:  # report, do not hide the headline line
+            out[name] = {"error": repr(e)}
+    return out
+
+
+def _dev_batch(gdn, torch, device, start, ln, page, flags, acc=None, order=None, num_rows=None,
+               max_rows=None, num_pages=None):
+    def put(v):
+        return torch.from_numpy(np.ascontiguousarray(np.asarray(v, np.int64).astype(np.uint32)
+                                                     .view(np.int32))).to(device)
+    arrs = [put(start), put(ln), put(page), put(flags)]
+    acc_t = None if acc is None else put(acc)
+    ord_t = None if order is None else put(order)
+    R = len(start)
+    num_rows = int(np.max(np.asarray(start) + np.asarray(ln))) if num_rows is None else num_rows
+    max_rows = int(np.max(ln)) if max_rows is None else max_rows
+    B = gdn.make_batch(R, num_rows, max_rows, R if num_pages is None else num_pages, *arrs,
+                       acc_t, ord_t)
+    B._keep = arrs + [acc_t, ord_t]
+    return B
+
+
+def _put_io(torch, device, t):
+    a = np.ascontiguousarray(t.store)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
+    """Spec verify: 64 pages, 1+7 candidates, conv + one-page verify per step."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import PagePool
+    d = synth.spec(steps=2)
+    sh, R, n = d["shapes"], d["R"], d["n"]
+    st = gdn.GDN_F32 if state == "f32" else gdn.GDN_BF16
+    dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 8, gdn.GDN_BF16, st, gdn.GDN_BF16)
+    A_log = torch.from_numpy(d["A_log"]).to(device)
+    dt = torch.from_numpy(d["dt_bias"]).to(device)
+    params = gdn.make_params(A_log, dt)
+    conv_w = _put_io(torch, device, d["conv_w"])
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    S_page = torch.from_numpy(d["S0"]).transpose(-1, -2).contiguous().to(device)
+    hist = _put_io(torch, device, d["hist0"])
+    pl = []
+    for _ in range(pools):
+        pool = PagePool(dims, R, device=device)
+        for r in range(R):
+            pool.state(r).copy_(S_page[r])
+            pool.window(r)[:3].copy_(hist[r])
+        pl.append(pool)
+    rows = d["step_rows"][0]
+    x, a, b = (_put_io(torch, device, rows[k]) for k in ("x", "a", "b"))
+    T = R * n
+    y = torch.empty(T, sh.C, dtype=torch.bfloat16, device=device)
+    o = torch.empty(T, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+    rng = np.random.default_rng(2)
+    accs = rng.integers(0, n, size=(8, R))
+    batches = {}
+    for par in (0, 1):
+        flags = np.full(R, gdn.GDN_REQ_SPEC | (gdn.GDN_REQ_PARITY if par else 0))
+        for k in range(8):
+            batches[(par, k)] = _dev_batch(gdn, torch, device, d["row_start"], d["row_len"],
+                                           np.arange(R), flags, acc=accs[k])
+    steps_done = [0] * pools
+
+    def launch(i, ev=None):
+        p = i % pools
+        B = batches[(steps_done[p] % 2, i % 8)]
+        steps_done[p] += 1
+        if ev is not None:
+            ev[0].record()
+        gdn.gdn_conv(dims, B, params, x, conv_w, y, gdn.GDN_BF16, pl[p].buf, status)
+        if ev is not None:
+            ev[1].record()
+        gdn.gdn_spec_verify(dims, B, params, y, a, b, o, pl[p].buf, status)
+        if ev is not None:
+            ev[2].record()
+
+    for i in range(W):
+        launch(i)
+    torch.cuda.synchronize()
+    evs = [_events(torch, 3) for _ in range(K)]
+    el = time_steps(lambda i: launch(W + i, evs[i]), K, torch)
+    code = int(status.item())
+    ver_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ssz = 4 if state == "f32" else 2
+    state_bytes = 2 * R * sh.Hv * sh.Dk * sh.Dv * ssz
+    mean_acc = float(np.mean(accs)) + 1.0
+    rec_row = (sh.C + 2 * sh.Hv) * 2
+    other = int(R * mean_acc * rec_row + T * (sh.C + 2 * sh.Hv) * 2 + T * sh.Hv * sh.Dv * 2)
+    flops = R * sh.Hv * sh.Dk * sh.Dv * (mean_acc + n) * 7
+    gbs = (state_bytes + other) / (ver_ms / 1e3) / 1e9
+    return {"workload": f"spec verify: {R} pages, 1+7 candidates, {state} state, conv + verify",
+            "ms_per_step": el / K * 1e3, "verify_ms": ver_ms, "conv_ms": conv_ms,
+            "tokens_per_s": T * K / el, "verify_gbs": gbs,
+            "verify_frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
+            "verify_tflops_fp32": flops / (ver_ms / 1e3) / 1e12, "status": code}
+
+
+def bench_mixed(device, peaks, K=20, W=4):
+    """Mixed step: 8 fresh prefills (45..400 tokens) + 32 spec requests."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import PagePool
+    d = synth.mixed()
+    sh, R, n, ns = d["shapes"], d["R"], d["n"], d["n_spec"]
+    dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 8, gdn.GDN_BF16, gdn.GDN_F32,
+                         gdn.GDN_BF16)
+    A_log = torch.from_numpy(d["A_log"]).to(device)
+    dt = torch.from_numpy(d["dt_bias"]).to(device)
+    params = gdn.make_params(A_log, dt)
+    conv_w = _put_io(torch, device, d["conv_w"])
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    pool = PagePool(dims, R, device=device)
+    S_page = torch.from_numpy(d["S0"]).transpose(-1, -2).contiguous().to(device)
+    for r in range(R):
+        pool.state(r).copy_(S_page[r])
+    x, a, b = (_put_io(torch, device, d[k]) for k in ("x", "a", "b"))
+    T = d["T"]
+    y = torch.empty(T, sh.C, dtype=torch.bfloat16, device=device)
+    o = torch.empty(T, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+    lengths = d["row_len"]
+    order = np.argsort(-lengths, kind="stable")
+    acc = np.where(d["is_spec"], np.concatenate([d["prev_accepted"],
+                                                 np.zeros(R - ns, np.int32)]), 0)
+    batches = []
+    for par in (0, 1):
+        flags = np.where(d["is_spec"], gdn.GDN_REQ_SPEC | (gdn.GDN_REQ_PARITY if par else 0),
+                         gdn.GDN_REQ_FRESH)
+        batches.append(_dev_batch(gdn, torch, device, d["row_start"], lengths, np.arange(R), flags,
+                                  acc=acc, order=order))
+
+    def launch(i, ev=None):
+        B = batches[i % 2]
+        if ev is not None:
+            ev[0].record()
+        gdn.gdn_conv(dims, B, params, x, conv_w, y, gdn.GDN_BF16, pool.buf, status)
+        if ev is not None:
+            ev[1].record()
+        gdn.gdn_seq(dims, B, params, y, a, b, o, pool.buf, status)
+        if ev is not None:
+            ev[2].record()
+        gdn.gdn_spec_verify(dims, B, params, y, a, b, o, pool.buf, status)
+        if ev is not None:
+            ev[3].record()
+
+    for i in range(W):
+        launch(i)
+    torch.cuda.synchronize()
+    evs = [_events(torch, 4) for _ in range(K)]
+    el = time_steps(lambda i: launch(W + i, evs[i]), K, torch)
+    return {"workload": f"mixed: 8 prefills of {int(lengths[ns:].min())}..{int(lengths[ns:].max())} "
+                        f"tokens + {ns} spec requests x {n} rows, {T} rows, row map longest first",
+            "ms_per_step": el / K * 1e3, "tokens_per_s": T * K / el,
+            "conv_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
+            "seq_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
+            "verify_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+            "longest_chain": int(lengths.max()), "status": int(status.item())}
+
+
+def bench_long_seq(device, peaks, K=3, W=3):
+    """4 x 8192-token prefill through the token-by-token rule (conv + seq)."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import PagePool
+    d = synth.long()
+    sh, R, T = d["shapes"], d["R"], d["T"]
+    dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 0, gdn.GDN_BF16, gdn.GDN_F32,
+                         gdn.GDN_BF16)
+    A_log = torch.from_numpy(d["A_log"]).to(device)
+    dt = torch.from_numpy(d["dt_bias"]).to(device)
+    params = gdn.make_params(A_log, dt)
+    conv_w = _put_io(torch, device, d["conv_w"])
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    pool = PagePool(dims, R, device=device)
+    x, a, b = (_put_io(torch, device, d[k]) for k in ("x", "a", "b"))
+    y = torch.empty(T, sh.C, dtype=torch.bfloat16, device=device)
+    o = torch.empty(T, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+    B = _dev_batch(gdn, torch, device, d["row_start"], d["row_len"], np.arange(R),
+                   np.full(R, gdn.GDN_REQ_FRESH))
+
+    def launch(i, ev=None):
+        if ev is not None:
+            ev[0].record()
+        gdn.gdn_conv(dims, B, params, x, conv_w, y, gdn.GDN_BF16, pool.buf, status)
+        if ev is not None:
+            ev[1].record()
+        gdn.gdn_seq(dims, B, params, y, a, b, o, pool.buf, status)
+        if ev is not None:
+            ev[2].record()
+
+    for i in range(W):
+        launch(i)
+    torch.cuda.synchronize()
+    evs = [_events(torch, 3) for _ in range(K)]
+    el = time_steps(lambda i: launch(W + i, evs[i]), K, torch)
+    seq_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    return {"workload": "long prefill: 4 x 8192 tokens through conv + token-by-token rule",
+            "ms_per_step": el / K * 1e3, "tokens_per_s": T * K / el, "seq_ms": seq_ms,
+            "seq_us_per_token_chain": seq_ms * 1e3 / int(d["row_len"][0]),
+            "status": int(status.item())}
+
+
+def bench_conv_long(device, peaks, K=10, W=3):
+    """The conv alone over 32768 rows x 8192 channels (1 GiB of row traffic)."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import PagePool
+    d = synth.long()
+    sh, R, T = d["shapes"], d["R"], d["T"]
+    dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 0, gdn.GDN_BF16, gdn.GDN_F32,
+                         gdn.GDN_BF16)
+    params = gdn.make_params(None, None)
+    conv_w = _put_io(torch, device, d["conv_w"])
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    pool = PagePool(dims, R, device=device)
+    x = _put_io(torch, device, d["x"])
+    y = torch.empty(T, sh.C, dtype=torch.bfloat16, device=device)
+    B = _dev_batch(gdn, torch, device, d["row_start"], d["row_len"], np.arange(R),
+                   np.zeros(R))
+    for i in range(W):
+        gdn.gdn_conv(dims, B, params, x, conv_w, y, gdn.GDN_BF16, pool.buf, status)
+    el = time_steps(lambda i: gdn.gdn_conv(dims, B, params, x, conv_w, y, gdn.GDN_BF16, pool.buf,
+                                           status), K, torch)
+    byts = 2 * T * sh.C * 2
+    gbs = byts / (el / K) / 1e9
+    return {"workload": "conv: 4 x 8192 rows x 8192 channels, bf16 in/out",
+            "ms_per_launch": el / K * 1e3, "gbs": gbs, "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
+            "status": int(status.item())}
+
+
+# ------------------------------------------------------- CPU oracle (reference)
+
+def oracle_decode_step(d, threads):
+    import oracle
+    sh = d["shapes"]
+    y, _ = oracle.conv_f64(d["x"].value, d["hist0"].value, d["conv_w"].value, d["row_start"],
+                           d["row_len"])
+    o, S = oracle.gdn_f64(y, d["a"].value, d["b"].value, d["A_log"], d["dt_bias"],
+                          d["row_start"], d["row_len"], sh.Hk, sh.Hv, sh.Dk, sh.Dv, S0=d["S0"],
+                          threads=threads)
+    return o
+
+
+def cpu_baseline(seconds=10.0, steps=None):
+    """The oracle, as it stands, on the decode batch: whole steps repeated
+    until about `seconds` of CPU time (or `steps` steps)."""
+    import oracle
+    d = synth.decode()
+    threads = oracle.default_threads()
+    oracle_decode_step(d, threads)  # load / warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle_decode_step(d, threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if (steps is not None and n >= steps) or (steps is None and el >= seconds):
+            break
+    return {"value": d["R"] * n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full decode steps (64 requests x 1 token, fp64 conv + rule) in "
+                      f"{el:.1f} s", "steps": n}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    K, W = args.steps, args.warmup
+    import oracle
+    d = synth.decode()
+    threads = oracle.default_threads()
+    for _ in range(W):
+        oracle_decode_step(d, threads)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle_decode_step(d, threads)
+    el = time.perf_counter() - t0
+    v = d["R"] * K / el
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "cpu oracle, rank 0 only"},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{K} full decode steps, fp64 oracle on the host cores"},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        if world > 1 and rank != 0:
+            return 0
+        line = run_reference(args, world, rank)
+        print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl")
+    line = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -187,7 +187,9 @@ __device__ __forceinline__ float through(float x) { return to_f(from_f<T>(x)); }
 // ln2 split into a 12-bit-trimmed high part and a low correction; e^r from
 // the Taylor series through r^7 (coefficients 1/k!), Horner's rule with
 // fused multiply-adds; scaling by 2^n as two exact power-of-two factors.
-// x >= 88.5 gives +inf and x <= -87 gives 0.
+// x at or above the float nearest ln(FLT_MAX) = 88.7228390520684 (that float,
+// 88.72283935546875, lies just above it, so every smaller x has a finite
+// result) gives +inf; x <= -87 gives 0.
 __host__ __device__ constexpr float recip_factorial(int k) {
   double f = 1.0;
   for (int i = 2; i <= k; ++i) f *= i;
@@ -202,7 +204,7 @@ __device__ __forceinline__ float own_exp(float x) {
   const float log2e = (float)(1.0 / kLn2);
   const float ln2_hi = __uint_as_float(0x3F317000u);
   const float ln2_lo = (float)(kLn2 - (double)0.693115234375);  // 0x3F317000 == 0.693115234375
-  if (x >= 88.5f) return __int_as_float(0x7f800000);
+  if (x >= 88.72283935546875f) return __int_as_float(0x7f800000);
   if (x <= -87.0f) return 0.0f;
   const float t = __fmul_rn(x, log2e);
   const float n = rintf(t);

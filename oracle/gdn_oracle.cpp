@@ -35,6 +35,7 @@
 // each a fused multiply-add) and evaluates SiLU with its own exp (below).
 // Build with -ffp-contract=off so the compiler adds no contractions.
 
+#include <cfloat>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -191,7 +192,9 @@ void parallel_for(long n, int threads, F f) {
 // then e^r from its Taylor series, truncated after the r^7 term and evaluated
 // by Horner's rule with fused multiply-adds; then scaling by 2^n, built from
 // two exact power-of-two factors so no intermediate leaves the normal range.
-// Inputs >= 88.5 give +inf, inputs <= -87 give 0.
+// Inputs at or above the float nearest ln(FLT_MAX) (which lies just above
+// it, so every smaller input has a finite result) give +inf; inputs <= -87
+// give 0 (the result would leave the normal range).
 struct OwnExpConsts {
   float log2e, ln2_hi, ln2_lo;
   float c[8];  // 1/k!, k = 0..7
@@ -224,7 +227,8 @@ float pow2_exact(int n) {  // 2^n for -126 <= n <= 127, built from the bits
 }
 
 float own_exp_f32(float x) {
-  if (x >= 88.5f) return INFINITY;
+  static const float kOverflow = (float)std::log((double)FLT_MAX);
+  if (x >= kOverflow) return INFINITY;
   if (x <= -87.0f) return 0.0f;
   const float t = x * kExp.log2e;        // one rounding, no contraction
   const float n = std::nearbyint(t);     // round half to even (default mode)

@@ -80,9 +80,8 @@ class Layer:
         arrs = [to_dev(row_start), to_dev(row_len), to_dev(page), to_dev(flags)]
         acc = None if n_accepted is None else to_dev(np.asarray(n_accepted, np.int32))
         ordr = None if order is None else to_dev(np.asarray(order, np.int32))
-        num_rows = int(row_start.max(initial=0) + row_len.max(initial=0)) if num_rows is None \
-            else num_rows
-        num_rows = max(num_rows, int((row_start + row_len).max(initial=0)))
+        end = int((row_start + row_len).max(initial=0))
+        num_rows = end if num_rows is None else max(int(num_rows), end)
         max_rows = int(row_len.max(initial=0)) if max_rows is None else max_rows
         B = gdn.make_batch(R, num_rows, max_rows, self.pool.num_pages, *arrs, acc, ordr)
         B._keep = arrs + [acc, ordr]  # the struct owns the device arrays it points to

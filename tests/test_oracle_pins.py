@@ -243,6 +243,16 @@ def test_own_exp_within_two_ulp():
         assert abs(got - ref) <= 2 * ulp, (x, got, ref)
     assert oracle.exp_f32(100.0) == math.inf
     assert oracle.exp_f32(-100.0) == 0.0
+    # the largest float with a finite e^x overflows nothing; the next one does
+    top = np.float32(math.log(float(np.finfo(np.float32).max)))
+    below = np.nextafter(top, np.float32(0))
+    assert math.exp(float(top)) > float(np.finfo(np.float32).max) > math.exp(float(below))
+    got = oracle.exp_f32(float(below))
+    assert math.isfinite(got) and abs(got - math.exp(float(below))) <= 2 * np.spacing(np.float32(got))
+    assert oracle.exp_f32(float(top)) == math.inf
+    for x in np.linspace(88.4, float(below), 200).astype(np.float32):
+        ref = math.exp(float(x))
+        assert abs(oracle.exp_f32(float(x)) - ref) <= 2 * np.spacing(np.float32(ref))
 
 
 def test_own_silu_within_four_ulp():
