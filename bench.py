@@ -338,7 +338,13 @@ def traffic_from_profile(name):
     with open(path) as f:
         data = json.load(f)
     v = data.get(name)
-    return None if v is None else v.get("dram_bytes_per_launch")
+    if v is None:
+        return None
+    import hashlib
+    blob = b"".join(open(os.path.join(ROOT, f), "rb").read() for f in v.get("sources", []))
+    if hashlib.sha256(blob).hexdigest()[:16] != v.get("source_hash"):
+        return None  # the kernel changed since the counters were taken
+    return v.get("dram_bytes_per_launch")
 
 
 def extra_workloads(device, peaks, args):
