@@ -347,7 +347,7 @@ def traffic_from_profile(name):
     return v.get("dram_bytes_per_launch")
 
 
-def extra_workloads(device, peaks, args):
+def extra_workloads(device, peaks, args, only=None):
     """The other workloads of the layer core, each timed the same way."""
     out = {}
     for name, fn in (("spec_verify_fp32_state", lambda: bench_spec(device, peaks, "f32")),
@@ -355,6 +355,8 @@ def extra_workloads(device, peaks, args):
                      ("mixed_prefill_spec", lambda: bench_mixed(device, peaks)),
                      ("long_prefill_token_by_token", lambda: bench_long_seq(device, peaks)),
                      ("conv_long_rows", lambda: bench_conv_long(device, peaks))):
+        if only is not None and name != only:
+            continue
         try:
             out[name] = fn()
         except Exception as e:  # report, do not hide the headline line
@@ -661,10 +663,20 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only", default=None,
+                    help="run one secondary workload alone (spec_verify_fp32_state, "
+                         "spec_verify_bf16_state, mixed_prefill_spec, "
+                         "long_prefill_token_by_token, conv_long_rows)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
+    if args.only:
+        import torch
+        torch.cuda.set_device(local)
+        res = extra_workloads(torch.device(f"cuda:{local}"), load_peaks()[0], args, args.only)
+        print(json.dumps(res), flush=True)
+        return 0
     if args.impl == "reference":
         if world > 1 and rank != 0:
             return 0

@@ -9,24 +9,24 @@
 //
 // Work decomposition. One CTA = (request, value head h, block of BV = 32
 // value columns); 4 warps of 8 columns; inside a warp 4 column groups of 8
-// lanes, each lane holding M = 2 columns x E = Dk/8 entries of S in
-// registers. The Dk entries a lane owns are chunks of VEC contiguous
-// elements, chunk i of lane r at Dk index VEC*(8i + r), so a warp's loads of
-// a column are contiguous 16-byte vectors. Every reduction over Dk is a
-// 3-level xor butterfly inside the 8-lane group (all lanes end with the same
-// bits), with no shared memory and no atomics on data.
+// lanes; a lane holds M = 2 adjacent columns x E = Dk/8 entries of S in
+// registers (as float2 pairs for the packed f32x2 FMA pipe). The Dk entries a
+// lane owns are chunks of VEC contiguous elements, chunk i of lane r at Dk
+// index VEC*(8i + r), so a warp's accesses to a column are contiguous.
 //
-// Per token (one HBM-free step once S is in registers):
-//   k^ = k / sqrt(|k|^2 + eps), q^ likewise (butterfly over the 8 lanes)
-//   sk = S^T k^, sq = S^T q^ from the OLD S, kq = k^.q^
-//   u  = beta (v - alpha sk),  o = scale (alpha sq + u kq)
-//   S  = alpha S + k^ u^T
+// Tokens are processed in chunks of TC. For each chunk the CTA stages, once,
+// in shared memory: q^ and k^ normalised in fp32, the CTA's 32 values of v,
+// and per token (alpha = e^g, beta, q^.k^). The raw rows of the next chunk
+// are fetched into registers while the current chunk runs. The per-token
+// step of a lane is then only
+//   sk = S^T k^, sq = S^T q^ (old S, f32x2 partial sums, one 8-lane
+//   transpose-reduce of the four sums), u = beta (v - alpha sk),
+//   o = scale (alpha sq + u q^.k^), S = alpha S + k^ u^T (f32x2)
 // which is the rule S <- alpha S; u = beta (v - S^T k^); S <- S + k^ u^T;
-// o = scale S^T q^ with the decay folded into the two dot products, so S is
-// read once and written once per token. All arithmetic uses explicit
-// round-to-nearest intrinsics: the compiler cannot contract differently in
-// the three kernels, which is what makes the one-page verify bit-identical to
-// the slot layout.
+// o = scale S^T q^ with the decay folded into the dot products, so S is read
+// once and written once per token. All arithmetic is explicit
+// round-to-nearest intrinsics and the three modes share this code path, so
+// the one-page verify is bit-identical to the slot layout.
 #pragma once
 
 #include "common.cuh"
@@ -36,8 +36,10 @@ namespace gdn {
 enum RuleMode { MODE_SEQ = 0, MODE_VERIFY = 1, MODE_SLOTS = 2 };
 
 constexpr int kRuleWarps = 4;
-constexpr int kColsPerLane = 2;                         // M
+constexpr int kRuleThreads = kRuleWarps * 32;
+constexpr int kColsPerLane = 2;                         // M (adjacent columns)
 constexpr int kBV = kRuleWarps * 4 * kColsPerLane;      // columns per CTA
+constexpr int kTC = 16;                                 // tokens per staged chunk
 
 template <int DK, class ST>
 struct LaneMap {
@@ -48,104 +50,224 @@ struct LaneMap {
   __device__ static int idx(int r8, int i) { return VEC * (8 * i + r8); }
 };
 
-__device__ __forceinline__ float group8_sum(float v) {
-  v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
-  v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 2));
-  v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 4));
-  return v;
-}
+template <int DK>
+struct Stage {
+  float q[kTC][DK];       // q^ (fp32, normalised)
+  float k[kTC][DK];       // k^
+  float v[kTC][kBV];      // the CTA's value columns
+  float4 sc[kTC];         // alpha, beta, q^.k^, unused
+};
 
-// One token's inputs for one lane.
-template <int E>
-struct TokenIn {
-  float q[E], k[E];
-  float v[kColsPerLane];
+// Where a chunk's rows come from: packed step rows or a page record.
+template <class IO>
+struct RowSrc {
+  const IO* rows;         // row 0 of the run
+  size_t row_stride;      // elements between rows
+  const IO* a;            // a of row 0 (head h)
+  const IO* b;
+  size_t ab_stride;
+};
+
+// N elements of T held raw (packed) in registers until they are used.
+template <class T, int N>
+struct RawVec {
+  static constexpr int BYTES = N * (int)sizeof(T);
+  static_assert(BYTES % 8 == 0, "raw vectors are whole 8-byte words");
+  uint32_t w[BYTES / 4];
+  __device__ __forceinline__ void load(const T* p) {
+    if constexpr (BYTES >= 16) {
+#pragma unroll
+      for (int v = 0; v < BYTES / 16; ++v) {
+        const uint4 u = reinterpret_cast<const uint4*>(p)[v];
+        w[4 * v] = u.x; w[4 * v + 1] = u.y; w[4 * v + 2] = u.z; w[4 * v + 3] = u.w;
+      }
+    } else {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      w[0] = u.x; w[1] = u.y;
+    }
+  }
+  __device__ __forceinline__ float get(int i) const {
+    if constexpr (sizeof(T) == 4) {
+      return __uint_as_float(w[i]);
+    } else {
+      const uint32_t x = w[i >> 1];
+      return __uint_as_float((i & 1) ? (x & 0xFFFF0000u) : (x << 16));
+    }
+  }
+};
+
+// The raw inputs one thread fetches for one token of a chunk: entries
+// [E*p, E*p + E) of q and k, value columns [4p, 4p+4) of the CTA's block.
+template <int DK, class IO>
+struct Fetch {
+  RawVec<IO, DK / 8> q, k;
+  RawVec<IO, 4> v;
   float a, b;
 };
 
-template <int DK, class IO, class ST>
-__device__ __forceinline__ void load_token(TokenIn<DK / 8>& in, const IO* row, const IO* a_ptr,
-                                           const IO* b_ptr, int kh, int h, const Geom& G,
-                                           const int* col, int r8) {
+template <int DK, class IO>
+__device__ __forceinline__ void fetch(Fetch<DK, IO>& f, const RowSrc<IO>& src, int t, int n_t,
+                                      int p, int kh, int h, int cb, const Geom& G) {
+  constexpr int PE = DK / 8;
+  if (t >= n_t) return;
+  const IO* row = src.rows + (size_t)t * src.row_stride;
+  f.q.load(row + (size_t)kh * DK + PE * p);
+  f.k.load(row + (size_t)G.Hk * DK + (size_t)kh * DK + PE * p);
+  f.v.load(row + 2 * (size_t)G.Hk * DK + (size_t)h * G.Dv + cb * kBV + 4 * p);
+  if (p == 0) {
+    f.a = to_f(src.a[(size_t)t * src.ab_stride]);
+    f.b = to_f(src.b[(size_t)t * src.ab_stride]);
+  }
+}
+
+// Normalise and publish one fetched token (8 threads per token).
+template <int DK, class IO>
+__device__ __forceinline__ void publish(Stage<DK>& st, const Fetch<DK, IO>& f, int t, int n_t,
+                                        int p, int h, const Params& P) {
+  constexpr int PE = DK / 8;
+  if (t >= n_t) return;  // whole 8-lane groups take this branch together
+  float fq[PE], fk[PE];
+#pragma unroll
+  for (int e = 0; e < PE; ++e) {
+    fq[e] = f.q.get(e);
+    fk[e] = f.k.get(e);
+  }
+  float qq = 0.0f, kk = 0.0f, qk = 0.0f;
+#pragma unroll
+  for (int e = 0; e < PE; ++e) {
+    qq = __fmaf_rn(fq[e], fq[e], qq);
+    kk = __fmaf_rn(fk[e], fk[e], kk);
+    qk = __fmaf_rn(fq[e], fk[e], qk);
+  }
+  const unsigned grp = 0xFFu << (threadIdx.x & 24);
+#pragma unroll
+  for (int d = 1; d < 8; d <<= 1) {
+    qq = __fadd_rn(qq, __shfl_xor_sync(grp, qq, d));
+    kk = __fadd_rn(kk, __shfl_xor_sync(grp, kk, d));
+    qk = __fadd_rn(qk, __shfl_xor_sync(grp, qk, d));
+  }
+  const float iq = rsqrtf(__fadd_rn(qq, P.eps));
+  const float ik = rsqrtf(__fadd_rn(kk, P.eps));
+#pragma unroll
+  for (int e = 0; e < PE; e += 4) {
+    *reinterpret_cast<float4*>(&st.q[t][PE * p + e]) =
+        make_float4(__fmul_rn(fq[e], iq), __fmul_rn(fq[e + 1], iq), __fmul_rn(fq[e + 2], iq),
+                    __fmul_rn(fq[e + 3], iq));
+    *reinterpret_cast<float4*>(&st.k[t][PE * p + e]) =
+        make_float4(__fmul_rn(fk[e], ik), __fmul_rn(fk[e + 1], ik), __fmul_rn(fk[e + 2], ik),
+                    __fmul_rn(fk[e + 3], ik));
+  }
+  *reinterpret_cast<float4*>(&st.v[t][4 * p]) =
+      make_float4(f.v.get(0), f.v.get(1), f.v.get(2), f.v.get(3));
+  if (p == 0) {
+    float alpha, beta;
+    gates(P, h, f.a, f.b, alpha, beta);
+    st.sc[t] = make_float4(alpha, beta, __fmul_rn(__fmul_rn(qk, iq), ik), 0.0f);
+  }
+}
+
+// The state of a lane: M columns x E entries as float2 pairs.
+template <int E>
+struct LaneState {
+  float2 s[kColsPerLane][E / 2];
+};
+
+// One token for one lane. Returns this lane's output column value in o (the
+// lanes with (r8 & 3) == 0 own column m = r8 >> 2 of their group).
+template <int DK, class ST>
+__device__ __forceinline__ float token_step(LaneState<DK / 8>& S, const Stage<DK>& st, int t, int r8,
+                                            int vcol, float scale, bool update) {
   using L = LaneMap<DK, ST>;
-  const IO* qp = row + (size_t)kh * DK;
-  const IO* kp = row + (size_t)G.Hk * DK + (size_t)kh * DK;
+  constexpr int E = DK / 8;
+  float2 q2[E / 2], k2[E / 2];
 #pragma unroll
   for (int i = 0; i < L::NI; ++i) {
-    load_f<IO, L::VEC>(qp + L::idx(r8, i), in.q + i * L::VEC);
-    load_f<IO, L::VEC>(kp + L::idx(r8, i), in.k + i * L::VEC);
-  }
-  const IO* vp = row + 2 * (size_t)G.Hk * DK + (size_t)h * G.Dv;
 #pragma unroll
-  for (int m = 0; m < kColsPerLane; ++m) in.v[m] = to_f(vp[col[m]]);
-  in.a = to_f(*a_ptr);
-  in.b = to_f(*b_ptr);
+    for (int e = 0; e < L::VEC; e += 4) {
+      const float4 qv = *reinterpret_cast<const float4*>(&st.q[t][L::idx(r8, i) + e]);
+      const float4 kv = *reinterpret_cast<const float4*>(&st.k[t][L::idx(r8, i) + e]);
+      q2[(i * L::VEC + e) / 2] = make_float2(qv.x, qv.y);
+      q2[(i * L::VEC + e) / 2 + 1] = make_float2(qv.z, qv.w);
+      k2[(i * L::VEC + e) / 2] = make_float2(kv.x, kv.y);
+      k2[(i * L::VEC + e) / 2 + 1] = make_float2(kv.z, kv.w);
+    }
+  }
+  const float4 sc = st.sc[t];
+  const float alpha = sc.x, beta = sc.y, kq = sc.z;
+  const float2 vv = *reinterpret_cast<const float2*>(&st.v[t][vcol]);
+
+  float2 ak0 = make_float2(0.f, 0.f), aq0 = ak0, ak1 = ak0, aq1 = ak0;
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j) {
+    ak0 = __ffma2_rn(S.s[0][j], k2[j], ak0);
+    aq0 = __ffma2_rn(S.s[0][j], q2[j], aq0);
+    ak1 = __ffma2_rn(S.s[1][j], k2[j], ak1);
+    aq1 = __ffma2_rn(S.s[1][j], q2[j], aq1);
+  }
+  // the four partial sums of this lane
+  const float v0 = __fadd_rn(ak0.x, ak0.y), v1 = __fadd_rn(aq0.x, aq0.y);
+  const float v2 = __fadd_rn(ak1.x, ak1.y), v3 = __fadd_rn(aq1.x, aq1.y);
+  // transpose-reduce over the 8 lanes of the group: afterwards lanes with
+  // bit 2 = m hold the full sums of column m (sk if bit 1 = 0, sq if 1)
+  const bool b2 = (r8 & 4) != 0, b1 = (r8 & 2) != 0;
+  float a0 = b2 ? v2 : v0, a1 = b2 ? v3 : v1;
+  const float s0 = b2 ? v0 : v2, s1 = b2 ? v1 : v3;
+  a0 = __fadd_rn(a0, __shfl_xor_sync(0xffffffffu, s0, 4));
+  a1 = __fadd_rn(a1, __shfl_xor_sync(0xffffffffu, s1, 4));
+  float kept = b1 ? a1 : a0;
+  const float sent = b1 ? a0 : a1;
+  kept = __fadd_rn(kept, __shfl_xor_sync(0xffffffffu, sent, 2));
+  kept = __fadd_rn(kept, __shfl_xor_sync(0xffffffffu, kept, 1));
+  const float other = __shfl_xor_sync(0xffffffffu, kept, 2);
+  const float sk = b1 ? other : kept;
+  const float sq = b1 ? kept : other;
+  const float vm = b2 ? vv.y : vv.x;
+  const float u = __fmul_rn(beta, __fsub_rn(vm, __fmul_rn(alpha, sk)));
+  const float o = __fmul_rn(scale, __fmaf_rn(u, kq, __fmul_rn(alpha, sq)));
+  if (update) {
+    const float u_x = __shfl_xor_sync(0xffffffffu, u, 4);
+    const float u0 = b2 ? u_x : u, u1 = b2 ? u : u_x;
+    const float2 al = make_float2(alpha, alpha);
+    const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
+#pragma unroll
+    for (int j = 0; j < E / 2; ++j) {
+      S.s[0][j] = __ffma2_rn(k2[j], uu0, __fmul2_rn(al, S.s[0][j]));
+      S.s[1][j] = __ffma2_rn(k2[j], uu1, __fmul2_rn(al, S.s[1][j]));
+    }
+  }
+  return o;
 }
 
-// The step. S is updated in place when `update`; o receives the outputs of
-// the lane's columns (identical on the 8 lanes of a group).
+template <int DK, class ST>
+__device__ __forceinline__ void load_state(LaneState<DK / 8>& S, const ST* base, const int* col,
+                                           int r8) {
+  using L = LaneMap<DK, ST>;
+#pragma unroll
+  for (int m = 0; m < kColsPerLane; ++m)
+#pragma unroll
+    for (int i = 0; i < L::NI; ++i)
+      load_f<ST, L::VEC>(base + (size_t)col[m] * DK + L::idx(r8, i),
+                         reinterpret_cast<float*>(&S.s[m][0]) + i * L::VEC);
+}
+
+template <int DK, class ST>
+__device__ __forceinline__ void store_state(ST* base, const LaneState<DK / 8>& S, const int* col,
+                                            int r8) {
+  using L = LaneMap<DK, ST>;
+#pragma unroll
+  for (int m = 0; m < kColsPerLane; ++m)
+#pragma unroll
+    for (int i = 0; i < L::NI; ++i)
+      store_f<ST, L::VEC>(base + (size_t)col[m] * DK + L::idx(r8, i),
+                          reinterpret_cast<const float*>(&S.s[m][0]) + i * L::VEC);
+}
+
 template <int E>
-__device__ __forceinline__ void token_step(float (&S)[kColsPerLane][E], const TokenIn<E>& in,
-                                           float alpha, float beta, float scale, float eps,
-                                           bool update, float (&o)[kColsPerLane]) {
-  float kk = 0.0f, qq = 0.0f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    kk = __fmaf_rn(in.k[e], in.k[e], kk);
-    qq = __fmaf_rn(in.q[e], in.q[e], qq);
-  }
-  kk = group8_sum(kk);
-  qq = group8_sum(qq);
-  const float ik = rsqrtf(__fadd_rn(kk, eps));
-  const float iq = rsqrtf(__fadd_rn(qq, eps));
-  float kh[E], qh[E];
-  float kq = 0.0f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    kh[e] = __fmul_rn(in.k[e], ik);
-    qh[e] = __fmul_rn(in.q[e], iq);
-    kq = __fmaf_rn(kh[e], qh[e], kq);
-  }
-  kq = group8_sum(kq);
-#pragma unroll
-  for (int m = 0; m < kColsPerLane; ++m) {
-    float sk = 0.0f, sq = 0.0f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      sk = __fmaf_rn(S[m][e], kh[e], sk);
-      sq = __fmaf_rn(S[m][e], qh[e], sq);
-    }
-    sk = group8_sum(sk);
-    sq = group8_sum(sq);
-    const float u = __fmul_rn(beta, __fsub_rn(in.v[m], __fmul_rn(alpha, sk)));
-    o[m] = __fmul_rn(scale, __fmaf_rn(u, kq, __fmul_rn(alpha, sq)));
-    if (update) {
-#pragma unroll
-      for (int e = 0; e < E; ++e) S[m][e] = __fmaf_rn(kh[e], u, __fmul_rn(alpha, S[m][e]));
-    }
-  }
-}
-
-template <int DK, class ST>
-__device__ __forceinline__ void load_state(float (&S)[kColsPerLane][DK / 8], const ST* base,
-                                           const int* col, int r8) {
-  using L = LaneMap<DK, ST>;
+__device__ __forceinline__ void zero_state(LaneState<E>& S) {
 #pragma unroll
   for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
-    for (int i = 0; i < L::NI; ++i)
-      load_f<ST, L::VEC>(base + (size_t)col[m] * DK + L::idx(r8, i), &S[m][i * L::VEC]);
-}
-
-template <int DK, class ST>
-__device__ __forceinline__ void store_state(ST* base, const float (&S)[kColsPerLane][DK / 8],
-                                            const int* col, int r8) {
-  using L = LaneMap<DK, ST>;
-#pragma unroll
-  for (int m = 0; m < kColsPerLane; ++m)
-#pragma unroll
-    for (int i = 0; i < L::NI; ++i)
-      store_f<ST, L::VEC>(base + (size_t)col[m] * DK + L::idx(r8, i), &S[m][i * L::VEC]);
+    for (int j = 0; j < E / 2; ++j) S.s[m][j] = make_float2(0.f, 0.f);
 }
 
 __device__ __forceinline__ void store_out(void* o, int out_f32, size_t off, float v) {
@@ -153,12 +275,56 @@ __device__ __forceinline__ void store_out(void* o, int out_f32, size_t off, floa
   else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
 }
 
+// Run n rows from `src` through the rule. Outputs go to o rows starting at
+// out_row (nullptr o: no outputs). The state is updated for every row but
+// the last when !update_last. `keep` is called after each row with the row
+// index (the slot layout stores the state there).
+template <int DK, class IO, class ST, class AfterRow>
+__device__ __forceinline__ void run_rows(LaneState<DK / 8>& S, Stage<DK>& st, const RowSrc<IO>& src,
+                                         int n, void* o, int out_f32, size_t out_row, int h,
+                                         int cb, int kh, const Geom& G, const Params& P,
+                                         bool update_last, AfterRow after_row) {
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31, cg = lane >> 3, r8 = lane & 7;
+  const int vcol = warp * 8 + cg * 2;                   // first of the lane's 2 columns
+  const int ft = tid >> 3, fp = tid & 7;                // fetch: token, part
+  Fetch<DK, IO> f;
+  fetch<DK, IO>(f, src, ft, n, fp, kh, h, cb, G);
+  for (int c0 = 0; c0 < n; c0 += kTC) {
+    const int n_t = min(kTC, n - c0);
+    __syncthreads();                                    // previous chunk fully read
+    publish<DK, IO>(st, f, ft, n_t, fp, h, P);
+    __syncthreads();
+    if (c0 + kTC < n) {                                 // prefetch the next chunk
+      RowSrc<IO> nx = src;
+      nx.rows += (size_t)(c0 + kTC) * src.row_stride;
+      nx.a += (size_t)(c0 + kTC) * src.ab_stride;
+      nx.b += (size_t)(c0 + kTC) * src.ab_stride;
+      fetch<DK, IO>(f, nx, ft, n - c0 - kTC, fp, kh, h, cb, G);
+    }
+    for (int t = 0; t < n_t; ++t) {
+      const bool upd = update_last || (c0 + t + 1 < n);
+      const float ov = token_step<DK, ST>(S, st, t, r8, vcol, P.scale, upd);
+      if (o != nullptr && (r8 & 3) == 0) {
+        const size_t off = ((out_row + c0 + t) * G.Hv + h) * G.Dv + cb * kBV + vcol + (r8 >> 2);
+        store_out(o, out_f32, off, ov);
+      }
+      after_row(c0 + t);
+    }
+  }
+}
+
+struct NoAfter {
+  __device__ void operator()(int) const {}
+};
+
 template <class IO, class ST, int DK, int MODE>
-__global__ void __launch_bounds__(kRuleWarps * 32)
+__global__ void __launch_bounds__(kRuleThreads)
 rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
             const IO* __restrict__ a_in, const IO* __restrict__ b_in, void* o, int out_f32,
             void* pages, int32_t* status) {
   constexpr int E = DK / 8;
+  __shared__ __align__(16) Stage<DK> st;
   const int nCB = G.Dv / kBV;
   const int h = blockIdx.x / nCB;
   const int cb = blockIdx.x % nCB;
@@ -176,13 +342,16 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
   const int cg = lane >> 3, r8 = lane & 7;
   int col[kColsPerLane];
 #pragma unroll
-  for (int m = 0; m < kColsPerLane; ++m) col[m] = cb * kBV + warp * 8 + m * 4 + cg;
+  for (int m = 0; m < kColsPerLane; ++m) col[m] = cb * kBV + warp * 8 + cg * 2 + m;
   const int kh = (int)(((long long)h * G.Hk) / G.Hv);
-  const float scale = P.scale;
 
-  float S[kColsPerLane][E];
-  float out[kColsPerLane];
-  TokenIn<E> in;
+  LaneState<E> S;
+  RowSrc<IO> rows_in;
+  rows_in.rows = qkv + (size_t)q.start * G.C;
+  rows_in.row_stride = G.C;
+  rows_in.a = a_in + (size_t)q.start * G.Hv + h;
+  rows_in.b = b_in + (size_t)q.start * G.Hv + h;
+  rows_in.ab_stride = G.Hv;
 
   if constexpr (MODE == MODE_SEQ) {
     char* pg = page_ptr(G, pages, q.page);
@@ -193,35 +362,13 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
     }
     ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
     if (q.fresh) {
-#pragma unroll
-      for (int m = 0; m < kColsPerLane; ++m)
-#pragma unroll
-        for (int e = 0; e < E; ++e) S[m][e] = 0.0f;
+      zero_state<E>(S);
     } else {
       if (q.len == 0) return;  // nothing to do
       load_state<DK, ST>(S, Sb, col, r8);
     }
-    if (q.len > 0) {
-      const IO* row0 = qkv + (size_t)q.start * G.C;
-      load_token<DK, IO, ST>(in, row0, a_in + (size_t)q.start * G.Hv + h,
-                             b_in + (size_t)q.start * G.Hv + h, kh, h, G, col, r8);
-    }
-    for (int t = 0; t < q.len; ++t) {
-      const TokenIn<E> cur = in;
-      if (t + 1 < q.len) {
-        const size_t rn = (size_t)q.start + t + 1;
-        load_token<DK, IO, ST>(in, qkv + rn * G.C, a_in + rn * G.Hv + h, b_in + rn * G.Hv + h, kh,
-                               h, G, col, r8);
-      }
-      float alpha, beta;
-      gates(P, h, cur.a, cur.b, alpha, beta);
-      token_step<E>(S, cur, alpha, beta, scale, P.eps, true, out);
-      if (r8 == 0) {
-        const size_t off = ((size_t)(q.start + t) * G.Hv + h) * G.Dv;
-#pragma unroll
-        for (int m = 0; m < kColsPerLane; ++m) store_out(o, out_f32, off + col[m], out[m]);
-      }
-    }
+    run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P, true,
+                         NoAfter());
     store_state<DK, ST>(Sb, S, col, r8);
     if (q.fresh && blockIdx.x == 0 && threadIdx.x == 0) *flagp = 0u;  // empty record
   } else if constexpr (MODE == MODE_VERIFY) {
@@ -235,42 +382,32 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
       return;
     }
     ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
-    const IO* rec = reinterpret_cast<const IO*>(pg + G.record_off);
+    IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
     load_state<DK, ST>(S, Sb, col, r8);
     if (ss.width > 0) {
       // replay rows 0..a of the live slot, then store the checkpoint
-      const IO* slot = rec + (size_t)ss.live * G.Kc * G.rec_row;
-      for (int i = 0; i <= ss.accepted; ++i) {
-        const IO* row = slot + (size_t)i * G.rec_row;
-        load_token<DK, IO, ST>(in, row, row + G.C + h, row + G.C + G.Hv + h, kh, h, G, col, r8);
-        float alpha, beta;
-        gates(P, h, in.a, in.b, alpha, beta);
-        token_step<E>(S, in, alpha, beta, scale, P.eps, true, out);
-      }
+      RowSrc<IO> rp;
+      rp.rows = rec + (size_t)ss.live * G.Kc * G.rec_row;
+      rp.row_stride = G.rec_row;
+      rp.a = rp.rows + G.C + h;
+      rp.b = rp.rows + G.C + G.Hv + h;
+      rp.ab_stride = G.rec_row;
+      run_rows<DK, IO, ST>(S, st, rp, ss.accepted + 1, nullptr, out_f32, 0, h, cb, kh, G, P, true,
+                           NoAfter());
       store_state<DK, ST>(Sb, S, col, r8);
       // continue from exactly what was stored (a bf16 page rounds here)
 #pragma unroll
       for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
-        for (int e = 0; e < E; ++e) S[m][e] = through<ST>(S[m][e]);
+        for (int j = 0; j < E / 2; ++j)
+          S.s[m][j] = make_float2(through<ST>(S.s[m][j].x), through<ST>(S.s[m][j].y));
     }
     // this step's candidates: outputs only, no per-candidate state
-    for (int t = 0; t < q.len; ++t) {
-      const size_t rn = (size_t)q.start + t;
-      load_token<DK, IO, ST>(in, qkv + rn * G.C, a_in + rn * G.Hv + h, b_in + rn * G.Hv + h, kh,
-                             h, G, col, r8);
-      float alpha, beta;
-      gates(P, h, in.a, in.b, alpha, beta);
-      token_step<E>(S, in, alpha, beta, scale, P.eps, t + 1 < q.len, out);
-      if (r8 == 0) {
-        const size_t off = (rn * G.Hv + h) * G.Dv;
-#pragma unroll
-        for (int m = 0; m < kColsPerLane; ++m) store_out(o, out_f32, off + col[m], out[m]);
-      }
-    }
+    run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P,
+                         false, NoAfter());
     // the candidates' gates go next to their conv'd rows in the other slot
     if (cb == 0 && threadIdx.x < q.len) {
-      IO* row = const_cast<IO*>(rec) + ((size_t)(1 - ss.live) * G.Kc + threadIdx.x) * G.rec_row;
+      IO* row = rec + ((size_t)(1 - ss.live) * G.Kc + threadIdx.x) * G.rec_row;
       const size_t rn = (size_t)q.start + threadIdx.x;
       row[G.C + h] = a_in[rn * G.Hv + h];
       row[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
@@ -298,25 +435,18 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
       return;
     }
     char* pool = reinterpret_cast<char*>(pages) + (size_t)q.page * SG.pool_bytes;
-    auto slot_state = [&](int i) {
-      return reinterpret_cast<ST*>(pool + (size_t)i * SG.slot_bytes + SG.state_off) +
-             (size_t)h * G.Dv * DK;
+    const size_t slot_bytes = SG.slot_bytes, state_off = SG.state_off;
+    const size_t head_off = (size_t)h * G.Dv * DK;
+    load_state<DK, ST>(S, reinterpret_cast<ST*>(pool + (size_t)src * slot_bytes + state_off) + head_off,
+                       col, r8);
+    // store after every candidate: the same kernel instance stores rows in
+    // order, so a slot is written by the CTA that owns its columns only
+    auto keep = [&](int i) {
+      store_state<DK, ST>(reinterpret_cast<ST*>(pool + (size_t)i * slot_bytes + state_off) + head_off,
+                          S, col, r8);
     };
-    load_state<DK, ST>(S, slot_state(src), col, r8);
-    for (int t = 0; t < q.len; ++t) {
-      const size_t rn = (size_t)q.start + t;
-      load_token<DK, IO, ST>(in, qkv + rn * G.C, a_in + rn * G.Hv + h, b_in + rn * G.Hv + h, kh,
-                             h, G, col, r8);
-      float alpha, beta;
-      gates(P, h, in.a, in.b, alpha, beta);
-      token_step<E>(S, in, alpha, beta, scale, P.eps, true, out);
-      if (r8 == 0) {
-        const size_t off = (rn * G.Hv + h) * G.Dv;
-#pragma unroll
-        for (int m = 0; m < kColsPerLane; ++m) store_out(o, out_f32, off + col[m], out[m]);
-      }
-      store_state<DK, ST>(slot_state(t), S, col, r8);
-    }
+    run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P, true,
+                         keep);
   }
 }
 
@@ -326,7 +456,7 @@ cudaError_t launch_rule_dk(int mode, const Geom& G, const Batch& B, const Params
                            const void* qkv, const void* a, const void* b, void* o, void* pages,
                            int32_t* status, cudaStream_t stream) {
   dim3 grid(G.Hv * (G.Dv / kBV), B.R);
-  dim3 block(kRuleWarps * 32);
+  dim3 block(kRuleThreads);
 #define GDN_RULE_LAUNCH(IO, ST, MODE)                                                         \
   rule_kernel<IO, ST, DK, MODE><<<grid, block, 0, stream>>>(                                  \
       G, B, P, SG, static_cast<const IO*>(qkv), static_cast<const IO*>(a),                   \
