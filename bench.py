@@ -354,6 +354,7 @@ def extra_workloads(device, peaks, args, only=None):
                      ("spec_verify_bf16_state", lambda: bench_spec(device, peaks, "bf16")),
                      ("mixed_prefill_spec", lambda: bench_mixed(device, peaks)),
                      ("long_prefill_token_by_token", lambda: bench_long_seq(device, peaks)),
+                     ("long_prefill_chunked", lambda: bench_long_chunk(device, peaks)),
                      ("conv_long_rows", lambda: bench_conv_long(device, peaks))):
         if only is not None and name != only:
             continue
@@ -566,6 +567,53 @@ def bench_long_seq(device, peaks, K=3, W=3):
     return {"workload": "long prefill: 4 x 8192 tokens through conv + token-by-token rule",
             "ms_per_step": el / K * 1e3, "tokens_per_s": T * K / el, "seq_ms": seq_ms,
             "seq_us_per_token_chain": seq_ms * 1e3 / int(d["row_len"][0]),
+            "status": int(status.item())}
+
+
+# Algorithmic flops of one full 64-token chunk of one head (Dk = Dv = 128):
+# [Q;K]K^T 2*128*64*128, W and U 2*(2*128*64*64), WS and QS 2*(2*128*64*128),
+# P Vn 2*128*64*64, state update 2*128*128*64.
+CHUNK_FLOPS = 2 * 128 * 64 * 128 + 2 * (2 * 128 * 64 * 64) + 2 * (2 * 128 * 64 * 128) \
+    + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64
+
+
+def bench_long_chunk(device, peaks, K=5, W=3):
+    """4 x 8192-token prefill through the tensor-core chunked form."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import PagePool
+    d = synth.long()
+    sh, R, T = d["shapes"], d["R"], d["T"]
+    dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 0, gdn.GDN_BF16, gdn.GDN_F32,
+                         gdn.GDN_BF16)
+    A_log = torch.from_numpy(d["A_log"]).to(device)
+    dt = torch.from_numpy(d["dt_bias"]).to(device)
+    params = gdn.make_params(A_log, dt)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    pool = PagePool(dims, R, device=device)
+    x, a, b = (_put_io(torch, device, d[k]) for k in ("x", "a", "b"))
+    o = torch.empty(T, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+    B = _dev_batch(gdn, torch, device, d["row_start"], d["row_len"], np.arange(R),
+                   np.full(R, gdn.GDN_REQ_FRESH))
+    ws_bytes = gdn.gdn_chunk_prefill_workspace_bytes(dims, B)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
+
+    def launch(i):
+        gdn.gdn_chunk_prefill(dims, B, params, x, a, b, o, pool.buf, ws, ws_bytes, status)
+
+    for i in range(W):
+        launch(i)
+    torch.cuda.synchronize()
+    el = time_steps(launch, K, torch)
+    chunks = R * (T // R // 64)
+    flops = chunks * sh.Hv * CHUNK_FLOPS
+    tf = flops / (el / K) / 1e12
+    return {"workload": "long prefill: 4 x 8192 tokens, chunk 64, tensor-core WY form (rule only; "
+                        "rows are conv'd bf16 N(0,1))",
+            "ms_per_launch": el / K * 1e3, "tokens_per_s": T * K / el,
+            "algorithmic_tflops": tf, "tensor_peak_tflops": float(peaks["bf16_tflops"]),
+            "frac_of_tensor_peak": tf / float(peaks["bf16_tflops"]),
+            "issued_mma_flops_per_chunk_head": 24117248,
             "status": int(status.item())}
 
 

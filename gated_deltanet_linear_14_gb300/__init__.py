@@ -30,6 +30,7 @@ STATUS = {
     -4: "GDN_ERR_WORKSPACE", -5: "GDN_ERR_NO_DEVICE", 1: "GDN_DEV_BAD_PAGE",
     2: "GDN_DEV_BAD_ROWS", 3: "GDN_DEV_BAD_ACCEPTED", 4: "GDN_DEV_STALE_STEP",
     5: "GDN_DEV_TOO_MANY_CANDIDATES", 6: "GDN_DEV_RECORD_OPEN", 7: "GDN_DEV_BAD_FLAG",
+    8: "GDN_DEV_TIMEOUT",
 }
 CODES = {v: k for k, v in STATUS.items()}
 

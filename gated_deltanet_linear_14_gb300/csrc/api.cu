@@ -1,8 +1,12 @@
 // C ABI of the GDN layer core: host-side validation, layouts and launches.
 // Every entry point checks its arguments completely before launching, so a
 // negative return means nothing was launched and nothing was written.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "gdn.h"
 #include "kernels.h"
@@ -158,6 +162,40 @@ gdn_status rule_entry(int mode, const gdn_dims* dims, const gdn_batch* batch,
   return GDN_OK;
 }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link-time
+// dependency on libcuda). The only process-wide value the library keeps.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// TMA descriptor of the packed rows [num_rows][C] bf16: boxes of 64 rows x
+// 64 channels (128 bytes), 128-byte swizzle, zero fill past the last row.
+gdn_status encode_rows_tmap(CUtensorMap* tm, const void* rows, int num_rows, const gdn_dims* d) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  if (!enc) return GDN_ERR_NO_DEVICE;
+  const cuuint64_t C = 2 * (cuuint64_t)d->num_k_heads * d->head_k_dim +
+                       (cuuint64_t)d->num_v_heads * d->head_v_dim;
+  cuuint64_t gdim[2] = {C, (cuuint64_t)num_rows};
+  cuuint64_t gstride[1] = {C * 2};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estride[2] = {1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(rows), gdim,
+                         gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_UNSUPPORTED;
+}
+
 }  // namespace
 
 extern "C" {
@@ -247,13 +285,32 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch, const
                              const void* qkv, const void* a, const void* b, void* o, void* pages,
                              void* workspace, size_t workspace_bytes, int32_t* status,
                              gdn_stream_t stream) {
-  (void)qkv; (void)a; (void)b; (void)o; (void)pages; (void)workspace; (void)workspace_bytes;
-  (void)status; (void)stream;
+  (void)workspace;
+  (void)workspace_bytes;
   gdn_status e = check_dims(dims);
   if (e != GDN_OK) return e;
   if ((e = check_batch(batch, true)) != GDN_OK) return e;
   if ((e = check_params(params, true)) != GDN_OK) return e;
-  return GDN_ERR_UNSUPPORTED;
+  if (dims->io_dtype != GDN_BF16 || dims->head_k_dim != 128 || dims->head_v_dim != 128)
+    return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages) return GDN_ERR_INVALID_ARG;
+  CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  if (batch->num_rows > 0) {
+    // with no rows every request has length 0 and the map is never read
+    if (!qkv || !a || !b || !o) return GDN_ERR_INVALID_ARG;
+    if (((uintptr_t)qkv & 15) != 0) return GDN_ERR_UNSUPPORTED;
+    const gdn_status te = encode_rows_tmap(&tmap, qkv, batch->num_rows, dims);
+    if (te != GDN_OK) return te;
+  }
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  if (launch_chunk(&tmap, G, B, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a, b,
+                   o, pages, status, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
 }
 
 const char* gdn_strerror(int32_t s) {
@@ -271,6 +328,7 @@ const char* gdn_strerror(int32_t s) {
     case GDN_DEV_TOO_MANY_CANDIDATES: return "device: more candidate rows than max_candidates";
     case GDN_DEV_RECORD_OPEN: return "device: plain rows on a page whose spec record is open";
     case GDN_DEV_BAD_FLAG: return "device: corrupt page flag word (or FRESH with SPEC)";
+    case GDN_DEV_TIMEOUT: return "device: a bounded on-chip wait gave up";
     default: return "unknown status";
   }
 }

@@ -1,0 +1,545 @@
+// Chunked prefill of the gated delta rule on the tcgen05 tensor cores
+// (sm_103a): the WY (UT-transform) chunk form, 64 tokens per chunk.
+//
+// r9700-stack v0.2.3, section 1, names the chunked GDN core used for prompts
+// above the token-by-token threshold and its numerics (solves on bf16 q/k
+// land at 5e-3 from an fp64 token-by-token reference). The chunk form is not
+// written out there; this is its standard statement. Per chunk with state S
+// (Dk x Dv), gamma_t = sum_{s<=t} g_s, k^/q^ the L2-normalised rows:
+//   A  = strictly_lower(beta_t e^{gamma_t-gamma_s} k^_t.k^_s),  T = (I+A)^-1
+//   W  = T diag(beta e^gamma) K^,   U = T diag(beta) V,   Vn = U - W S
+//   O  = scale (diag(e^gamma) Q^ S + (Q^ K^T o e^{gamma_t-gamma_s} o causal) Vn)
+//   S <- e^{gamma_L} S + (diag(e^{gamma_L-gamma}) K^)^T Vn
+//
+// Design. One CTA (4 warps) per (request, value head) walks the request's
+// chunks. Every contraction is an M = 128 tcgen05.mma with bf16 operands in
+// 128B-swizzled shared memory and fp32 accumulators in tensor memory; the
+// 128 rows are Dk or Dv (or the 64 q rows stacked on the 64 k rows), so each
+// thread owns one TMEM lane (one row) in every epilogue:
+//   MMA1  [Q;K] K^T          -> QK^T and KK^T (raw bf16: exact products);
+//                               |k_t|^2 is the diagonal of KK^T
+//   MMA2  K^T T_W^T          -> W^T   (T_W = T diag(beta e^gamma / |k|))
+//   MMA3  V^T T_U^T          -> U^T   (T_U = T diag(beta))
+//   MMA4  S^T W^T            -> (W S)^T
+//   MMA5  S^T Q^T            -> (Q S)^T
+//   MMA6  Vn^T P^T           -> (P Vn)^T   (P = masked, gated, normalised QK^T)
+//   MMA7  S^T += V'^T K      (V' = diag(e^{gamma_L-gamma} / |k|) Vn), on top
+//                               of e^{gamma_L} S written back into TMEM
+// Raw q/k/v are exact in bf16; every fp32 operand (T_W, T_U, S, W, Vn, P,
+// V') is split into bf16 hi + lo and the products summed (dropping lo x lo),
+// which keeps about 2^-16 relative accuracy: fp32-grade results from the
+// bf16 tensor pipe. The 64 x 64 unit-lower-triangular inverse T is computed
+// on the CUDA cores in 16 x 16 blocks. The state stays fp32 in TMEM for the
+// whole request. Tiles arrive by TMA (SWIZZLE_128B) straight into the
+// operand layout; the next chunk's tiles are fetched while the current
+// chunk's outputs are written.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "umma.cuh"
+
+namespace gdn {
+
+using namespace umma;
+
+constexpr int kCL = 64;               // tokens per chunk
+constexpr int kCD = 128;              // Dk = Dv
+constexpr int kChunkThreads = 128;
+
+// Shared memory map (bytes from a 1024-aligned base).
+constexpr uint32_t OFF_QK = 0;        // per 64-column atom a (a*16384): Q rows 0..63, K rows 64..127
+constexpr uint32_t OFF_V = 32768;     // V atom a at OFF_V + a*8192 (64 rows each)
+constexpr uint32_t OFF_P = 49152;     // P hi [64][64] | P lo
+constexpr uint32_t OFF_R1 = 65536;    // T_W hi | T_W lo | T_U hi | T_U lo (8 KB each)
+                                      //  -> Vn^T hi | lo ([128][64], 16 KB each); solve scratch
+constexpr uint32_t OFF_R2 = 98304;    // A, T fp32 [64][64] -> W^T hi | lo -> V'^T hi | lo
+constexpr uint32_t OFF_S = 131072;    // S^T hi: atom a at a*16384 ([128][64]); S^T lo at +32768
+constexpr uint32_t OFF_VEC = 196608;  // per-token vectors (5 x 64 floats)
+constexpr uint32_t kChunkSmem = OFF_VEC + 5 * 64 * 4 + 2048;  // + 1024-byte alignment slack
+
+// TMEM columns (512 allocated).
+constexpr uint32_t TM_D1 = 0, TM_W = 64, TM_U = 128, TM_WS = 192, TM_S = 256, TM_OQ = 384,
+                   TM_OP = 448;
+
+constexpr long long kWaitLimit = 1LL << 26;
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
+  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
+  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
+  return a | (b << 16);
+}
+
+// Write 64 fp32 values as row `row` of two [rows][64] SW128 bf16 tiles: the
+// bf16 rounding (hi) and the rounding of the remainder (lo).
+__device__ __forceinline__ void store_row_hilo(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                               const float* v) {
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = v[ch * 8 + 2 * e], x1 = v[ch * 8 + 2 * e + 1];
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+      h[e] = pack_bf16(h0, h1);
+      l[e] = pack_bf16(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
+    }
+    const uint32_t off = sw128_chunk(row, ch);
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// T = (I + A)^-1 for a strictly lower 64 x 64 A (row-major fp32, stride 64),
+// in 16 x 16 blocks: diagonal blocks by forward substitution (one thread per
+// block column), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj by block
+// distance. Xs: 3 x 256 floats of scratch. All 128 threads call this.
+__device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, float* Xs, int tid) {
+  if (tid < 64) {
+    const int b = tid >> 4, cc = tid & 15;
+    const float* Ab = Am + (16 * b) * 64 + 16 * b;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.0f : 0.0f;
+#pragma unroll
+    for (int r = 1; r < 16; ++r) {
+      float acc = 0.0f;
+#pragma unroll
+      for (int k = 0; k < r; ++k) acc = __fmaf_rn(Ab[r * 64 + k], x[k], acc);
+      if (r > cc) x[r] = -acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tm[(16 * b + r) * 64 + 16 * b + cc] = x[r];
+  } else {
+    // blocks above the diagonal are zero
+    for (int idx = tid - 64; idx < 6 * 256; idx += 64) {
+      const int blk = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+      const int bi = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
+      const int bj = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      Tm[(16 * bi + r) * 64 + 16 * bj + cc] = 0.0f;
+    }
+  }
+  __syncthreads();
+  for (int d = 1; d < 4; ++d) {
+    const int nb = 4 - d;
+    for (int idx = tid; idx < nb * 256; idx += kChunkThreads) {
+      const int bj = idx >> 8, bi = bj + d, r = (idx >> 4) & 15, cc = idx & 15;
+      float acc = 0.0f;
+      for (int k = 16 * bj; k < 16 * bi; ++k)
+        acc = __fmaf_rn(Am[(16 * bi + r) * 64 + k], Tm[k * 64 + 16 * bj + cc], acc);
+      Xs[idx] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nb * 256; idx += kChunkThreads) {
+      const int bj = idx >> 8, bi = bj + d, r = (idx >> 4) & 15, cc = idx & 15;
+      float acc = 0.0f;
+      for (int m = 0; m <= r; ++m)
+        acc = __fmaf_rn(Tm[(16 * bi + r) * 64 + 16 * bi + m], Xs[(bj << 8) + m * 16 + cc], acc);
+      Tm[(16 * bi + r) * 64 + 16 * bj + cc] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
+template <class ST>
+__global__ void __launch_bounds__(kChunkThreads, 1)
+chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params P,
+             const bf16* __restrict__ a_in, const bf16* __restrict__ b_in, void* o, int out_f32,
+             void* pages, int32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ uint32_t tmem_slot;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int h = blockIdx.x;
+  const bool reporter = (h == 0 && tid == 0);
+  const Req q = load_req(B, blockIdx.y);
+  if (q.err) {
+    if (reporter) report(status, q.err);
+    return;
+  }
+  if (q.spec) return;
+  char* pg = page_ptr(G, pages, q.page);
+  uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+  if (!q.fresh && flag_width(*flagp) != 0) {
+    if (reporter) report(status, GDN_DEV_RECORD_OPEN);
+    return;
+  }
+  if (!q.fresh && q.len == 0) return;
+  ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * kCD * kCD;
+  const int kh = (int)(((long long)h * G.Hk) / G.Hv);
+
+  float* s_g = reinterpret_cast<float*>(sm + OFF_VEC);
+  float* s_beta = s_g + 64;
+  float* s_gam = s_beta + 64;
+  float* s_iq = s_gam + 64;
+  float* s_ik = s_iq + 64;
+  float* Am = reinterpret_cast<float*>(sm + OFF_R2);
+  float* Tm = Am + 64 * 64;
+  float* Xs = reinterpret_cast<float*>(sm + OFF_R1);
+
+  const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+  if (tid == 0) {
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+  const uint32_t sb = smem_u32(sm);
+
+  // the initial state S^T (row j = tid) into TMEM
+  {
+    float v[32];
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      if (q.fresh) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+      } else {
+        load_f<ST, 32>(Sb + (size_t)tid * kCD + cc * 32, v);
+      }
+      tmem_st32(trow + TM_S + cc * 32, v);
+    }
+    tmem_st_wait();
+  }
+
+  const int nchunks = (q.len + kCL - 1) / kCL;
+  const int xq = kh * kCD, xk = G.Hk * kCD + kh * kCD, xv = 2 * G.Hk * kCD + h * G.Dv;
+  auto issue_tma = [&](int c) {
+    const int y = q.start + c * kCL;
+    mbar_expect_tx(bar_tma, 6 * 8192);
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      tma_load_2d(sb + OFF_QK + a * 16384, &tm_qkv, xq + 64 * a, y, bar_tma);
+      tma_load_2d(sb + OFF_QK + a * 16384 + 8192, &tm_qkv, xk + 64 * a, y, bar_tma);
+      tma_load_2d(sb + OFF_V + a * 8192, &tm_qkv, xv + 64 * a, y, bar_tma);
+    }
+  };
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && nchunks > 0) issue_tma(0);
+
+  uint32_t mma_count = 0;
+  bool fail = false;
+  auto wait_mma = [&]() -> bool {
+    const bool ok = mbar_wait(bar_mma, mma_count & 1, kWaitLimit);
+    ++mma_count;
+    const bool any_fail = __syncthreads_or(!ok);
+    tc_fence_after();
+    return !any_fail;
+  };
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int n_c = min(kCL, q.len - c * kCL);
+    const size_t R0 = (size_t)q.start + (size_t)c * kCL;
+    float a_t = 0.0f, b_t = 0.0f;
+    if (tid < n_c) {
+      a_t = to_f(a_in[(R0 + tid) * G.Hv + h]);
+      b_t = to_f(b_in[(R0 + tid) * G.Hv + h]);
+    }
+    {
+      const bool ok = mbar_wait(bar_tma, c & 1, kWaitLimit);
+      if (__syncthreads_or(!ok)) { fail = true; break; }
+    }
+    if (n_c < kCL) {
+      // rows past the request's end belong to other requests: zero them
+      const int nrow = kCL - n_c;
+      for (int idx = tid; idx < nrow * 6 * 8; idx += kChunkThreads) {
+        const int r = n_c + idx / 48, rest = idx % 48, tile = rest / 8, ch = rest % 8;
+        const uint32_t base = (tile < 4) ? OFF_QK + (tile >> 1) * 16384 + (tile & 1) * 8192
+                                         : OFF_V + (tile - 4) * 8192;
+        *reinterpret_cast<uint4*>(sm + base + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      }
+      fence_async_smem();
+    }
+    __syncthreads();
+
+    // MMA1: [Q;K] K^T
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t base = sb + OFF_QK + (ks >> 2) * 16384 + (ks & 3) * 32;
+        mma_bf16(tmem + TM_D1, sdesc(base, 16, 1024), sdesc(base + 8192, 16, 1024), id, ks > 0);
+      }
+      mma_commit(bar_mma);
+    }
+    // gates and q norms while it runs
+    if (tid < kCL) {
+      float g = 0.0f, beta = 0.0f;
+      if (tid < n_c) gate_log(P, h, a_t, b_t, g, beta);
+      s_g[tid] = g;
+      s_beta[tid] = beta;
+      float qq = 0.0f;
+#pragma unroll
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 u = *reinterpret_cast<const uint4*>(sm + OFF_QK + a * 16384 + sw128_chunk(tid, ch));
+          const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = __uint_as_float(w4[e] << 16), x1 = __uint_as_float(w4[e] & 0xFFFF0000u);
+            qq = __fmaf_rn(x0, x0, qq);
+            qq = __fmaf_rn(x1, x1, qq);
+          }
+        }
+      s_iq[tid] = rsqrtf(__fadd_rn(qq, P.eps));
+    }
+    __syncthreads();
+    if (tid < kCL) {
+      float gm = 0.0f;
+      for (int s = 0; s <= tid; ++s) gm = __fadd_rn(gm, s_g[s]);
+      s_gam[tid] = gm;
+    }
+    if (!wait_mma()) { fail = true; break; }
+
+    float row[64];
+    tmem_ld32(trow + TM_D1, row);
+    tmem_ld32(trow + TM_D1 + 32, row + 32);
+    if (tid >= kCL) {
+      const int t = tid - kCL;
+      float kk = 0.0f;
+#pragma unroll
+      for (int s = 0; s < 64; ++s) kk = (s == t) ? row[s] : kk;
+      s_ik[t] = rsqrtf(__fadd_rn(kk, P.eps));
+    }
+    __syncthreads();
+    const float gL = s_gam[kCL - 1];
+    if (tid < kCL) {
+      // P row t: masked, gated, normalised q_t . k_s  (s <= t < n_c)
+      const int t = tid;
+      const float iq = s_iq[t], gt = s_gam[t];
+#pragma unroll
+      for (int s = 0; s < 64; ++s)
+        row[s] = (s <= t && t < n_c)
+                     ? __fmul_rn(__fmul_rn(__fmul_rn(row[s], iq), s_ik[s]), expf(__fsub_rn(gt, s_gam[s])))
+                     : 0.0f;
+      store_row_hilo(sm + OFF_P, sm + OFF_P + 8192, t, row);
+    } else {
+      // A row t: beta_t e^{gamma_t - gamma_s} k^_t . k^_s for s < t
+      const int t = tid - kCL;
+      const float ikt = s_ik[t], gt = s_gam[t], bt = s_beta[t];
+#pragma unroll
+      for (int s = 0; s < 64; s += 4) {
+        float4 v;
+        float* vp = &v.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ss = s + e;
+          vp[e] = (ss < t && t < n_c)
+                      ? __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(row[ss], ikt), s_ik[ss]), bt),
+                                  expf(__fsub_rn(gt, s_gam[ss])))
+                      : 0.0f;
+        }
+        *reinterpret_cast<float4*>(&Am[t * 64 + s]) = v;
+      }
+    }
+    __syncthreads();
+    solve_unit_lower64(Am, Tm, Xs, tid);
+
+    // T_W = T diag(beta e^gamma / |k|), T_U = T diag(beta), hi/lo bf16 tiles
+    {
+      const int t = tid & 63;
+      float w[64];
+#pragma unroll
+      for (int s = 0; s < 64; s += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(&Tm[t * 64 + s]);
+        w[s] = v.x; w[s + 1] = v.y; w[s + 2] = v.z; w[s + 3] = v.w;
+      }
+      if (tid < kCL) {
+#pragma unroll
+        for (int s = 0; s < 64; ++s)
+          w[s] = __fmul_rn(w[s], __fmul_rn(__fmul_rn(s_beta[s], expf(s_gam[s])), s_ik[s]));
+        store_row_hilo(sm + OFF_R1, sm + OFF_R1 + 8192, t, w);
+      } else {
+#pragma unroll
+        for (int s = 0; s < 64; ++s) w[s] = __fmul_rn(w[s], s_beta[s]);
+        store_row_hilo(sm + OFF_R1 + 16384, sm + OFF_R1 + 24576, t, w);
+      }
+    }
+    fence_async_smem();
+    __syncthreads();
+    // MMA2: W^T = K^T T_W^T ; MMA3: U^T = V^T T_U^T
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + TM_W, sdesc(sb + OFF_QK + 8192 + ks * 2048, 16384, 1024),
+                   sdesc(sb + OFF_R1 + pass * 8192 + ks * 32, 16, 1024), id, (pass | ks) != 0);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + TM_U, sdesc(sb + OFF_V + ks * 2048, 8192, 1024),
+                   sdesc(sb + OFF_R1 + 16384 + pass * 8192 + ks * 32, 16, 1024), id, (pass | ks) != 0);
+      mma_commit(bar_mma);
+    }
+    // S^T hi/lo operand tiles, and e^{gamma_L} S^T back into TMEM for MMA7
+    {
+      const float eL = expf(gL);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float v[64];
+        tmem_ld32(trow + TM_S + half * 64, v);
+        tmem_ld32(trow + TM_S + half * 64 + 32, v + 32);
+        store_row_hilo(sm + OFF_S + half * 16384, sm + OFF_S + 32768 + half * 16384, tid, v);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) v[i] = __fmul_rn(v[i], eL);
+        tmem_st32(trow + TM_S + half * 64, v);
+        tmem_st32(trow + TM_S + half * 64 + 32, v + 32);
+      }
+      tmem_st_wait();
+    }
+    if (!wait_mma()) { fail = true; break; }
+
+    // W^T rows (MN-major B operand of MMA4)
+    {
+      float w[64];
+      tmem_ld32(trow + TM_W, w);
+      tmem_ld32(trow + TM_W + 32, w + 32);
+      store_row_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, w);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // MMA4: (W S)^T = S^T W^T (3 hi/lo passes) ; MMA5: (Q S)^T = S^T Q^T
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id4 = idesc_bf16(128, 64, 0, 1);
+      const int sel_s[3] = {0, 0, 1}, sel_w[3] = {0, 1, 0};
+#pragma unroll
+      for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(tmem + TM_WS,
+                   sdesc(sb + OFF_S + sel_s[pass] * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                   sdesc(sb + OFF_R2 + sel_w[pass] * 16384 + ks * 2048, 16384, 1024), id4,
+                   (pass | ks) != 0);
+      const uint32_t id5 = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_bf16(tmem + TM_OQ,
+                   sdesc(sb + OFF_S + pass * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
+                   sdesc(sb + OFF_QK + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id5,
+                   (pass | ks) != 0);
+      mma_commit(bar_mma);
+    }
+    if (!wait_mma()) { fail = true; break; }
+
+    // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
+    {
+      float u[64], ws[64];
+      tmem_ld32(trow + TM_U, u);
+      tmem_ld32(trow + TM_U + 32, u + 32);
+      tmem_ld32(trow + TM_WS, ws);
+      tmem_ld32(trow + TM_WS + 32, ws + 32);
+#pragma unroll
+      for (int s = 0; s < 64; ++s) u[s] = __fsub_rn(u[s], ws[s]);
+      store_row_hilo(sm + OFF_R1, sm + OFF_R1 + 16384, tid, u);
+#pragma unroll
+      for (int s = 0; s < 64; ++s)
+        u[s] = __fmul_rn(u[s], __fmul_rn(expf(__fsub_rn(gL, s_gam[s])), s_ik[s]));
+      store_row_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, u);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // MMA6: (P Vn)^T = Vn^T P^T ; MMA7: S^T += V'^T K
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id6 = idesc_bf16(128, 64, 0, 0);
+      const int sel_v[3] = {0, 0, 1}, sel_p[3] = {0, 1, 0};
+#pragma unroll
+      for (int pass = 0; pass < 3; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + TM_OP, sdesc(sb + OFF_R1 + sel_v[pass] * 16384 + ks * 32, 16, 1024),
+                   sdesc(sb + OFF_P + sel_p[pass] * 8192 + ks * 32, 16, 1024), id6,
+                   (pass | ks) != 0);
+      const uint32_t id7 = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + TM_S, sdesc(sb + OFF_R2 + pass * 16384 + ks * 32, 16, 1024),
+                   sdesc(sb + OFF_QK + 8192 + ks * 2048, 16384, 1024), id7, 1u);
+      mma_commit(bar_mma);
+    }
+    if (!wait_mma()) { fail = true; break; }
+    if (tid == 0 && c + 1 < nchunks) issue_tma(c + 1);
+
+    // outputs: O[t][j] = scale (e^{gamma_t} |q_t|^-1 (S^T Q^T)[j][t] + (Vn^T P^T)[j][t])
+    {
+      float oq[64], op[64];
+      tmem_ld32(trow + TM_OQ, oq);
+      tmem_ld32(trow + TM_OQ + 32, oq + 32);
+      tmem_ld32(trow + TM_OP, op);
+      tmem_ld32(trow + TM_OP + 32, op + 32);
+#pragma unroll
+      for (int t = 0; t < 64; ++t) {
+        if (t < n_c) {
+          const float v = __fmul_rn(P.scale, __fmaf_rn(__fmul_rn(expf(s_gam[t]), s_iq[t]), oq[t], op[t]));
+          const size_t off = ((R0 + t) * G.Hv + h) * G.Dv + tid;
+          if (out_f32) reinterpret_cast<float*>(o)[off] = v;
+          else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  if (!fail) {
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      float v[32];
+      tmem_ld32(trow + TM_S + cc * 32, v);
+      store_f<ST, 32>(Sb + (size_t)tid * kCD + cc * 32, v);
+    }
+    if (q.fresh && h == 0 && tid == 0) *flagp = 0u;  // empty record
+  } else if (tid == 0) {
+    report(status, GDN_DEV_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const Params& P,
+                         int state_bf16, int out_f32, const void* a, const void* b, void* o,
+                         void* pages, int32_t* status, cudaStream_t stream) {
+  const CUtensorMap& tm = *static_cast<const CUtensorMap*>(tmap);
+  dim3 grid(G.Hv, B.R);
+  if (state_bf16) {
+    cudaError_t e = cudaFuncSetAttribute(chunk_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kChunkSmem);
+    if (e != cudaSuccess) return e;
+    chunk_kernel<bf16><<<grid, kChunkThreads, kChunkSmem, stream>>>(
+        tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
+        status);
+  } else {
+    cudaError_t e = cudaFuncSetAttribute(chunk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kChunkSmem);
+    if (e != cudaSuccess) return e;
+    chunk_kernel<float><<<grid, kChunkThreads, kChunkSmem, stream>>>(
+        tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
+        status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -248,4 +248,19 @@ __device__ __forceinline__ void gates(const Params& P, int h, float a_in, float 
   beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
 }
 
+// g (the log decay) and beta, for the chunked form (which works with
+// prefix sums of g rather than with e^g).
+__device__ __forceinline__ void gate_log(const Params& P, int h, float a_in, float b_in, float& g,
+                                         float& beta) {
+  if (P.gate_mode == 1) {
+    g = a_in;
+    beta = b_in;
+    return;
+  }
+  const float x = __fadd_rn(a_in, P.dt_bias[h]);
+  const float sp = (x > 20.0f) ? x : log1pf(expf(x));
+  g = -__fmul_rn(expf(P.A_log[h]), sp);
+  beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
+}
+
 }  // namespace gdn

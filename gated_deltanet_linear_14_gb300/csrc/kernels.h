@@ -22,6 +22,12 @@ cudaError_t launch_rule(int mode, const Geom& G, const Batch& B, const Params& P
                         const void* qkv, const void* a, const void* b, void* o, void* pages,
                         int32_t* status, cudaStream_t stream);
 
+// Chunked prefill on the tensor cores; tmap points to the CUtensorMap of
+// the packed qkv rows ([num_rows][C] bf16, box 64 x 64, 128B swizzle).
+cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const Params& P,
+                         int state_bf16, int out_f32, const void* a, const void* b, void* o,
+                         void* pages, int32_t* status, cudaStream_t stream);
+
 // per head dimension (one translation unit each)
 cudaError_t launch_rule_d32(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
                             int, int, int, const void*, const void*, const void*, void*, void*,

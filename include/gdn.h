@@ -90,7 +90,9 @@ typedef enum {
   GDN_DEV_STALE_STEP = 4,     /* page parity differs from the request's bit  */
   GDN_DEV_TOO_MANY_CANDIDATES = 5, /* spec row count above max_candidates   */
   GDN_DEV_RECORD_OPEN = 6,    /* plain rows on a page with an open record    */
-  GDN_DEV_BAD_FLAG = 7        /* corrupt flag word                           */
+  GDN_DEV_BAD_FLAG = 7,       /* corrupt flag word, or FRESH with SPEC       */
+  GDN_DEV_TIMEOUT = 8         /* a bounded on-chip wait gave up (the request's
+                                 results are not written)                    */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -270,8 +272,11 @@ size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims,
  *   S <- e^{gamma_L} S + (diag(e^{gamma_L-gamma}) K^)^T Vn.
  * Equal to gdn_seq in exact arithmetic; within 1e-4 relative in fp32.
  * Arguments as gdn_seq, plus a device workspace of at least
- * gdn_chunk_prefill_workspace_bytes() bytes (contents need not be zeroed,
- * not kept between calls). SPEC requests are skipped.                      */
+ * gdn_chunk_prefill_workspace_bytes() bytes (0 today: the pointer may be
+ * NULL). SPEC requests are skipped. Requires io dtype bf16 and
+ * Dk = Dv = 128 (else GDN_ERR_UNSUPPORTED) and qkv 16-byte aligned (the rows
+ * are read by TMA). One CTA per (request, value head) walks the request's
+ * chunks; its tensor memory holds the fp32 state throughout.               */
 gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
                              const gdn_params* params, const void* qkv,
                              const void* a, const void* b, void* o,

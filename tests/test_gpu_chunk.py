@@ -1,0 +1,146 @@
+"""gdn_chunk_prefill (tensor-core chunked form) against the fp64 token loop.
+
+Bar: relative error <= 1e-4 per tensor with fp32 state and fp32 outputs, on
+ragged requests (several chunks, an exact chunk, one token, none), with and
+without an initial state, and at the full long-prefill size (4 x 8192 tokens,
+16/32 heads) on sampled heads the oracle recomputes exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_14_gb300 as gdn
+import oracle
+import synth
+from tests.gpu_util import Layer, f64, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+def chunk_run(L, B, qkv, a, b, o_dtype=torch.float32):
+    o = torch.zeros(B.num_rows, L.sh.Hv, L.sh.Dv, dtype=o_dtype, device="cuda")
+    ws_bytes = gdn.gdn_chunk_prefill_workspace_bytes(L.dims, B)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
+    gdn.gdn_chunk_prefill(L.dims, B, L.params, qkv, a, b, o, L.pool.buf, ws, ws_bytes, L.status)
+    return o
+
+
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_chunk_ragged_requests_vs_oracle(state):
+    sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
+    rng = np.random.default_rng(101)
+    lengths = [200, 64, 1, 130, 0, 129]
+    R = len(lengths)
+    order = [3, 0, 5, 1, 4, 2]
+    start, ln, T = synth.pack(lengths, order)
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    S0 = synth.state(rng, R, sh, std=0.1)
+    fresh = np.array([False, True, False, True, True, False])
+    S0[fresh] = 0.0
+    if state == gdn.GDN_BF16:
+        S0 = oracle.round_bf16(S0).astype(np.float32)
+    L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], state=state, num_pages=R)
+    L.seed(range(R), S0=S0)
+    B = L.batch(start, ln, flags=np.where(fresh, gdn.GDN_REQ_FRESH, 0))
+    o = chunk_run(L, B, to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"]))
+    L.ok()
+    o_ref, S_ref = oracle.gdn_f64(rows["x"].value, rows["a"].value, rows["b"].value, d["A_log"],
+                                  d["dt_bias"], start, ln, sh.Hk, sh.Hv, sh.Dk, sh.Dv, S0=S0)
+    assert rel(f64(o), o_ref) <= TOL
+    S = np.stack([f64(L.pool.state_math(r)) for r in range(R)])
+    tol_s = TOL if state == gdn.GDN_F32 else 4e-3   # a bf16 page rounds the stored state
+    for r in range(R):
+        if ln[r]:
+            sl = slice(start[r], start[r] + ln[r])
+            assert rel(f64(o[sl]), o_ref[sl]) <= TOL, r
+        assert rel(S[r], S_ref[r]) <= tol_s, r
+
+
+def test_chunk_agrees_with_token_by_token_kernel_and_skips_spec():
+    """Plain requests: chunked and token-by-token GPU results agree; SPEC
+    requests in the same batch are left alone by the chunked prefill."""
+    sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
+    rng = np.random.default_rng(7)
+    lengths = [150, 70, 8]
+    start, ln, T = synth.pack(lengths)
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    S0 = synth.state(rng, 3, sh, std=0.05)
+    qkv, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    flags = [0, 0, gdn.GDN_REQ_SPEC]
+    L1 = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=3)
+    L1.seed(range(3), S0=S0)
+    before = L1.pool.state(2).clone()
+    o1 = chunk_run(L1, L1.batch(start, ln, flags=flags, n_accepted=[0, 0, 0]), qkv, a, b)
+    L1.ok()
+    L2 = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=3)
+    L2.seed(range(3), S0=S0)
+    o2 = L2.seq(L2.batch(start, ln, flags=flags, n_accepted=[0, 0, 0]), qkv, a, b)
+    L2.ok()
+    sl = slice(0, 220)
+    assert rel(f64(o1[sl]), f64(o2[sl])) <= 2 * TOL
+    for r in range(2):
+        assert rel(f64(L1.pool.state_math(r)), f64(L2.pool.state_math(r))) <= 2 * TOL
+    assert torch.equal(L1.pool.state(2), before)
+
+
+def test_chunk_gate_mode_precomputed():
+    sh = synth.Shapes(Hk=1, Hv=2, Dk=128, Dv=128)
+    rng = np.random.default_rng(8)
+    T = 100
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    rows["a"] = synth.as_io(-np.abs(rng.standard_normal((T, sh.Hv))) * 0.5, synth.BF16)
+    rows["b"] = synth.as_io(rng.uniform(0, 1, (T, sh.Hv)), synth.BF16)
+    L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], gate_mode=1)
+    B = L.batch([0], [T], flags=gdn.GDN_REQ_FRESH)
+    o = chunk_run(L, B, to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"]))
+    L.ok()
+    o_ref, S_ref = oracle.gdn_f64(rows["x"].value, rows["a"].value, rows["b"].value, d["A_log"],
+                                  d["dt_bias"], [0], [T], 1, 2, 128, 128, gate_mode=1)
+    assert rel(f64(o), o_ref) <= TOL
+    assert rel(f64(L.pool.state_math(0)), S_ref[0]) <= TOL
+
+
+def _head_pair(d, rows, r, kh, start, ln):
+    """The oracle's inputs for value heads 2kh, 2kh+1 (q/k head kh) of request r."""
+    sh = d["shapes"]
+    D = sh.Dk
+    sl = slice(start[r], start[r] + ln[r])
+    x = rows["x"].value[sl]
+    h0 = kh * (sh.Hv // sh.Hk)
+    q = x[:, kh * D:(kh + 1) * D]
+    k = x[:, sh.Hk * D + kh * D: sh.Hk * D + (kh + 1) * D]
+    v = x[:, 2 * sh.Hk * D + h0 * D: 2 * sh.Hk * D + (h0 + 2) * D]
+    qkv = np.concatenate([q, k, v], axis=1)
+    a = rows["a"].value[sl][:, h0:h0 + 2]
+    b = rows["b"].value[sl][:, h0:h0 + 2]
+    return qkv, a, b, h0
+
+
+def test_chunk_long_prefill_full_size_sampled_heads():
+    """4 x 8192 tokens at 16/32 heads, launched as the benchmark launches it;
+    the oracle recomputes four sampled (request, head-pair) chains whole."""
+    d = synth.long()
+    sh = d["shapes"]
+    start, ln = d["row_start"], d["row_len"]
+    L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], num_pages=d["R"])
+    B = L.batch(start, ln, flags=gdn.GDN_REQ_FRESH)
+    rows = {"x": d["x"], "a": d["a"], "b": d["b"]}
+    o = chunk_run(L, B, to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"]))
+    L.ok()
+    assert torch.isfinite(o).all()
+    for r, kh in ((0, 0), (1, 7), (2, 11), (3, 15)):
+        qkv, a, b, h0 = _head_pair(d, rows, r, kh, start, ln)
+        o_ref, S_ref = oracle.gdn_f64(qkv, a, b, d["A_log"][h0:h0 + 2], d["dt_bias"][h0:h0 + 2],
+                                      [0], [ln[r]], 1, 2, sh.Dk, sh.Dv)
+        sl = slice(start[r], start[r] + ln[r])
+        assert rel(f64(o[sl, h0:h0 + 2]), o_ref) <= TOL, (r, kh)
+        S = f64(L.pool.state_math(r))[h0:h0 + 2]
+        assert rel(S, S_ref[0]) <= TOL, (r, kh)
