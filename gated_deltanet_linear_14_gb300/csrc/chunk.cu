@@ -55,8 +55,8 @@ constexpr uint32_t OFF_R1 = 65536;    // T_W hi | T_W lo | T_U hi | T_U lo (8 KB
                                       //  -> Vn^T hi | lo ([128][64], 16 KB each); solve scratch
 constexpr uint32_t OFF_R2 = 98304;    // A, T fp32 [64][64] -> W^T hi | lo -> V'^T hi | lo
 constexpr uint32_t OFF_S = 131072;    // S^T hi: atom a at a*16384 ([128][64]); S^T lo at +32768
-constexpr uint32_t OFF_VEC = 196608;  // per-token vectors (5 x 64 floats)
-constexpr uint32_t kChunkSmem = OFF_VEC + 5 * 64 * 4 + 2048;  // + 1024-byte alignment slack
+constexpr uint32_t OFF_VEC = 196608;  // per-token vectors (8 x 64 floats)
+constexpr uint32_t kChunkSmem = OFF_VEC + 8 * 64 * 4 + 2048;  // + 1024-byte alignment slack
 
 // TMEM columns (512 allocated).
 constexpr uint32_t TM_D1 = 0, TM_W = 64, TM_U = 128, TM_WS = 192, TM_S = 256, TM_OQ = 384,
@@ -86,6 +86,26 @@ __device__ __forceinline__ void store_row_hilo(uint8_t* hi_tile, uint8_t* lo_til
       l[e] = pack_bf16(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
     }
     const uint32_t off = sw128_chunk(row, ch);
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// The same for 32 values: chunks 4*half .. 4*half+3 of the row.
+__device__ __forceinline__ void store_half_hilo(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                                int half, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = v[c * 8 + 2 * e], x1 = v[c * 8 + 2 * e + 1];
+      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+      h[e] = pack_bf16(h0, h1);
+      l[e] = pack_bf16(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
+    }
+    const uint32_t off = sw128_chunk(row, 4 * half + c);
     *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
   }
@@ -176,6 +196,9 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   float* s_gam = s_beta + 64;
   float* s_iq = s_gam + 64;
   float* s_ik = s_iq + 64;
+  float* s_cw = s_ik + 64;   // beta e^gamma / |k|      (columns of T_W)
+  float* s_cv = s_cw + 64;   // e^{gamma_L-gamma} / |k| (columns of V')
+  float* s_co = s_cv + 64;   // e^gamma / |q|           (rows of the Q S term)
   float* Am = reinterpret_cast<float*>(sm + OFF_R2);
   float* Tm = Am + 64 * 64;
   float* Xs = reinterpret_cast<float*>(sm + OFF_R1);
@@ -315,6 +338,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     __syncthreads();
     const float gL = s_gam[kCL - 1];
     if (tid < kCL) {
+      const float eg = expf(s_gam[tid]);
+      s_cw[tid] = __fmul_rn(__fmul_rn(s_beta[tid], eg), s_ik[tid]);
+      s_cv[tid] = __fmul_rn(expf(__fsub_rn(gL, s_gam[tid])), s_ik[tid]);
+      s_co[tid] = __fmul_rn(eg, s_iq[tid]);
+    }
+    if (tid < kCL) {
       // P row t: masked, gated, normalised q_t . k_s  (s <= t < n_c)
       const int t = tid;
       const float iq = s_iq[t], gt = s_gam[t];
@@ -357,8 +386,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       }
       if (tid < kCL) {
 #pragma unroll
-        for (int s = 0; s < 64; ++s)
-          w[s] = __fmul_rn(w[s], __fmul_rn(__fmul_rn(s_beta[s], expf(s_gam[s])), s_ik[s]));
+        for (int s = 0; s < 64; ++s) w[s] = __fmul_rn(w[s], s_cw[s]);
         store_row_hilo(sm + OFF_R1, sm + OFF_R1 + 8192, t, w);
       } else {
 #pragma unroll
@@ -390,15 +418,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     {
       const float eL = expf(gL);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        float v[64];
-        tmem_ld32(trow + TM_S + half * 64, v);
-        tmem_ld32(trow + TM_S + half * 64 + 32, v + 32);
-        store_row_hilo(sm + OFF_S + half * 16384, sm + OFF_S + 32768 + half * 16384, tid, v);
+      for (int cc = 0; cc < 4; ++cc) {
+        float v[32];
+        tmem_ld32(trow + TM_S + cc * 32, v);
+        store_half_hilo(sm + OFF_S + (cc >> 1) * 16384, sm + OFF_S + 32768 + (cc >> 1) * 16384, tid,
+                        cc & 1, v);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = __fmul_rn(v[i], eL);
-        tmem_st32(trow + TM_S + half * 64, v);
-        tmem_st32(trow + TM_S + half * 64 + 32, v + 32);
+        for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], eL);
+        tmem_st32(trow + TM_S + cc * 32, v);
       }
       tmem_st_wait();
     }
@@ -406,10 +433,12 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // W^T rows (MN-major B operand of MMA4)
     {
-      float w[64];
-      tmem_ld32(trow + TM_W, w);
-      tmem_ld32(trow + TM_W + 32, w + 32);
-      store_row_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, w);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float w[32];
+        tmem_ld32(trow + TM_W + half * 32, w);
+        store_half_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, half, w);
+      }
     }
     fence_async_smem();
     tc_fence_before();
@@ -442,18 +471,18 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
     {
-      float u[64], ws[64];
-      tmem_ld32(trow + TM_U, u);
-      tmem_ld32(trow + TM_U + 32, u + 32);
-      tmem_ld32(trow + TM_WS, ws);
-      tmem_ld32(trow + TM_WS + 32, ws + 32);
 #pragma unroll
-      for (int s = 0; s < 64; ++s) u[s] = __fsub_rn(u[s], ws[s]);
-      store_row_hilo(sm + OFF_R1, sm + OFF_R1 + 16384, tid, u);
+      for (int half = 0; half < 2; ++half) {
+        float u[32], ws[32];
+        tmem_ld32(trow + TM_U + half * 32, u);
+        tmem_ld32(trow + TM_WS + half * 32, ws);
 #pragma unroll
-      for (int s = 0; s < 64; ++s)
-        u[s] = __fmul_rn(u[s], __fmul_rn(expf(__fsub_rn(gL, s_gam[s])), s_ik[s]));
-      store_row_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, u);
+        for (int s = 0; s < 32; ++s) u[s] = __fsub_rn(u[s], ws[s]);
+        store_half_hilo(sm + OFF_R1, sm + OFF_R1 + 16384, tid, half, u);
+#pragma unroll
+        for (int s = 0; s < 32; ++s) u[s] = __fmul_rn(u[s], s_cv[half * 32 + s]);
+        store_half_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, half, u);
+      }
     }
     fence_async_smem();
     tc_fence_before();
@@ -484,18 +513,20 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // outputs: O[t][j] = scale (e^{gamma_t} |q_t|^-1 (S^T Q^T)[j][t] + (Vn^T P^T)[j][t])
     {
-      float oq[64], op[64];
-      tmem_ld32(trow + TM_OQ, oq);
-      tmem_ld32(trow + TM_OQ + 32, oq + 32);
-      tmem_ld32(trow + TM_OP, op);
-      tmem_ld32(trow + TM_OP + 32, op + 32);
 #pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        if (t < n_c) {
-          const float v = __fmul_rn(P.scale, __fmaf_rn(__fmul_rn(expf(s_gam[t]), s_iq[t]), oq[t], op[t]));
-          const size_t off = ((R0 + t) * G.Hv + h) * G.Dv + tid;
-          if (out_f32) reinterpret_cast<float*>(o)[off] = v;
-          else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
+      for (int half = 0; half < 2; ++half) {
+        float oq[32], op[32];
+        tmem_ld32(trow + TM_OQ + half * 32, oq);
+        tmem_ld32(trow + TM_OP + half * 32, op);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = half * 32 + i;
+          if (t < n_c) {
+            const float v = __fmul_rn(P.scale, __fmaf_rn(s_co[t], oq[i], op[i]));
+            const size_t off = ((R0 + t) * G.Hv + h) * G.Dv + tid;
+            if (out_f32) reinterpret_cast<float*>(o)[off] = v;
+            else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
+          }
         }
       }
     }

@@ -27,6 +27,7 @@ namespace gdn {
 
 constexpr int kConvThreads = 128;
 constexpr int kConvRows = 32;  // rows per tile (>= W-1)
+constexpr int kConvBatch = 8;  // rows whose loads are in flight together
 
 template <class IO, class YT, int W, bool SLOTS>
 __global__ void __launch_bounds__(kConvThreads)
@@ -119,33 +120,49 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
     }
   }
 
+  // rows in groups of kConvBatch: all loads of a group are issued before any
+  // of its arithmetic, so each thread keeps kConvBatch x 16 bytes in flight
   const int t_end = min(q.len, t0 + kConvRows);
-  for (int t = t0; t < t_end; ++t) {
-    float xv[V];
-    load_f<IO, V>(x + (size_t)(q.start + t) * G.C + c0, xv);
-    float yv[V];
+  for (int tb = t0; tb < t_end; tb += kConvBatch) {
+    uint4 raw[kConvBatch];
 #pragma unroll
-    for (int v = 0; v < V; ++v) {
-      float acc = bias[v];
+    for (int i = 0; i < kConvBatch; ++i)
+      if (tb + i < t_end)
+        raw[i] = *reinterpret_cast<const uint4*>(x + (size_t)(q.start + tb + i) * G.C + c0);
 #pragma unroll
-      for (int j = 0; j < H; ++j) acc = __fmaf_rn(wt[j][v], h[j][v], acc);
-      acc = __fmaf_rn(wt[H][v], xv[v], acc);
-      yv[v] = own_silu(acc);
-    }
-    store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
+    for (int i = 0; i < kConvBatch; ++i) {
+      const int t = tb + i;
+      if (t >= t_end) break;
+      float xv[V];
+      {
+        const IO* e = reinterpret_cast<const IO*>(&raw[i]);
 #pragma unroll
-    for (int j = 0; j < H - 1; ++j)
+        for (int v = 0; v < V; ++v) xv[v] = to_f(e[v]);
+      }
+      float yv[V];
 #pragma unroll
-      for (int v = 0; v < V; ++v) h[j][v] = h[j + 1][v];
+      for (int v = 0; v < V; ++v) {
+        float acc = bias[v];
 #pragma unroll
-    for (int v = 0; v < V; ++v) h[H - 1][v] = xv[v];
-    if constexpr (!SLOTS) {
-      if (rec_out) store_f<IO, V>(rec_out + (size_t)t * G.rec_row + c0, yv);
-    } else {
-      // window after candidate t goes to slot t
-      IO* wdst = reinterpret_cast<IO*>(pool + (size_t)t * SG.slot_bytes + SG.window_off);
+        for (int j = 0; j < H; ++j) acc = __fmaf_rn(wt[j][v], h[j][v], acc);
+        acc = __fmaf_rn(wt[H][v], xv[v], acc);
+        yv[v] = own_silu(acc);
+      }
+      store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
 #pragma unroll
-      for (int j = 0; j < H; ++j) store_f<IO, V>(wdst + (size_t)j * G.C + c0, h[j]);
+      for (int j = 0; j < H - 1; ++j)
+#pragma unroll
+        for (int v = 0; v < V; ++v) h[j][v] = h[j + 1][v];
+#pragma unroll
+      for (int v = 0; v < V; ++v) h[H - 1][v] = xv[v];
+      if constexpr (!SLOTS) {
+        if (rec_out) store_f<IO, V>(rec_out + (size_t)t * G.rec_row + c0, yv);
+      } else {
+        // window after candidate t goes to slot t
+        IO* wdst = reinterpret_cast<IO*>(pool + (size_t)t * SG.slot_bytes + SG.window_off);
+#pragma unroll
+        for (int j = 0; j < H; ++j) store_f<IO, V>(wdst + (size_t)j * G.C + c0, h[j]);
+      }
     }
   }
 
