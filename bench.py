@@ -1,9 +1,11 @@
 """Benchmark of the GB300 Gated DeltaNet layer core.
 
 One step = one pass of the layer core over one batch: the causal conv +
-SiLU (gdn_conv) and the fused post-conv + gated delta rule (gdn_seq). The
-headline workload is the decode batch: 64 requests x 1 token, 16 q/k heads,
-32 value heads, Dk = Dv = 128 (8192 conv channels), bf16 rows, fp32 state.
+SiLU, the q/k norm and gates, and the gated delta rule, run as the fused
+decode launch (gdn_decode; the same step as two launches, gdn_conv then
+gdn_seq, is timed beside it). The headline workload is the decode batch: 64
+requests x 1 token, 16 q/k heads, 32 value heads, Dk = Dv = 128 (8192 conv
+channels), bf16 rows, fp32 state.
 
 Metric: GDN tokens/s per layer, plus the state-traffic HBM GB/s of the rule
 kernel against the measured HBM peak.
@@ -195,20 +197,30 @@ class Decode:
         self.h_a.copy_(self.a.cpu())
         self.h_b.copy_(self.b.cpu())
 
-    # bytes the rule kernel must move per launch (decode)
-    def rule_bytes(self):
+    # bytes the fused decode kernel must move per launch
+    def decode_bytes(self):
         sh, R = self.sh, self.R
         state = 2 * R * sh.Hv * sh.Dk * sh.Dv * 4            # read + write fp32 state
-        rows = R * (2 * sh.Hk * sh.Dk + sh.Hv * sh.Dv) * 2   # conv'd q|k|v rows (bf16)
+        x = R * sh.C * 2                                     # raw rows (bf16)
+        window = 2 * R * (sh.W - 1) * sh.C * 2               # conv window read + write
+        taps = sh.C * sh.W * 2
         gates = 2 * R * sh.Hv * 2                            # a, b
         out = R * sh.Hv * sh.Dv * 2                          # o (bf16)
-        return state + rows + gates + out, state
-
-    def conv_bytes(self):
-        sh, R = self.sh, self.R
-        return R * sh.C * 2 * 2 + R * 2 * (sh.W - 1) * sh.C * 2 + sh.C * sh.W * 2
+        return state + x + window + taps + gates + out, state
 
     def launch(self, i, ev=None):
+        """One decode step: the fused conv + rule launch."""
+        gdn = self.gdn
+        pool = self.pools[i % len(self.pools)]
+        if ev is not None:
+            ev[0].record()
+        gdn.gdn_decode(self.dims, self.batch, self.params, self.x, self.conv_w, self.a, self.b,
+                       self.o, pool.buf, self.status)
+        if ev is not None:
+            ev[1].record()
+
+    def launch_two(self, i, ev=None):
+        """The same step as two launches: gdn_conv, then gdn_seq."""
         gdn = self.gdn
         pool = self.pools[i % len(self.pools)]
         if ev is not None:
@@ -265,8 +277,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     wl.check()
 
-    # timed region: K steps, per-kernel events on the launching stream
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    # timed region: K steps, a CUDA event pair around each launch on the
+    # launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
@@ -276,9 +289,16 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     wl.check()
-    conv_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
-    rule_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    dec_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
     elapsed_max = reduce_max(elapsed, world)
+
+    # the same steps as two launches (conv, then the rule), for comparison
+    K2 = min(K, 500)
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K2)]
+    el2 = time_steps(lambda i: wl.launch_two(W + K + i, ev2[i]), K2, torch)
+    wl.check()
+    conv_ms = [e[0].elapsed_time(e[1]) for e in ev2]
+    rule_ms = [e[1].elapsed_time(e[2]) for e in ev2]
 
     # end-to-end through host buffers
     for i in range(W):
@@ -290,10 +310,10 @@ def run_ours(args, world, rank, local):
     h2d, d2h = wl.e2e_bytes()
 
     tokens = wl.R * K * world
-    rule_bytes, state_bytes = wl.rule_bytes()
-    rule_s = statistics.mean(rule_ms) / 1e3
+    dec_bytes, state_bytes = wl.decode_bytes()
+    dec_s = statistics.mean(dec_ms) / 1e3
     hbm_peak = float(peaks["hbm_gbs"])
-    achieved = rule_bytes / rule_s / 1e9
+    achieved = dec_bytes / dec_s / 1e9
     line = {
         "metric": METRIC,
         "value": tokens / elapsed_max,
@@ -310,16 +330,19 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "parallelism": f"replicas x{world}",
                    "l2": f"{POOLS} rotating page pools ({POOLS * wl.pools[0].buf.numel() / 2**20:.0f} "
                          "MiB) exceed the 129 MB L2"},
-        "state_gbs": state_bytes / rule_s / 1e9,
+        "state_gbs": state_bytes / dec_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": traffic_from_profile("rule_decode"),
-                     "kernel": "rule_kernel (gdn_seq, decode)",
-                     "algorithmic_bytes_per_launch": rule_bytes,
-                     "launch_ms": rule_s * 1e3, "peak_source": f"{peak_src} hbm_gbs (burst)"},
-        "kernels_ms": {"gdn_conv": statistics.mean(conv_ms), "gdn_seq": statistics.mean(rule_ms)},
+                     "frac": achieved / hbm_peak, "traffic": traffic_from_profile("decode_fused"),
+                     "kernel": "decode_kernel (gdn_decode: conv + rule, one launch)",
+                     "algorithmic_bytes_per_launch": dec_bytes,
+                     "launch_ms": dec_s * 1e3, "peak_source": f"{peak_src} hbm_gbs (burst)"},
+        "kernels_ms": {"gdn_decode": statistics.mean(dec_ms)},
+        "two_launch_step": {"ms_per_step": el2 / K2 * 1e3, "gdn_conv_ms": statistics.mean(conv_ms),
+                            "gdn_seq_ms": statistics.mean(rule_ms),
+                            "tokens_per_s": wl.R * K2 / el2},
         "e2e": {"value": tokens / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max / K * 1e3},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K,
         "clocks": clk.summary(),
         "wall_s": wall,
     }
@@ -355,8 +378,12 @@ def extra_workloads(device, peaks, args, only=None):
                      ("mixed_prefill_spec", lambda: bench_mixed(device, peaks)),
                      ("long_prefill_token_by_token", lambda: bench_long_seq(device, peaks)),
                      ("long_prefill_chunked", lambda: bench_long_chunk(device, peaks)),
+                     ("chunked_small", lambda: bench_long_chunk(device, peaks, K=3, W=3,
+                                                                small=True)),
                      ("conv_long_rows", lambda: bench_conv_long(device, peaks))):
         if only is not None and name != only:
+            continue
+        if only is None and name == "chunked_small":
             continue
         try:
             out[name] = fn()
@@ -577,12 +604,14 @@ CHUNK_FLOPS = 2 * 128 * 64 * 128 + 2 * (2 * 128 * 64 * 64) + 2 * (2 * 128 * 64 *
     + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64
 
 
-def bench_long_chunk(device, peaks, K=5, W=3):
-    """4 x 8192-token prefill through the tensor-core chunked form."""
+def bench_long_chunk(device, peaks, K=5, W=3, small=False):
+    """4 x 8192-token prefill through the tensor-core chunked form (small:
+    1 x 4096 tokens at 4/8 heads, the case the ncu capture uses)."""
     import torch
     import gated_deltanet_linear_14_gb300 as gdn
     from gated_deltanet_linear_14_gb300.pages import PagePool
-    d = synth.long()
+    d = synth.long(B=1, T=4096, sh=synth.Shapes(Hk=4, Hv=8, Dk=128, Dv=128)) if small \
+        else synth.long()
     sh, R, T = d["shapes"], d["R"], d["T"]
     dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 0, gdn.GDN_BF16, gdn.GDN_F32,
                          gdn.GDN_BF16)
@@ -705,8 +734,8 @@ def run_reference(args, world, rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")

@@ -276,6 +276,29 @@ gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gd
   return GDN_OK;
 }
 
+gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                      const void* x, const void* conv_w, const void* a, const void* b, void* o,
+                      void* pages, int32_t* status, gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, true)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  const int items = (dims->num_v_heads / dims->num_k_heads) * (dims->head_v_dim / 32);
+  if (items > 16) return GDN_ERR_UNSUPPORTED;
+  if (batch->max_rows > 1) return GDN_ERR_INVALID_ARG;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages || !conv_w) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!x || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  if (launch_decode(G, B, P, dims->io_dtype == GDN_BF16, dims->state_dtype == GDN_BF16,
+                    dims->out_dtype == GDN_F32, x, conv_w, a, b, o, pages, status,
+                    (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
 size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims, const gdn_batch* batch) {
   if (check_dims(dims) != GDN_OK || check_batch(batch, true) != GDN_OK) return 0;
   return 0;

@@ -124,10 +124,13 @@ __device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, f
     for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.0f : 0.0f;
 #pragma unroll
     for (int r = 1; r < 16; ++r) {
-      float acc = 0.0f;
+      float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
-      for (int k = 0; k < r; ++k) acc = __fmaf_rn(Ab[r * 64 + k], x[k], acc);
-      if (r > cc) x[r] = -acc;
+      for (int k = 0; k < r; k += 2) {
+        acc0 = __fmaf_rn(Ab[r * 64 + k], x[k], acc0);
+        if (k + 1 < r) acc1 = __fmaf_rn(Ab[r * 64 + k + 1], x[k + 1], acc1);
+      }
+      if (r > cc) x[r] = -__fadd_rn(acc0, acc1);
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) Tm[(16 * b + r) * 64 + 16 * b + cc] = x[r];
@@ -143,20 +146,28 @@ __device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, f
   __syncthreads();
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
+    // X_ij = sum_{k=j}^{i-1} A_ik T_kj, 16 terms per block step, 4 partial sums
     for (int idx = tid; idx < nb * 256; idx += kChunkThreads) {
       const int bj = idx >> 8, bi = bj + d, r = (idx >> 4) & 15, cc = idx & 15;
-      float acc = 0.0f;
-      for (int k = 16 * bj; k < 16 * bi; ++k)
-        acc = __fmaf_rn(Am[(16 * bi + r) * 64 + k], Tm[k * 64 + 16 * bj + cc], acc);
-      Xs[idx] = acc;
+      const float* arow = Am + (16 * bi + r) * 64;
+      const float* tcol = Tm + 16 * bj + cc;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int kb = 16 * bj; kb < 16 * bi; kb += 16) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k & 3] = __fmaf_rn(arow[kb + k], tcol[(kb + k) * 64], acc[k & 3]);
+      }
+      Xs[idx] = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
     }
     __syncthreads();
+    // T_ij = -T_ii X_ij (T_ii is stored with zeros above its diagonal)
     for (int idx = tid; idx < nb * 256; idx += kChunkThreads) {
       const int bj = idx >> 8, bi = bj + d, r = (idx >> 4) & 15, cc = idx & 15;
-      float acc = 0.0f;
-      for (int m = 0; m <= r; ++m)
-        acc = __fmaf_rn(Tm[(16 * bi + r) * 64 + 16 * bi + m], Xs[(bj << 8) + m * 16 + cc], acc);
-      Tm[(16 * bi + r) * 64 + 16 * bj + cc] = -acc;
+      const float* trow = Tm + (16 * bi + r) * 64 + 16 * bi;
+      const float* xcol = Xs + (bj << 8) + cc;
+      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int m = 0; m < 16; ++m) acc[m & 3] = __fmaf_rn(trow[m], xcol[m * 16], acc[m & 3]);
+      Tm[(16 * bi + r) * 64 + 16 * bj + cc] = -__fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
     }
     __syncthreads();
   }
@@ -171,6 +182,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t bars[2];
   __shared__ uint32_t tmem_slot;
+  __shared__ float gamma_carry;
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int h = blockIdx.x;
@@ -296,12 +308,13 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       mma_commit(bar_mma);
     }
     // gates and q norms while it runs
+    float g_mine = 0.0f;
     if (tid < kCL) {
-      float g = 0.0f, beta = 0.0f;
-      if (tid < n_c) gate_log(P, h, a_t, b_t, g, beta);
-      s_g[tid] = g;
+      float beta = 0.0f;
+      if (tid < n_c) gate_log(P, h, a_t, b_t, g_mine, beta);
+      s_g[tid] = g_mine;
       s_beta[tid] = beta;
-      float qq = 0.0f;
+      float qq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -311,18 +324,23 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float x0 = __uint_as_float(w4[e] << 16), x1 = __uint_as_float(w4[e] & 0xFFFF0000u);
-            qq = __fmaf_rn(x0, x0, qq);
-            qq = __fmaf_rn(x1, x1, qq);
+            qq[e] = __fmaf_rn(x0, x0, qq[e]);
+            qq[e] = __fmaf_rn(x1, x1, qq[e]);
           }
         }
-      s_iq[tid] = rsqrtf(__fadd_rn(qq, P.eps));
+      s_iq[tid] = rsqrtf(__fadd_rn(__fadd_rn(__fadd_rn(qq[0], qq[1]), __fadd_rn(qq[2], qq[3])), P.eps));
+      // gamma: inclusive prefix sum of g over the chunk (warp scans, then
+      // the second warp adds the first warp's total)
+      const int lane = tid & 31;
+#pragma unroll
+      for (int dd = 1; dd < 32; dd <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, g_mine, dd);
+        if (lane >= dd) g_mine = __fadd_rn(g_mine, y);
+      }
+      if (tid == 31) gamma_carry = g_mine;
     }
     __syncthreads();
-    if (tid < kCL) {
-      float gm = 0.0f;
-      for (int s = 0; s <= tid; ++s) gm = __fadd_rn(gm, s_g[s]);
-      s_gam[tid] = gm;
-    }
+    if (tid < kCL) s_gam[tid] = (tid >= 32) ? __fadd_rn(g_mine, gamma_carry) : g_mine;
     if (!wait_mma()) { fail = true; break; }
 
     float row[64];

@@ -28,6 +28,12 @@ cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const 
                          int state_bf16, int out_f32, const void* a, const void* b, void* o,
                          void* pages, int32_t* status, cudaStream_t stream);
 
+// Fused conv + rule for one token per request (plain requests).
+cudaError_t launch_decode(const Geom& G, const Batch& B, const Params& P, int io_bf16,
+                          int state_bf16, int out_f32, const void* x, const void* w, const void* a,
+                          const void* b, void* o, void* pages, int32_t* status,
+                          cudaStream_t stream);
+
 // per head dimension (one translation unit each)
 cudaError_t launch_rule_d32(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
                             int, int, int, const void*, const void*, const void*, void*, void*,

@@ -176,7 +176,14 @@ struct LaneState {
 // lanes with (r8 & 3) == 0 own column m = r8 >> 2 of their group).
 template <int DK, class ST>
 __device__ __forceinline__ float token_step(LaneState<DK / 8>& S, const Stage<DK>& st, int t, int r8,
-                                            int vcol, float scale, bool update) {
+                                            int vcol, float scale, bool update);
+
+// The step on explicit shared-memory rows: q^ and k^ (DK floats each), the
+// CTA's value block (vcol indexes it) and (alpha, beta, q^.k^).
+template <int DK, class ST>
+__device__ __forceinline__ float token_step_rows(LaneState<DK / 8>& S, const float* qrow,
+                                                 const float* krow, const float* vrow, float4 sc,
+                                                 int r8, int vcol, float scale, bool update) {
   using L = LaneMap<DK, ST>;
   constexpr int E = DK / 8;
   float2 q2[E / 2], k2[E / 2];
@@ -184,17 +191,16 @@ __device__ __forceinline__ float token_step(LaneState<DK / 8>& S, const Stage<DK
   for (int i = 0; i < L::NI; ++i) {
 #pragma unroll
     for (int e = 0; e < L::VEC; e += 4) {
-      const float4 qv = *reinterpret_cast<const float4*>(&st.q[t][L::idx(r8, i) + e]);
-      const float4 kv = *reinterpret_cast<const float4*>(&st.k[t][L::idx(r8, i) + e]);
+      const float4 qv = *reinterpret_cast<const float4*>(&qrow[L::idx(r8, i) + e]);
+      const float4 kv = *reinterpret_cast<const float4*>(&krow[L::idx(r8, i) + e]);
       q2[(i * L::VEC + e) / 2] = make_float2(qv.x, qv.y);
       q2[(i * L::VEC + e) / 2 + 1] = make_float2(qv.z, qv.w);
       k2[(i * L::VEC + e) / 2] = make_float2(kv.x, kv.y);
       k2[(i * L::VEC + e) / 2 + 1] = make_float2(kv.z, kv.w);
     }
   }
-  const float4 sc = st.sc[t];
   const float alpha = sc.x, beta = sc.y, kq = sc.z;
-  const float2 vv = *reinterpret_cast<const float2*>(&st.v[t][vcol]);
+  const float2 vv = *reinterpret_cast<const float2*>(&vrow[vcol]);
 
   float2 ak0 = make_float2(0.f, 0.f), aq0 = ak0, ak1 = ak0, aq1 = ak0;
 #pragma unroll
@@ -236,6 +242,12 @@ __device__ __forceinline__ float token_step(LaneState<DK / 8>& S, const Stage<DK
     }
   }
   return o;
+}
+
+template <int DK, class ST>
+__device__ __forceinline__ float token_step(LaneState<DK / 8>& S, const Stage<DK>& st, int t, int r8,
+                                            int vcol, float scale, bool update) {
+  return token_step_rows<DK, ST>(S, st.q[t], st.k[t], st.v[t], st.sc[t], r8, vcol, scale, update);
 }
 
 template <int DK, class ST>

@@ -207,6 +207,22 @@ gdn_status gdn_seq(const gdn_dims* dims, const gdn_batch* batch,
                    const void* b, void* o, void* pages, int32_t* status,
                    gdn_stream_t stream);
 
+/* Fused decode step: gdn_conv (io-dtype output) followed by gdn_seq for a
+ * batch of one token per request, in one launch, with the same results bit
+ * for bit (outputs, states, conv windows; the conv'd rows are not written).
+ * This is the "one launch per layer" design the r9700-stack v0.2.3 notes
+ * (section 1) credit for the short-step speed-up, extended to the conv.
+ * Plain requests with row_len 1 (or 0: a FRESH request is zeroed) are
+ * processed; SPEC requests are skipped; row_len > 1 is GDN_DEV_BAD_ROWS.
+ * Requires (Hv/Hk) * (Dv/32) <= 16 and batch->max_rows <= 1.
+ *   x       device [num_rows][C] io dtype (raw conv inputs)
+ *   conv_w  device [C][W];  a, b, o, pages, status as gdn_seq.            */
+gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch,
+                      const gdn_params* params, const void* x,
+                      const void* conv_w, const void* a, const void* b,
+                      void* o, void* pages, int32_t* status,
+                      gdn_stream_t stream);
+
 /* One-page speculative verify for the SPEC requests of the batch; plain
  * requests are skipped (r9700-stack v0.2.4, "What it does";
  * r9k_gdn_spec_verify / r9k_gdn_spec_commit). Per SPEC request with page
