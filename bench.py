@@ -380,10 +380,11 @@ def extra_workloads(device, peaks, args, only=None):
                      ("long_prefill_chunked", lambda: bench_long_chunk(device, peaks)),
                      ("chunked_small", lambda: bench_long_chunk(device, peaks, K=3, W=3,
                                                                 small=True)),
+                     ("decode_fused", lambda: bench_decode_only(device, peaks)),
                      ("conv_long_rows", lambda: bench_conv_long(device, peaks))):
         if only is not None and name != only:
             continue
-        if only is None and name == "chunked_small":
+        if only is None and name in ("chunked_small", "decode_fused"):
             continue
         try:
             out[name] = fn()
@@ -644,6 +645,18 @@ def bench_long_chunk(device, peaks, K=5, W=3, small=False):
             "frac_of_tensor_peak": tf / float(peaks["bf16_tflops"]),
             "issued_mma_flops_per_chunk_head": 24117248,
             "status": int(status.item())}
+
+
+def bench_decode_only(device, peaks, K=20, W=5):
+    """The fused decode step alone (what the ncu capture of decode_kernel runs)."""
+    import torch
+    wl = Decode(device)
+    for i in range(W):
+        wl.launch(i)
+    torch.cuda.synchronize()
+    el = time_steps(lambda i: wl.launch(W + i), K, torch)
+    wl.check()
+    return {"workload": WORKLOAD, "ms_per_step": el / K * 1e3}
 
 
 def bench_conv_long(device, peaks, K=10, W=3):

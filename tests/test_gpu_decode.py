@@ -20,7 +20,7 @@ def two_layers(d, R, state, out, Kc=0):
     S0 = d["S0"][:R]
     if state == gdn.GDN_BF16:
         S0 = oracle.round_bf16(S0).astype(np.float32)
-    pages = np.array([(3 * r + 1) % (R + 3) for r in range(R)])   # scattered pages
+    pages = np.random.default_rng(R).permutation(R + 3)[:R].astype(np.int32)  # scattered, distinct
     for L in Ls:
         L.seed(pages, S0=S0, hist=to_dev(d["hist0"])[:R])
     return Ls, pages, S0
