@@ -45,7 +45,7 @@ using namespace umma;
 
 constexpr int kCL = 64;               // tokens per chunk
 constexpr int kCD = 128;              // Dk = Dv
-constexpr int kChunkThreads = 128;
+constexpr int kChunkThreads = 256;      // two warpgroups; warps w and w+4 share TMEM lanes
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_QK = 0;        // per 64-column atom a (a*16384): Q rows 0..63, K rows 64..127
@@ -136,7 +136,7 @@ __device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, f
     for (int r = 0; r < 16; ++r) Tm[(16 * b + r) * 64 + 16 * b + cc] = x[r];
   } else {
     // blocks above the diagonal are zero
-    for (int idx = tid - 64; idx < 6 * 256; idx += 64) {
+    for (int idx = tid - 64; idx < 6 * 256; idx += kChunkThreads - 64) {
       const int blk = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
       const int bi = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
       const int bj = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
@@ -185,6 +185,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   __shared__ float gamma_carry;
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int row = tid & 127;    // TMEM lane (row) of this thread
+  const int wg = tid >> 7;      // column half this warpgroup handles
   const int h = blockIdx.x;
   const bool reporter = (h == 0 && tid == 0);
   const Req q = load_req(B, blockIdx.y);
@@ -226,19 +228,20 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lanes
+  const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lanes
   const uint32_t sb = smem_u32(sm);
 
-  // the initial state S^T (row j = tid) into TMEM
+  // the initial state S^T (row j, columns of this warpgroup's half) into TMEM
   {
     float v[32];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int cc = 2 * wg + c2;
       if (q.fresh) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = 0.0f;
       } else {
-        load_f<ST, 32>(Sb + (size_t)tid * kCD + cc * 32, v);
+        load_f<ST, 32>(Sb + (size_t)row * kCD + cc * 32, v);
       }
       tmem_st32(trow + TM_S + cc * 32, v);
     }
@@ -343,14 +346,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     if (tid < kCL) s_gam[tid] = (tid >= 32) ? __fadd_rn(g_mine, gamma_carry) : g_mine;
     if (!wait_mma()) { fail = true; break; }
 
-    float row[64];
-    tmem_ld32(trow + TM_D1, row);
-    tmem_ld32(trow + TM_D1 + 32, row + 32);
-    if (tid >= kCL) {
-      const int t = tid - kCL;
+    float d1[32];   // columns [32 wg, 32 wg + 32) of this thread's row of [QK^T; KK^T]
+    tmem_ld32(trow + TM_D1 + 32 * wg, d1);
+    if (row >= kCL && ((row - kCL) >> 5) == wg) {
+      // |k_t|^2 is the diagonal of KK^T: column t sits in this half
+      const int t = row - kCL;
       float kk = 0.0f;
 #pragma unroll
-      for (int s = 0; s < 64; ++s) kk = (s == t) ? row[s] : kk;
+      for (int s = 0; s < 32; ++s) kk = (s == (t & 31)) ? d1[s] : kk;
       s_ik[t] = rsqrtf(__fadd_rn(kk, P.eps));
     }
     __syncthreads();
@@ -361,33 +364,35 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       s_cv[tid] = __fmul_rn(expf(__fsub_rn(gL, s_gam[tid])), s_ik[tid]);
       s_co[tid] = __fmul_rn(eg, s_iq[tid]);
     }
-    if (tid < kCL) {
-      // P row t: masked, gated, normalised q_t . k_s  (s <= t < n_c)
-      const int t = tid;
+    if (row < kCL) {
+      // P row t, columns of this half: masked, gated, normalised q_t . k_s (s <= t < n_c)
+      const int t = row;
       const float iq = s_iq[t], gt = s_gam[t];
 #pragma unroll
-      for (int s = 0; s < 64; ++s)
-        row[s] = (s <= t && t < n_c)
-                     ? __fmul_rn(__fmul_rn(__fmul_rn(row[s], iq), s_ik[s]), expf(__fsub_rn(gt, s_gam[s])))
-                     : 0.0f;
-      store_row_hilo(sm + OFF_P, sm + OFF_P + 8192, t, row);
+      for (int i = 0; i < 32; ++i) {
+        const int s = 32 * wg + i;
+        d1[i] = (s <= t && t < n_c)
+                    ? __fmul_rn(__fmul_rn(__fmul_rn(d1[i], iq), s_ik[s]), expf(__fsub_rn(gt, s_gam[s])))
+                    : 0.0f;
+      }
+      store_half_hilo(sm + OFF_P, sm + OFF_P + 8192, t, wg, d1);
     } else {
       // A row t: beta_t e^{gamma_t - gamma_s} k^_t . k^_s for s < t
-      const int t = tid - kCL;
+      const int t = row - kCL;
       const float ikt = s_ik[t], gt = s_gam[t], bt = s_beta[t];
 #pragma unroll
-      for (int s = 0; s < 64; s += 4) {
+      for (int i = 0; i < 32; i += 4) {
         float4 v;
         float* vp = &v.x;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int ss = s + e;
+          const int ss = 32 * wg + i + e;
           vp[e] = (ss < t && t < n_c)
-                      ? __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(row[ss], ikt), s_ik[ss]), bt),
+                      ? __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(d1[i + e], ikt), s_ik[ss]), bt),
                                   expf(__fsub_rn(gt, s_gam[ss])))
                       : 0.0f;
         }
-        *reinterpret_cast<float4*>(&Am[t * 64 + s]) = v;
+        *reinterpret_cast<float4*>(&Am[t * 64 + 32 * wg + i]) = v;
       }
     }
     __syncthreads();
@@ -395,22 +400,18 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // T_W = T diag(beta e^gamma / |k|), T_U = T diag(beta), hi/lo bf16 tiles
     {
-      const int t = tid & 63;
-      float w[64];
+      // thread -> (row t, which of T_W / T_U, column half)
+      const int t = tid & 63, which = (tid >> 6) & 1, half = tid >> 7;
+      float w[32];
 #pragma unroll
-      for (int s = 0; s < 64; s += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(&Tm[t * 64 + s]);
-        w[s] = v.x; w[s + 1] = v.y; w[s + 2] = v.z; w[s + 3] = v.w;
+      for (int i = 0; i < 32; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(&Tm[t * 64 + 32 * half + i]);
+        w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
       }
-      if (tid < kCL) {
+      const float* colscale = which ? s_beta : s_cw;
 #pragma unroll
-        for (int s = 0; s < 64; ++s) w[s] = __fmul_rn(w[s], s_cw[s]);
-        store_row_hilo(sm + OFF_R1, sm + OFF_R1 + 8192, t, w);
-      } else {
-#pragma unroll
-        for (int s = 0; s < 64; ++s) w[s] = __fmul_rn(w[s], s_beta[s]);
-        store_row_hilo(sm + OFF_R1 + 16384, sm + OFF_R1 + 24576, t, w);
-      }
+      for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(w[i], colscale[32 * half + i]);
+      store_half_hilo(sm + OFF_R1 + which * 16384, sm + OFF_R1 + which * 16384 + 8192, t, half, w);
     }
     fence_async_smem();
     __syncthreads();
@@ -436,10 +437,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     {
       const float eL = expf(gL);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int cc = 2 * wg + c2;
         float v[32];
         tmem_ld32(trow + TM_S + cc * 32, v);
-        store_half_hilo(sm + OFF_S + (cc >> 1) * 16384, sm + OFF_S + 32768 + (cc >> 1) * 16384, tid,
+        store_half_hilo(sm + OFF_S + (cc >> 1) * 16384, sm + OFF_S + 32768 + (cc >> 1) * 16384, row,
                         cc & 1, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(v[i], eL);
@@ -451,11 +453,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // W^T rows (MN-major B operand of MMA4)
     {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
         float w[32];
-        tmem_ld32(trow + TM_W + half * 32, w);
-        store_half_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, half, w);
+        tmem_ld32(trow + TM_W + wg * 32, w);
+        store_half_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, row, wg, w);
       }
     }
     fence_async_smem();
@@ -489,17 +490,17 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
     {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
+        const int half = wg;
         float u[32], ws[32];
         tmem_ld32(trow + TM_U + half * 32, u);
         tmem_ld32(trow + TM_WS + half * 32, ws);
 #pragma unroll
         for (int s = 0; s < 32; ++s) u[s] = __fsub_rn(u[s], ws[s]);
-        store_half_hilo(sm + OFF_R1, sm + OFF_R1 + 16384, tid, half, u);
+        store_half_hilo(sm + OFF_R1, sm + OFF_R1 + 16384, row, half, u);
 #pragma unroll
         for (int s = 0; s < 32; ++s) u[s] = __fmul_rn(u[s], s_cv[half * 32 + s]);
-        store_half_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, tid, half, u);
+        store_half_hilo(sm + OFF_R2, sm + OFF_R2 + 16384, row, half, u);
       }
     }
     fence_async_smem();
@@ -531,8 +532,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
     // outputs: O[t][j] = scale (e^{gamma_t} |q_t|^-1 (S^T Q^T)[j][t] + (Vn^T P^T)[j][t])
     {
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      {
+        const int half = wg;
         float oq[32], op[32];
         tmem_ld32(trow + TM_OQ + half * 32, oq);
         tmem_ld32(trow + TM_OP + half * 32, op);
@@ -541,7 +542,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
           const int t = half * 32 + i;
           if (t < n_c) {
             const float v = __fmul_rn(P.scale, __fmaf_rn(s_co[t], oq[i], op[i]));
-            const size_t off = ((R0 + t) * G.Hv + h) * G.Dv + tid;
+            const size_t off = ((R0 + t) * G.Hv + h) * G.Dv + row;
             if (out_f32) reinterpret_cast<float*>(o)[off] = v;
             else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
           }
@@ -554,10 +555,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
   if (!fail) {
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
+    for (int c2 = 0; c2 < 2; ++c2) {
+      const int cc = 2 * wg + c2;
       float v[32];
       tmem_ld32(trow + TM_S + cc * 32, v);
-      store_f<ST, 32>(Sb + (size_t)tid * kCD + cc * 32, v);
+      store_f<ST, 32>(Sb + (size_t)row * kCD + cc * 32, v);
     }
     if (q.fresh && h == 0 && tid == 0) *flagp = 0u;  // empty record
   } else if (tid == 0) {

@@ -40,12 +40,23 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// What the items of one CTA share: one token's q^ and k^, and per item the
+// value block and (alpha, beta, q^.k^).
+template <int DK>
+struct DecStage {
+  float q[DK];
+  float k[DK];
+  float v[kTC][kBV];
+  float4 sc[kTC];
+  float kq;
+};
+
 template <class IO, class ST, int DK>
 struct DecLayout {
   static constexpr uint32_t TILE = kBV * DK;                       // state elements per item
   static constexpr uint32_t TILE_BYTES = TILE * sizeof(ST);
-  static constexpr uint32_t OFF_STAGE = kDecStages * TILE_BYTES;   // Stage<DK>
-  static constexpr uint32_t OFF_ROW = OFF_STAGE + ((sizeof(Stage<DK>) + 127) / 128) * 128;
+  static constexpr uint32_t OFF_STAGE = kDecStages * TILE_BYTES;   // DecStage<DK>
+  static constexpr uint32_t OFF_ROW = OFF_STAGE + ((sizeof(DecStage<DK>) + 127) / 128) * 128;
   static constexpr uint32_t BYTES = OFF_ROW + kDecMaxRow * sizeof(IO);
 };
 
@@ -58,7 +69,7 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
   constexpr int PE = DK / 8;
   extern __shared__ __align__(128) uint8_t dsm[];
   ST* tiles = reinterpret_cast<ST*>(dsm);
-  Stage<DK>& st = *reinterpret_cast<Stage<DK>*>(dsm + Lay::OFF_STAGE);
+  DecStage<DK>& st = *reinterpret_cast<DecStage<DK>*>(dsm + Lay::OFF_STAGE);
   IO* mrow = reinterpret_cast<IO*>(dsm + Lay::OFF_ROW);
   __shared__ __align__(8) uint64_t full[kDecStages];
 
@@ -173,21 +184,56 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
     return;
   }
 
-  // stage q^, k^, each item's value block and gates exactly as gdn_seq does
+  // Stage q^, k^, each item's value block and gates with the arithmetic of
+  // the token-by-token kernel's publish step (same 8-lane partial sums and
+  // butterfly, same rounding), so the token step sees bit-identical inputs.
   {
     const int t = tid >> 3, p = tid & 7;
-    Fetch<DK, IO> f;
+    if (t == 0) {
+      RawVec<IO, PE> rq, rk;
+      rq.load(mrow + PE * p);
+      rk.load(mrow + DK + PE * p);
+      float fq[PE], fk[PE];
+#pragma unroll
+      for (int e = 0; e < PE; ++e) {
+        fq[e] = rq.get(e);
+        fk[e] = rk.get(e);
+      }
+      float qq = 0.0f, kk = 0.0f, qk = 0.0f;
+#pragma unroll
+      for (int e = 0; e < PE; ++e) {
+        qq = __fmaf_rn(fq[e], fq[e], qq);
+        kk = __fmaf_rn(fk[e], fk[e], kk);
+        qk = __fmaf_rn(fq[e], fk[e], qk);
+      }
+#pragma unroll
+      for (int d = 1; d < 8; d <<= 1) {
+        qq = __fadd_rn(qq, __shfl_xor_sync(0xFFu, qq, d));
+        kk = __fadd_rn(kk, __shfl_xor_sync(0xFFu, kk, d));
+        qk = __fadd_rn(qk, __shfl_xor_sync(0xFFu, qk, d));
+      }
+      const float iq = rsqrtf(__fadd_rn(qq, P.eps));
+      const float ik = rsqrtf(__fadd_rn(kk, P.eps));
+#pragma unroll
+      for (int e = 0; e < PE; ++e) {
+        st.q[PE * p + e] = __fmul_rn(fq[e], iq);
+        st.k[PE * p + e] = __fmul_rn(fk[e], ik);
+      }
+      if (p == 0) st.kq = __fmul_rn(__fmul_rn(qk, iq), ik);
+    }
+    float alpha = 0.0f, beta = 0.0f;
     if (t < n_items) {
       const int g = t / nCB, cb = t % nCB;
-      f.q.load(mrow + PE * p);
-      f.k.load(mrow + DK + PE * p);
-      f.v.load(mrow + 2 * DK + g * G.Dv + cb * kBV + 4 * p);
-      if (p == 0) {
-        f.a = to_f(a_in[(size_t)q.start * G.Hv + h0 + g]);
-        f.b = to_f(b_in[(size_t)q.start * G.Hv + h0 + g]);
-      }
+      RawVec<IO, 4> rv;
+      rv.load(mrow + 2 * DK + g * G.Dv + cb * kBV + 4 * p);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.v[t][4 * p + e] = rv.get(e);
+      if (p == 0)
+        gates(P, h0 + g, to_f(a_in[(size_t)q.start * G.Hv + h0 + g]),
+              to_f(b_in[(size_t)q.start * G.Hv + h0 + g]), alpha, beta);
     }
-    publish<DK, IO>(st, f, t, n_items, p, h0 + (t < n_items ? t / nCB : 0), P);
+    __syncthreads();
+    if (t < n_items && p == 0) st.sc[t] = make_float4(alpha, beta, st.kq, 0.0f);
   }
   __syncthreads();
 
@@ -199,17 +245,19 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
     LaneState<DK / 8> S;
     if (stream_state) {
       const bool ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((i / kDecStages) & 1), kDecWaitLimit);
+      // one barrier per item: past it every thread has also finished reading
+      // the previous item's stage, which can then be refilled
       if (__syncthreads_or(!ok)) {
         failed = true;
         break;
       }
+      if (tid == 0 && i > 0 && issued < n_items) issue(issued++);
       load_state<DK, ST>(S, tiles + (size_t)s * Lay::TILE, col, r8);
-      __syncthreads();  // every thread has read stage s
-      if (tid == 0 && i + kDecStages < n_items) issue(issued++);
     } else {
       zero_state<DK / 8>(S);
     }
-    const float ov = token_step<DK, ST>(S, st, i, r8, vcol, P.scale, true);
+    const float ov = token_step_rows<DK, ST>(S, st.q, st.k, st.v[i], st.sc[i], r8, vcol, P.scale,
+                                             true);
     if ((r8 & 3) == 0) {
       const size_t off = ((size_t)q.start * G.Hv + h) * G.Dv + (size_t)cb * kBV + vcol + (r8 >> 2);
       store_out(o, out_f32, off, ov);
