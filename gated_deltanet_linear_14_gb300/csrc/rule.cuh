@@ -396,16 +396,32 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
     ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
     IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
     load_state<DK, ST>(S, Sb, col, r8);
-    if (ss.width > 0) {
-      // replay rows 0..a of the live slot, then store the checkpoint
-      RowSrc<IO> rp;
-      rp.rows = rec + (size_t)ss.live * G.Kc * G.rec_row;
-      rp.row_stride = G.rec_row;
-      rp.a = rp.rows + G.C + h;
-      rp.b = rp.rows + G.C + G.Hv + h;
-      rp.ab_stride = G.rec_row;
-      run_rows<DK, IO, ST>(S, st, rp, ss.accepted + 1, nullptr, out_f32, 0, h, cb, kh, G, P, true,
-                           NoAfter());
+    // Rows 0..a of the live record slot (the replay) and this step's
+    // candidates are at most 2 Kc <= kTC rows: stage them together, once.
+    const int n_rep = (ss.width > 0) ? ss.accepted + 1 : 0;
+    const int n_all = n_rep + q.len;
+    {
+      const int ft = threadIdx.x >> 3, fp = threadIdx.x & 7;
+      Fetch<DK, IO> f;
+      RowSrc<IO> src;
+      int tt = ft;
+      if (ft < n_rep) {
+        src.rows = rec + (size_t)ss.live * G.Kc * G.rec_row;
+        src.row_stride = G.rec_row;
+        src.a = src.rows + G.C + h;
+        src.b = src.rows + G.C + G.Hv + h;
+        src.ab_stride = G.rec_row;
+      } else {
+        src = rows_in;
+        tt = ft - n_rep;
+      }
+      fetch<DK, IO>(f, src, tt, ft < n_all ? tt + 1 : 0, fp, kh, h, cb, G);
+      publish<DK, IO>(st, f, ft, n_all, fp, h, P);
+    }
+    __syncthreads();
+    const int vcol = warp * 8 + cg * 2;
+    for (int t = 0; t < n_rep; ++t) token_step<DK, ST>(S, st, t, r8, vcol, P.scale, true);
+    if (n_rep > 0) {
       store_state<DK, ST>(Sb, S, col, r8);
       // continue from exactly what was stored (a bf16 page rounds here)
 #pragma unroll
@@ -415,8 +431,13 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
           S.s[m][j] = make_float2(through<ST>(S.s[m][j].x), through<ST>(S.s[m][j].y));
     }
     // this step's candidates: outputs only, no per-candidate state
-    run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P,
-                         false, NoAfter());
+    for (int t = 0; t < q.len; ++t) {
+      const float ov = token_step<DK, ST>(S, st, n_rep + t, r8, vcol, P.scale, t + 1 < q.len);
+      if ((r8 & 3) == 0) {
+        const size_t off = (((size_t)q.start + t) * G.Hv + h) * G.Dv + cb * kBV + vcol + (r8 >> 2);
+        store_out(o, out_f32, off, ov);
+      }
+    }
     // the candidates' gates go next to their conv'd rows in the other slot
     if (cb == 0 && threadIdx.x < q.len) {
       IO* row = rec + ((size_t)(1 - ss.live) * G.Kc + threadIdx.x) * G.rec_row;
