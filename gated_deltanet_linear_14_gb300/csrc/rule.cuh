@@ -166,25 +166,11 @@ __device__ __forceinline__ void publish(Stage<DK>& st, const Fetch<DK, IO>& f, i
   }
 }
 
-// The state of a lane: M columns x E entries as float2 pairs, held scaled:
-// the state is c * s (c is the same on every lane of the CTA). The decay then
-// multiplies c instead of every entry, and a token's write is one fused
-// multiply-add per entry. store_state writes c * s; materialize folds c in.
+// The state of a lane: M columns x E entries as float2 pairs.
 template <int E>
 struct LaneState {
   float2 s[kColsPerLane][E / 2];
-  float c;
 };
-
-template <int E>
-__device__ __forceinline__ void materialize(LaneState<E>& S) {
-  const float2 cc = make_float2(S.c, S.c);
-#pragma unroll
-  for (int m = 0; m < kColsPerLane; ++m)
-#pragma unroll
-    for (int j = 0; j < E / 2; ++j) S.s[m][j] = __fmul2_rn(S.s[m][j], cc);
-  S.c = 1.0f;
-}
 
 // One token for one lane. Returns this lane's output column value in o (the
 // lanes with (r8 & 3) == 0 own column m = r8 >> 2 of their group).
@@ -239,27 +225,21 @@ __device__ __forceinline__ float token_step_rows(LaneState<DK / 8>& S, const flo
   kept = __fadd_rn(kept, __shfl_xor_sync(0xffffffffu, sent, 2));
   kept = __fadd_rn(kept, __shfl_xor_sync(0xffffffffu, kept, 1));
   const float other = __shfl_xor_sync(0xffffffffu, kept, 2);
-  // the sums over the stored entries, times c, are the sums over the state
-  const float sk = __fmul_rn(S.c, b1 ? other : kept);
-  const float sq = __fmul_rn(S.c, b1 ? kept : other);
+  const float sk = b1 ? other : kept;
+  const float sq = b1 ? kept : other;
   const float vm = b2 ? vv.y : vv.x;
   const float u = __fmul_rn(beta, __fsub_rn(vm, __fmul_rn(alpha, sk)));
   const float o = __fmul_rn(scale, __fmaf_rn(u, kq, __fmul_rn(alpha, sq)));
   if (update) {
-    // state' = alpha c s + k u^T = c' (s + k u^T / c') with c' = alpha c
-    const float c_new = __fmul_rn(alpha, S.c);
-    const float w = __fmul_rn(u, __frcp_rn(c_new));
-    const float w_x = __shfl_xor_sync(0xffffffffu, w, 4);
-    const float w0 = b2 ? w_x : w, w1 = b2 ? w : w_x;
-    const float2 ww0 = make_float2(w0, w0), ww1 = make_float2(w1, w1);
+    const float u_x = __shfl_xor_sync(0xffffffffu, u, 4);
+    const float u0 = b2 ? u_x : u, u1 = b2 ? u : u_x;
+    const float2 al = make_float2(alpha, alpha);
+    const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
 #pragma unroll
     for (int j = 0; j < E / 2; ++j) {
-      S.s[0][j] = __ffma2_rn(k2[j], ww0, S.s[0][j]);
-      S.s[1][j] = __ffma2_rn(k2[j], ww1, S.s[1][j]);
+      S.s[0][j] = __ffma2_rn(k2[j], uu0, __fmul2_rn(al, S.s[0][j]));
+      S.s[1][j] = __ffma2_rn(k2[j], uu1, __fmul2_rn(al, S.s[1][j]));
     }
-    S.c = c_new;
-    // keep c inside [2^-30, 2^30] so s stays far from the fp32 limits
-    if (!(c_new >= 0x1p-30f && c_new <= 0x1p30f)) materialize<E>(S);
   }
   return o;
 }
@@ -274,7 +254,6 @@ template <int DK, class ST>
 __device__ __forceinline__ void load_state(LaneState<DK / 8>& S, const ST* base, const int* col,
                                            int r8) {
   using L = LaneMap<DK, ST>;
-  S.c = 1.0f;
 #pragma unroll
   for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
@@ -283,30 +262,20 @@ __device__ __forceinline__ void load_state(LaneState<DK / 8>& S, const ST* base,
                          reinterpret_cast<float*>(&S.s[m][0]) + i * L::VEC);
 }
 
-// Stores c * s and leaves the running, scaled state untouched, so a store
-// never changes the rounding of what follows (the slot layout stores after
-// every candidate, the one-page verify only at its checkpoint).
 template <int DK, class ST>
 __device__ __forceinline__ void store_state(ST* base, const LaneState<DK / 8>& S, const int* col,
                                             int r8) {
   using L = LaneMap<DK, ST>;
-  constexpr int E = DK / 8;
-  const float2 cc = make_float2(S.c, S.c);
 #pragma unroll
-  for (int m = 0; m < kColsPerLane; ++m) {
-    float2 t[E / 2];
-#pragma unroll
-    for (int j = 0; j < E / 2; ++j) t[j] = __fmul2_rn(S.s[m][j], cc);
+  for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
     for (int i = 0; i < L::NI; ++i)
       store_f<ST, L::VEC>(base + (size_t)col[m] * DK + L::idx(r8, i),
-                          reinterpret_cast<const float*>(&t[0]) + i * L::VEC);
-  }
+                          reinterpret_cast<const float*>(&S.s[m][0]) + i * L::VEC);
 }
 
 template <int E>
 __device__ __forceinline__ void zero_state(LaneState<E>& S) {
-  S.c = 1.0f;
 #pragma unroll
   for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
@@ -451,13 +420,10 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
     }
     __syncthreads();
     const int vcol = warp * 8 + cg * 2;
-#pragma unroll 2
     for (int t = 0; t < n_rep; ++t) token_step<DK, ST>(S, st, t, r8, vcol, P.scale, true);
     if (n_rep > 0) {
       store_state<DK, ST>(Sb, S, col, r8);
-      // continue from exactly what was stored (c folded in; a bf16 page
-      // also rounds here)
-      materialize<E>(S);
+      // continue from exactly what was stored (a bf16 page rounds here)
 #pragma unroll
       for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
@@ -465,7 +431,6 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
           S.s[m][j] = make_float2(through<ST>(S.s[m][j].x), through<ST>(S.s[m][j].y));
     }
     // this step's candidates: outputs only, no per-candidate state
-#pragma unroll 2
     for (int t = 0; t < q.len; ++t) {
       const float ov = token_step<DK, ST>(S, st, n_rep + t, r8, vcol, P.scale, t + 1 < q.len);
       if ((r8 & 3) == 0) {
