@@ -381,10 +381,11 @@ def extra_workloads(device, peaks, args, only=None):
                      ("chunked_small", lambda: bench_long_chunk(device, peaks, K=3, W=3,
                                                                 small=True)),
                      ("decode_fused", lambda: bench_decode_only(device, peaks)),
+                     ("crossover", lambda: bench_crossover(device, peaks)),
                      ("conv_long_rows", lambda: bench_conv_long(device, peaks))):
         if only is not None and name != only:
             continue
-        if only is None and name in ("chunked_small", "decode_fused"):
+        if only is None and name in ("chunked_small", "decode_fused", "crossover"):
             continue
         try:
             out[name] = fn()
@@ -645,6 +646,45 @@ def bench_long_chunk(device, peaks, K=5, W=3, small=False):
             "frac_of_tensor_peak": tf / float(peaks["bf16_tflops"]),
             "issued_mma_flops_per_chunk_head": 24117248,
             "status": int(status.item())}
+
+
+def bench_crossover(device, peaks, K=5, W=2):
+    """gdn_seq vs gdn_chunk_prefill on R fresh requests of T tokens each
+    (16/32 heads, Dk = Dv = 128): where the chunked form starts to win."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import PagePool
+    sh = synth.FULL
+    out = {}
+    for R in (1, 8):
+        rows_t = []
+        for T in (8, 16, 32, 48, 64, 96, 128, 256, 512, 1024):
+            d = synth.long(B=R, T=T)
+            dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 0, gdn.GDN_BF16, gdn.GDN_F32,
+                                 gdn.GDN_BF16)
+            A_log = torch.from_numpy(d["A_log"]).to(device)
+            dt = torch.from_numpy(d["dt_bias"]).to(device)
+            params = gdn.make_params(A_log, dt)
+            status = torch.zeros(1, dtype=torch.int32, device=device)
+            pool = PagePool(dims, R, device=device)
+            x, a, b = (_put_io(torch, device, d[k]) for k in ("x", "a", "b"))
+            o = torch.empty(R * T, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+            B = _dev_batch(gdn, torch, device, d["row_start"], d["row_len"], np.arange(R),
+                           np.full(R, gdn.GDN_REQ_FRESH))
+            seq = lambda i: gdn.gdn_seq(dims, B, params, x, a, b, o, pool.buf, status)
+            chk = lambda i: gdn.gdn_chunk_prefill(dims, B, params, x, a, b, o, pool.buf, None, 0,
+                                                  status)
+            res = {}
+            for name, fn in (("seq_us", seq), ("chunk_us", chk)):
+                for i in range(W):
+                    fn(i)
+                torch.cuda.synchronize()
+                res[name] = time_steps(fn, K, torch) / K * 1e6
+            res["T"] = T
+            rows_t.append(res)
+        wins = [r["T"] for r in rows_t if r["chunk_us"] < r["seq_us"]]
+        out[f"R={R}"] = {"rows": rows_t, "chunk_wins_from_T": min(wins) if wins else None}
+    return out
 
 
 def bench_decode_only(device, peaks, K=20, W=5):

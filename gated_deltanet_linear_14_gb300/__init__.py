@@ -6,7 +6,7 @@ device memory and streams. The binding raises if the library is missing; it
 never falls back to another implementation.
 
 Entry points (same names as the C ABI): ``gdn_conv``, ``gdn_seq``,
-``gdn_decode``, ``gdn_spec_verify``, ``gdn_spec_slots``, ``gdn_chunk_prefill``,
+``gdn_decode``, ``gdn_prefill``, ``gdn_spec_verify``, ``gdn_spec_slots``, ``gdn_chunk_prefill``,
 ``gdn_chunk_prefill_workspace_bytes``, ``gdn_page_layout``,
 ``gdn_slot_layout``, ``gdn_strerror``, ``gdn_abi_version``.
 """
@@ -102,6 +102,7 @@ def load_library(path: str = LIB_PATH):
             "gdn_seq": ([D, B, PR, P, P, P, P, P, P, P], I),
             "gdn_spec_verify": ([D, B, PR, P, P, P, P, P, P, P], I),
             "gdn_decode": ([D, B, PR, P, P, P, P, P, P, P, P], I),
+            "gdn_prefill": ([D, B, PR, P, P, P, P, P, I, P, P], I),
             "gdn_spec_slots": ([D, B, PR, P, P, P, P, P, P, P, P, P], I),
             "gdn_chunk_prefill_workspace_bytes": ([D, B], S),
             "gdn_chunk_prefill": ([D, B, PR, P, P, P, P, P, P, S, P, P], I),
@@ -185,6 +186,13 @@ def gdn_decode(dims, batch, params, x, conv_w, a, b, o, pages, status, stream=No
     _check(load_library().gdn_decode(ctypes.byref(dims), ctypes.byref(batch), ctypes.byref(params),
                                      _ptr(x), _ptr(conv_w), _ptr(a), _ptr(b), _ptr(o), _ptr(pages),
                                      _ptr(status), _stream(stream)), "gdn_decode")
+
+
+def gdn_prefill(dims, batch, params, qkv, a, b, o, pages, status, chunk_min_rows=0, stream=None):
+    _check(load_library().gdn_prefill(ctypes.byref(dims), ctypes.byref(batch), ctypes.byref(params),
+                                      _ptr(qkv), _ptr(a), _ptr(b), _ptr(o), _ptr(pages),
+                                      int(chunk_min_rows), _ptr(status), _stream(stream)),
+           "gdn_prefill")
 
 
 def gdn_spec_verify(dims, batch, params, qkv, a, b, o, pages, status, stream=None):

@@ -116,6 +116,8 @@ Batch make_batch(const gdn_batch* b) {
   B.flags = b->flags;
   B.n_accepted = b->n_accepted;
   B.order = b->order;
+  B.min_len = 0;
+  B.max_len = 0x7fffffff;
   return B;
 }
 
@@ -295,6 +297,41 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch, const gdn_pa
   if (launch_decode(G, B, P, dims->io_dtype == GDN_BF16, dims->state_dtype == GDN_BF16,
                     dims->out_dtype == GDN_F32, x, conv_w, a, b, o, pages, status,
                     (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
+gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                       const void* qkv, const void* a, const void* b, void* o, void* pages,
+                       int32_t chunk_min_rows, int32_t* status, gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, true)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!qkv || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  const int threshold = chunk_min_rows > 0 ? chunk_min_rows : GDN_PREFILL_CHUNK_MIN_ROWS;
+  const bool chunk_ok = dims->io_dtype == GDN_BF16 && dims->head_k_dim == 128 &&
+                        dims->head_v_dim == 128 && ((uintptr_t)qkv & 15) == 0;
+  const bool any_long = chunk_ok && batch->max_rows >= threshold && batch->num_rows > 0;
+  const Geom G = make_geom(dims);
+  const Params P = make_params(params, dims);
+  const cudaStream_t s = (cudaStream_t)stream;
+  Batch Bs = make_batch(batch);
+  if (any_long) Bs.max_len = threshold - 1;
+  SlotGeom SG{};
+  if (rule(0, G, Bs, P, SG, dims, qkv, a, b, o, pages, status, s) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  if (!any_long) return GDN_OK;
+  CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  const gdn_status te = encode_rows_tmap(&tmap, qkv, batch->num_rows, dims);
+  if (te != GDN_OK) return te;
+  Batch Bc = make_batch(batch);
+  Bc.min_len = threshold;
+  if (launch_chunk(&tmap, G, Bc, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a,
+                   b, o, pages, status, s) != cudaSuccess)
     return GDN_ERR_LAUNCH;
   return GDN_OK;
 }

@@ -195,6 +195,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     return;
   }
   if (q.spec) return;
+  if (q.len < B.min_len || q.len > B.max_len) return;
   char* pg = page_ptr(G, pages, q.page);
   uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
   if (!q.fresh && flag_width(*flagp) != 0) {
@@ -576,15 +577,13 @@ cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const 
   const CUtensorMap& tm = *static_cast<const CUtensorMap*>(tmap);
   dim3 grid(G.Hv, B.R);
   if (state_bf16) {
-    cudaError_t e = cudaFuncSetAttribute(chunk_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kChunkSmem);
+    cudaError_t e = ensure_smem_limit(chunk_kernel<bf16>, (int)kChunkSmem);
     if (e != cudaSuccess) return e;
     chunk_kernel<bf16><<<grid, kChunkThreads, kChunkSmem, stream>>>(
         tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
         status);
   } else {
-    cudaError_t e = cudaFuncSetAttribute(chunk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kChunkSmem);
+    cudaError_t e = ensure_smem_limit(chunk_kernel<float>, (int)kChunkSmem);
     if (e != cudaSuccess) return e;
     chunk_kernel<float><<<grid, kChunkThreads, kChunkSmem, stream>>>(
         tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,

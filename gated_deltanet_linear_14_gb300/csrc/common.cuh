@@ -29,6 +29,9 @@ struct Batch {
   const uint32_t* flags;
   const int32_t* n_accepted;
   const int32_t* order;
+  // plain requests with row counts outside [min_len, max_len] are left to
+  // another launch (the prefill dispatch splits a batch this way)
+  int min_len, max_len;
 };
 
 // Slot pool geometry of the slot-per-candidate layout.
@@ -261,6 +264,21 @@ __device__ __forceinline__ void gate_log(const Params& P, int h, float a_in, flo
   const float sp = (x > 20.0f) ? x : log1pf(expf(x));
   g = -__fmul_rn(expf(P.A_log[h]), sp);
   beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
+}
+
+// Raise a kernel's dynamic shared memory limit once per device (host side;
+// later launches, including ones being captured into a graph, skip the call).
+template <class Kernel>
+inline cudaError_t ensure_smem_limit(Kernel kernel, int bytes) {
+  static unsigned long long done = 0;  // bit d: set on device d (benign race)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done |= bit;
+  return e;
 }
 
 }  // namespace gdn

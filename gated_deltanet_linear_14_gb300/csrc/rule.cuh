@@ -348,6 +348,7 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
     return;
   }
   if (MODE == MODE_SEQ && q.spec) return;
+  if (MODE == MODE_SEQ && (q.len < B.min_len || q.len > B.max_len)) return;
   if (MODE == MODE_VERIFY && !q.spec) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

@@ -300,6 +300,25 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
                              size_t workspace_bytes, int32_t* status,
                              gdn_stream_t stream);
 
+/* Token counts at which the chunked form overtakes the token-by-token rule
+ * for one request, measured on GB300 (see gdn_prefill). */
+#define GDN_PREFILL_CHUNK_MIN_ROWS 64
+
+/* Prefill dispatch: the plain requests of the batch with at least
+ * chunk_min_rows rows (<= 0 selects GDN_PREFILL_CHUNK_MIN_ROWS) go through
+ * gdn_chunk_prefill, the others through gdn_seq; two launches on `stream`,
+ * each leaving the other's requests alone. The r9700-stack v0.2.3 notes
+ * (section 1) describe the same split by prefill length (R9K_GDN_PREFILL_MAX,
+ * break-even measured per model and card); here the threshold is a call
+ * argument. When the chunked form does not support the shape (io dtype other
+ * than bf16, Dk or Dv other than 128, or an unaligned qkv) every request goes
+ * token by token. Arguments otherwise as gdn_seq; SPEC requests are skipped. */
+gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch,
+                       const gdn_params* params, const void* qkv, const void* a,
+                       const void* b, void* o, void* pages,
+                       int32_t chunk_min_rows, int32_t* status,
+                       gdn_stream_t stream);
+
 /* Text for a status code (host, static storage). */
 const char* gdn_strerror(int32_t status);
 

@@ -144,3 +144,50 @@ def test_chunk_long_prefill_full_size_sampled_heads():
         assert rel(f64(o[sl, h0:h0 + 2]), o_ref) <= TOL, (r, kh)
         S = f64(L.pool.state_math(r))[h0:h0 + 2]
         assert rel(S, S_ref[0]) <= TOL, (r, kh)
+
+
+def test_prefill_dispatch_matches_each_path():
+    """gdn_prefill sends requests with >= threshold rows through the chunked
+    form and the rest token by token: each request equals, bit for bit, the
+    kernel it was sent to, and all are within 1e-4 of the oracle."""
+    sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
+    rng = np.random.default_rng(55)
+    lengths = [20, 63, 64, 200, 1, 0, 130]
+    R = len(lengths)
+    start, ln, T = synth.pack(lengths, [6, 2, 0, 5, 1, 4, 3])
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    S0 = synth.state(rng, R, sh, std=0.1)
+    fresh = np.array([False, True, False, False, False, True, False])
+    S0[fresh] = 0.0
+    qkv, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    flags = np.where(fresh, gdn.GDN_REQ_FRESH, 0)
+    thr = 64
+
+    def layer():
+        L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], num_pages=R)
+        L.seed(range(R), S0=S0)
+        return L
+
+    Lp = layer()
+    Bp = Lp.batch(start, ln, flags=flags)
+    op = Lp.out(T)
+    gdn.gdn_prefill(Lp.dims, Bp, Lp.params, qkv, a, b, op, Lp.pool.buf, Lp.status, thr)
+    Lp.ok()
+    Ls = layer()
+    os_ = Ls.seq(Ls.batch(start, ln, flags=flags), qkv, a, b)
+    Ls.ok()
+    Lc = layer()
+    oc = chunk_run(Lc, Lc.batch(start, ln, flags=flags), qkv, a, b)
+    Lc.ok()
+    for r in range(R):
+        sl = slice(start[r], start[r] + ln[r])
+        ref_o, ref_L = (oc, Lc) if ln[r] >= thr else (os_, Ls)
+        assert torch.equal(op[sl], ref_o[sl]), r
+        assert torch.equal(Lp.pool.state(r), ref_L.pool.state(r)), r
+    o_ref, S_ref = oracle.gdn_f64(rows["x"].value, rows["a"].value, rows["b"].value, d["A_log"],
+                                  d["dt_bias"], start, ln, sh.Hk, sh.Hv, sh.Dk, sh.Dv, S0=S0)
+    assert rel(f64(op), o_ref) <= TOL
+    S = np.stack([f64(Lp.pool.state_math(r)) for r in range(R)])
+    assert rel(S, S_ref) <= TOL
