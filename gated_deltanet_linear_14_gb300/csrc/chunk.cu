@@ -577,13 +577,13 @@ cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const 
   const CUtensorMap& tm = *static_cast<const CUtensorMap*>(tmap);
   dim3 grid(G.Hv, B.R);
   if (state_bf16) {
-    cudaError_t e = ensure_smem_limit(chunk_kernel<bf16>, (int)kChunkSmem);
+    cudaError_t e = ensure_smem_limit<chunk_kernel<bf16>>((int)kChunkSmem);
     if (e != cudaSuccess) return e;
     chunk_kernel<bf16><<<grid, kChunkThreads, kChunkSmem, stream>>>(
         tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
         status);
   } else {
-    cudaError_t e = ensure_smem_limit(chunk_kernel<float>, (int)kChunkSmem);
+    cudaError_t e = ensure_smem_limit<chunk_kernel<float>>((int)kChunkSmem);
     if (e != cudaSuccess) return e;
     chunk_kernel<float><<<grid, kChunkThreads, kChunkSmem, stream>>>(
         tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,

@@ -268,8 +268,9 @@ __device__ __forceinline__ void gate_log(const Params& P, int h, float a_in, flo
 
 // Raise a kernel's dynamic shared memory limit once per device (host side;
 // later launches, including ones being captured into a graph, skip the call).
-template <class Kernel>
-inline cudaError_t ensure_smem_limit(Kernel kernel, int bytes) {
+// One instantiation, and so one record of devices done, per kernel.
+template <auto kernel>
+inline cudaError_t ensure_smem_limit(int bytes) {
   static unsigned long long done = 0;  // bit d: set on device d (benign race)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

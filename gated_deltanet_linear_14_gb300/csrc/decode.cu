@@ -283,7 +283,7 @@ static cudaError_t launch_decode_t(const Geom& G, const Batch& B, const Params& 
                                    const void* x, const void* w, const void* a, const void* b,
                                    void* o, void* pages, int32_t* status, cudaStream_t stream) {
   using Lay = DecLayout<IO, ST, DK>;
-  cudaError_t e = ensure_smem_limit(decode_kernel<IO, ST, DK>, (int)Lay::BYTES);
+  cudaError_t e = ensure_smem_limit<decode_kernel<IO, ST, DK>>((int)Lay::BYTES);
   if (e != cudaSuccess) return e;
   dim3 grid(G.Hk, B.R);
   decode_kernel<IO, ST, DK><<<grid, kRuleThreads, Lay::BYTES, stream>>>(
