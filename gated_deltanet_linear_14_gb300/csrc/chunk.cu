@@ -531,23 +531,34 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     if (!wait_mma()) { fail = true; break; }
     if (tid == 0 && c + 1 < nchunks) issue_tma(c + 1);
 
-    // outputs: O[t][j] = scale (e^{gamma_t} |q_t|^-1 (S^T Q^T)[j][t] + (Vn^T P^T)[j][t])
+    // outputs: O[t][j] = scale (e^{gamma_t} |q_t|^-1 (S^T Q^T)[j][t] + (Vn^T P^T)[j][t]),
+    // gathered as a [64][128] tile in shared memory (the Vn^T region, free
+    // once MMA6 has read it) and written out as whole 16-byte row pieces
     {
-      {
-        const int half = wg;
-        float oq[32], op[32];
-        tmem_ld32(trow + TM_OQ + half * 32, oq);
-        tmem_ld32(trow + TM_OP + half * 32, op);
+      const int half = wg;
+      float oq[32], op[32];
+      tmem_ld32(trow + TM_OQ + half * 32, oq);
+      tmem_ld32(trow + TM_OP + half * 32, op);
+      float* of = reinterpret_cast<float*>(sm + OFF_R1);
+      bf16* ob = reinterpret_cast<bf16*>(sm + OFF_R1);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = half * 32 + i;
-          if (t < n_c) {
-            const float v = __fmul_rn(P.scale, __fmaf_rn(s_co[t], oq[i], op[i]));
-            const size_t off = ((R0 + t) * G.Hv + h) * G.Dv + row;
-            if (out_f32) reinterpret_cast<float*>(o)[off] = v;
-            else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
-          }
-        }
+      for (int i = 0; i < 32; ++i) {
+        const int t = half * 32 + i;
+        const float v = __fmul_rn(P.scale, __fmaf_rn(s_co[t], oq[i], op[i]));
+        if (out_f32) of[t * kCD + row] = v;
+        else ob[t * kCD + row] = __float2bfloat16_rn(v);
+      }
+    }
+    __syncthreads();
+    {
+      const int per_row = out_f32 ? kCD / 4 : kCD / 8;   // 16-byte pieces per row
+      const uint4* src = reinterpret_cast<const uint4*>(sm + OFF_R1);
+      for (int idx = tid; idx < n_c * per_row; idx += kChunkThreads) {
+        const int t = idx / per_row, piece = idx % per_row;
+        const size_t row_off = ((R0 + t) * G.Hv + h) * G.Dv;
+        uint4* dst = out_f32 ? reinterpret_cast<uint4*>(reinterpret_cast<float*>(o) + row_off)
+                             : reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(o) + row_off);
+        dst[piece] = src[t * per_row + piece];
       }
     }
     tc_fence_before();
