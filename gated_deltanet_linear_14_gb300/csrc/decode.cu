@@ -32,14 +32,6 @@ constexpr int kDecStages = 4;
 constexpr int kDecMaxRow = 2 * 128 + 512;  // q | k | the group's v (items <= kTC)
 constexpr long long kDecWaitLimit = 1LL << 26;
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"((uint64_t)src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // What the items of one CTA share: one token's q^ and k^, and per item the
 // value block and (alpha, beta, q^.k^).
 template <int DK>
@@ -184,42 +176,17 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
     return;
   }
 
-  // Stage q^, k^, each item's value block and gates with the arithmetic of
-  // the token-by-token kernel's publish step (same 8-lane partial sums and
-  // butterfly, same rounding), so the token step sees bit-identical inputs.
+  // Stage q^, k^ (through the token-by-token kernel's own normalisation, so
+  // the token step sees bit-identical inputs), each item's value block and
+  // gates.
   {
     const int t = tid >> 3, p = tid & 7;
     if (t == 0) {
       RawVec<IO, PE> rq, rk;
       rq.load(mrow + PE * p);
       rk.load(mrow + DK + PE * p);
-      float fq[PE], fk[PE];
-#pragma unroll
-      for (int e = 0; e < PE; ++e) {
-        fq[e] = rq.get(e);
-        fk[e] = rk.get(e);
-      }
-      float qq = 0.0f, kk = 0.0f, qk = 0.0f;
-#pragma unroll
-      for (int e = 0; e < PE; ++e) {
-        qq = __fmaf_rn(fq[e], fq[e], qq);
-        kk = __fmaf_rn(fk[e], fk[e], kk);
-        qk = __fmaf_rn(fq[e], fk[e], qk);
-      }
-#pragma unroll
-      for (int d = 1; d < 8; d <<= 1) {
-        qq = __fadd_rn(qq, __shfl_xor_sync(0xFFu, qq, d));
-        kk = __fadd_rn(kk, __shfl_xor_sync(0xFFu, kk, d));
-        qk = __fadd_rn(qk, __shfl_xor_sync(0xFFu, qk, d));
-      }
-      const float iq = rsqrtf(__fadd_rn(qq, P.eps));
-      const float ik = rsqrtf(__fadd_rn(kk, P.eps));
-#pragma unroll
-      for (int e = 0; e < PE; ++e) {
-        st.q[PE * p + e] = __fmul_rn(fq[e], iq);
-        st.k[PE * p + e] = __fmul_rn(fk[e], ik);
-      }
-      if (p == 0) st.kq = __fmul_rn(__fmul_rn(qk, iq), ik);
+      const float kq = publish_qk<DK, IO>(&st.q[PE * p], &st.k[PE * p], rq, rk, P);
+      if (p == 0) st.kq = kq;
     }
     float alpha = 0.0f, beta = 0.0f;
     if (t < n_items) {

@@ -1,5 +1,6 @@
-// Token-by-token gated delta rule: gdn_seq, gdn_spec_verify and the
-// slot-per-candidate layout (sm_103a).
+// Token-by-token gated delta rule: gdn_seq and the slot-per-candidate layout,
+// plus the staging and token step that gdn_spec_verify (verify.cu) and the
+// fused decode (decode.cu) run too (sm_103a).
 //
 // r9700-stack v0.2.3, section 1 (r9k_gdn_seq: any number of tokens, the state
 // in registers, the batch's own rows); v0.2.4, "What it does" (one page per
@@ -25,15 +26,15 @@
 // which is the rule S <- alpha S; u = beta (v - S^T k^); S <- S + k^ u^T;
 // o = scale S^T q^ with the decay folded into the dot products, so S is read
 // once and written once per token. All arithmetic is explicit
-// round-to-nearest intrinsics and the three modes share this code path, so
-// the one-page verify is bit-identical to the slot layout.
+// round-to-nearest intrinsics and every kernel shares this code path, so the
+// one-page verify is bit-identical to the slot layout.
 #pragma once
 
 #include "common.cuh"
 
 namespace gdn {
 
-enum RuleMode { MODE_SEQ = 0, MODE_VERIFY = 1, MODE_SLOTS = 2 };
+enum RuleMode { MODE_SEQ = 0, MODE_SLOTS = 2 };
 
 constexpr int kRuleWarps = 4;
 constexpr int kRuleThreads = kRuleWarps * 32;
@@ -120,17 +121,21 @@ __device__ __forceinline__ void fetch(Fetch<DK, IO>& f, const RowSrc<IO>& src, i
   }
 }
 
-// Normalise and publish one fetched token (8 threads per token).
+// q^ and k^ of one token from its raw parts, 8 threads per token (thread p
+// holds entries [PE p, PE p + PE)): 8-lane butterfly sums of q.q, k.k and
+// q.k, then 1/sqrt(x.x + eps). Writes this thread's parts of q^, k^ and
+// returns q^.k^ (the same value in all 8 threads). Every kernel that stages
+// rows for the token step normalises through here, so they all see
+// bit-identical q^, k^.
 template <int DK, class IO>
-__device__ __forceinline__ void publish(Stage<DK>& st, const Fetch<DK, IO>& f, int t, int n_t,
-                                        int p, int h, const Params& P) {
+__device__ __forceinline__ float publish_qk(float* qdst, float* kdst, const RawVec<IO, DK / 8>& rq,
+                                            const RawVec<IO, DK / 8>& rk, const Params& P) {
   constexpr int PE = DK / 8;
-  if (t >= n_t) return;  // whole 8-lane groups take this branch together
   float fq[PE], fk[PE];
 #pragma unroll
   for (int e = 0; e < PE; ++e) {
-    fq[e] = f.q.get(e);
-    fk[e] = f.k.get(e);
+    fq[e] = rq.get(e);
+    fk[e] = rk.get(e);
   }
   float qq = 0.0f, kk = 0.0f, qk = 0.0f;
 #pragma unroll
@@ -150,19 +155,29 @@ __device__ __forceinline__ void publish(Stage<DK>& st, const Fetch<DK, IO>& f, i
   const float ik = rsqrtf(__fadd_rn(kk, P.eps));
 #pragma unroll
   for (int e = 0; e < PE; e += 4) {
-    *reinterpret_cast<float4*>(&st.q[t][PE * p + e]) =
+    *reinterpret_cast<float4*>(&qdst[e]) =
         make_float4(__fmul_rn(fq[e], iq), __fmul_rn(fq[e + 1], iq), __fmul_rn(fq[e + 2], iq),
                     __fmul_rn(fq[e + 3], iq));
-    *reinterpret_cast<float4*>(&st.k[t][PE * p + e]) =
+    *reinterpret_cast<float4*>(&kdst[e]) =
         make_float4(__fmul_rn(fk[e], ik), __fmul_rn(fk[e + 1], ik), __fmul_rn(fk[e + 2], ik),
                     __fmul_rn(fk[e + 3], ik));
   }
+  return __fmul_rn(__fmul_rn(qk, iq), ik);
+}
+
+// Normalise and publish one fetched token (8 threads per token).
+template <int DK, class IO>
+__device__ __forceinline__ void publish(Stage<DK>& st, const Fetch<DK, IO>& f, int t, int n_t,
+                                        int p, int h, const Params& P) {
+  constexpr int PE = DK / 8;
+  if (t >= n_t) return;  // whole 8-lane groups take this branch together
+  const float kq = publish_qk<DK, IO>(&st.q[t][PE * p], &st.k[t][PE * p], f.q, f.k, P);
   *reinterpret_cast<float4*>(&st.v[t][4 * p]) =
       make_float4(f.v.get(0), f.v.get(1), f.v.get(2), f.v.get(3));
   if (p == 0) {
     float alpha, beta;
     gates(P, h, f.a, f.b, alpha, beta);
-    st.sc[t] = make_float4(alpha, beta, __fmul_rn(__fmul_rn(qk, iq), ik), 0.0f);
+    st.sc[t] = make_float4(alpha, beta, kq, 0.0f);
   }
 }
 
@@ -242,6 +257,52 @@ __device__ __forceinline__ float token_step_rows(LaneState<DK / 8>& S, const flo
     }
   }
   return o;
+}
+
+// A token that only advances the state (no output), for rows replayed from
+// a record. Its S^T k^ sums pair the lanes exactly as token_step_rows does
+// (lane bit 2, then bit 1, then bit 0; fp32 addition is commutative), so the
+// state it leaves is bit-identical, without the S^T q^ half of the work.
+template <int DK, class ST>
+__device__ __forceinline__ void token_update_rows(LaneState<DK / 8>& S, const float* krow,
+                                                  const float* vrow, float alpha, float beta,
+                                                  int r8, int vcol) {
+  using L = LaneMap<DK, ST>;
+  constexpr int E = DK / 8;
+  float2 k2[E / 2];
+#pragma unroll
+  for (int i = 0; i < L::NI; ++i) {
+#pragma unroll
+    for (int e = 0; e < L::VEC; e += 4) {
+      const float4 kv = *reinterpret_cast<const float4*>(&krow[L::idx(r8, i) + e]);
+      k2[(i * L::VEC + e) / 2] = make_float2(kv.x, kv.y);
+      k2[(i * L::VEC + e) / 2 + 1] = make_float2(kv.z, kv.w);
+    }
+  }
+  const float2 vv = *reinterpret_cast<const float2*>(&vrow[vcol]);
+  float2 ak0 = make_float2(0.f, 0.f), ak1 = ak0;
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j) {
+    ak0 = __ffma2_rn(S.s[0][j], k2[j], ak0);
+    ak1 = __ffma2_rn(S.s[1][j], k2[j], ak1);
+  }
+  const float v0 = __fadd_rn(ak0.x, ak0.y), v2 = __fadd_rn(ak1.x, ak1.y);
+  const bool b2 = (r8 & 4) != 0;
+  // lanes with bit 2 = m reduce column m
+  float sk = __fadd_rn(b2 ? v2 : v0, __shfl_xor_sync(0xffffffffu, b2 ? v0 : v2, 4));
+  sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, 2));
+  sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, 1));
+  const float vm = b2 ? vv.y : vv.x;
+  const float u = __fmul_rn(beta, __fsub_rn(vm, __fmul_rn(alpha, sk)));
+  const float u_x = __shfl_xor_sync(0xffffffffu, u, 4);
+  const float u0 = b2 ? u_x : u, u1 = b2 ? u : u_x;
+  const float2 al = make_float2(alpha, alpha);
+  const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
+#pragma unroll
+  for (int j = 0; j < E / 2; ++j) {
+    S.s[0][j] = __ffma2_rn(k2[j], uu0, __fmul2_rn(al, S.s[0][j]));
+    S.s[1][j] = __ffma2_rn(k2[j], uu1, __fmul2_rn(al, S.s[1][j]));
+  }
 }
 
 template <int DK, class ST>
@@ -349,7 +410,6 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
   }
   if (MODE == MODE_SEQ && q.spec) return;
   if (MODE == MODE_SEQ && (q.len < B.min_len || q.len > B.max_len)) return;
-  if (MODE == MODE_VERIFY && !q.spec) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cg = lane >> 3, r8 = lane & 7;
@@ -384,80 +444,6 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
                          NoAfter());
     store_state<DK, ST>(Sb, S, col, r8);
     if (q.fresh && blockIdx.x == 0 && threadIdx.x == 0) *flagp = 0u;  // empty record
-  } else if constexpr (MODE == MODE_VERIFY) {
-    char* pg = page_ptr(G, pages, q.page);
-    uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
-    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
-    SpecState ss = spec_state(G, B, q, flag);
-    if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
-    if (ss.err) {
-      if (reporter) report(status, ss.err);
-      return;
-    }
-    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
-    IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
-    load_state<DK, ST>(S, Sb, col, r8);
-    // Rows 0..a of the live record slot (the replay) and this step's
-    // candidates are at most 2 Kc <= kTC rows: stage them together, once.
-    const int n_rep = (ss.width > 0) ? ss.accepted + 1 : 0;
-    const int n_all = n_rep + q.len;
-    {
-      const int ft = threadIdx.x >> 3, fp = threadIdx.x & 7;
-      Fetch<DK, IO> f;
-      RowSrc<IO> src;
-      int tt = ft;
-      if (ft < n_rep) {
-        src.rows = rec + (size_t)ss.live * G.Kc * G.rec_row;
-        src.row_stride = G.rec_row;
-        src.a = src.rows + G.C + h;
-        src.b = src.rows + G.C + G.Hv + h;
-        src.ab_stride = G.rec_row;
-      } else {
-        src = rows_in;
-        tt = ft - n_rep;
-      }
-      fetch<DK, IO>(f, src, tt, ft < n_all ? tt + 1 : 0, fp, kh, h, cb, G);
-      publish<DK, IO>(st, f, ft, n_all, fp, h, P);
-    }
-    __syncthreads();
-    const int vcol = warp * 8 + cg * 2;
-    for (int t = 0; t < n_rep; ++t) token_step<DK, ST>(S, st, t, r8, vcol, P.scale, true);
-    if (n_rep > 0) {
-      store_state<DK, ST>(Sb, S, col, r8);
-      // continue from exactly what was stored (a bf16 page rounds here)
-#pragma unroll
-      for (int m = 0; m < kColsPerLane; ++m)
-#pragma unroll
-        for (int j = 0; j < E / 2; ++j)
-          S.s[m][j] = make_float2(through<ST>(S.s[m][j].x), through<ST>(S.s[m][j].y));
-    }
-    // this step's candidates: outputs only, no per-candidate state
-    for (int t = 0; t < q.len; ++t) {
-      const float ov = token_step<DK, ST>(S, st, n_rep + t, r8, vcol, P.scale, t + 1 < q.len);
-      if ((r8 & 3) == 0) {
-        const size_t off = (((size_t)q.start + t) * G.Hv + h) * G.Dv + cb * kBV + vcol + (r8 >> 2);
-        store_out(o, out_f32, off, ov);
-      }
-    }
-    // the candidates' gates go next to their conv'd rows in the other slot
-    if (cb == 0 && threadIdx.x < q.len) {
-      IO* row = rec + ((size_t)(1 - ss.live) * G.Kc + threadIdx.x) * G.rec_row;
-      const size_t rn = (size_t)q.start + threadIdx.x;
-      row[G.C + h] = a_in[rn * G.Hv + h];
-      row[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
-    }
-    // last CTA of this request publishes the new flag word
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const uint32_t total = (uint32_t)(G.Hv * nCB);
-      const uint32_t old = atomicAdd(flagp, 256u);
-      if ((old >> 8) == total - 1) {
-        __threadfence();
-        const int live = (q.len > 0) ? 1 - ss.live : ss.live;
-        atomicExch(flagp, make_flag(live, 1 - ss.parity, q.len));
-      }
-    }
   } else {  // MODE_SLOTS
     const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
     if (src < 0 || src >= G.Kc) {
@@ -497,7 +483,6 @@ cudaError_t launch_rule_dk(int mode, const Geom& G, const Batch& B, const Params
       static_cast<const IO*>(b), o, out_f32, pages, status)
 #define GDN_RULE_MODES(IO, ST)                       \
   if (mode == MODE_SEQ) GDN_RULE_LAUNCH(IO, ST, MODE_SEQ);          \
-  else if (mode == MODE_VERIFY) GDN_RULE_LAUNCH(IO, ST, MODE_VERIFY); \
   else GDN_RULE_LAUNCH(IO, ST, MODE_SLOTS);
   if (io_bf16) {
     if (state_bf16) { GDN_RULE_MODES(bf16, bf16) } else { GDN_RULE_MODES(bf16, float) }

@@ -316,3 +316,50 @@ def test_device_errors_page_index_and_candidate_count():
     L.reset_status()
     L.verify(B, x, a, b)
     assert L.status_code() == gdn.CODES["GDN_DEV_TOO_MANY_CANDIDATES"]
+
+
+# (Hk, Hv, Dk) spanning the verify kernel's work units: a group of 1, 3, 6 or
+# 32 (value head, 32-column block) items, cut into units of 1, 2 or 4 items
+OTHER_SHAPES = [(2, 2, 32), (2, 6, 32), (2, 6, 64), (1, 8, 128)]
+
+
+@pytest.mark.parametrize("io", [synth.BF16, synth.F32])
+@pytest.mark.parametrize("hk,hv,dk", OTHER_SHAPES)
+def test_one_page_bit_identical_to_slots_other_shapes_ragged(hk, hv, dk, io):
+    """Other head shapes, 1..8 candidates per request and step, packed in a
+    shuffled row order: outputs and the committed state stay bit-identical
+    to the slot-per-candidate layout."""
+    sh = synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk)
+    R, steps = 6, 5
+    rng = np.random.default_rng(100 + hk * 1000 + hv * 10 + dk)
+    d = synth.spec(seed=int(rng.integers(1 << 30)), R=R, steps=1, n=1, sh=sh, io=io)
+    state = gdn.GDN_F32
+    L1, L2, _ = make_layers(d, R, state)
+    prev_len = np.zeros(R, np.int64)
+    for s in range(steps):
+        ln = rng.integers(1, 9, size=R)
+        order = rng.permutation(R)
+        start, _, T = synth.pack(ln, order)
+        rows = synth.rows(rng, T, sh, io)
+        x, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+        acc = np.where(prev_len > 0, rng.integers(0, np.maximum(prev_len, 1)), 0).astype(np.int32)
+        flags = spec_flags(s, R)
+        B1 = L1.batch(start, ln, flags=flags, n_accepted=acc, max_rows=8)
+        y1 = L1.conv(B1, x)
+        o1 = L1.verify(B1, y1, a, b)
+        B2 = L2.batch(start, ln, flags=flags, n_accepted=acc, max_rows=8)
+        y2, o2 = L2.spec_slots(B2, x, a, b)
+        L1.ok()
+        L2.ok()
+        assert np.array_equal(bits(y1), bits(y2)), f"conv rows differ at step {s}"
+        assert np.array_equal(bits(o1), bits(o2)), f"outputs differ at step {s}"
+        prev_len = ln
+    acc = rng.integers(0, prev_len).astype(np.int32)
+    zero = np.zeros(R, np.int32)
+    B = L1.batch(np.zeros(R, np.int32), zero, flags=spec_flags(steps, R), n_accepted=acc,
+                 num_rows=1)
+    L1.conv(B, x)
+    L1.verify(B, y1, a, b)
+    L1.ok()
+    for r in range(R):
+        assert np.array_equal(bits(L1.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
