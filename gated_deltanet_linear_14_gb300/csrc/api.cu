@@ -159,14 +159,8 @@ gdn_status rule_entry(int mode, const gdn_dims* dims, const gdn_batch* batch,
   const Batch B = make_batch(batch);
   const Params P = make_params(params, dims);
   SlotGeom SG{};
-  cudaError_t ce;
-  if (mode == 1)
-    ce = launch_verify(G, B, P, dims->io_dtype == GDN_BF16, dims->state_dtype == GDN_BF16,
-                       dims->out_dtype == GDN_F32, qkv, a, b, o, pages, status,
-                       (cudaStream_t)stream);
-  else
-    ce = rule(mode, G, B, P, SG, dims, qkv, a, b, o, pages, status, (cudaStream_t)stream);
-  if (ce != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (rule(mode, G, B, P, SG, dims, qkv, a, b, o, pages, status, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
   return GDN_OK;
 }
 

@@ -15,8 +15,8 @@ cudaError_t launch_conv_slots(const Geom& G, const Batch& B, const Params& P, co
                               int io_bf16, const void* x, const void* w, void* y, void* slots,
                               int32_t* status, cudaStream_t stream);
 
-// mode: 0 = token-by-token rule (plain requests), 2 = slot-per-candidate
-// layout (every request).
+// mode: 0 = token-by-token rule (plain requests), 1 = one-page verify (SPEC
+// requests), 2 = slot-per-candidate layout (every request).
 cudaError_t launch_rule(int mode, const Geom& G, const Batch& B, const Params& P,
                         const SlotGeom& SG, int io_bf16, int state_bf16, int out_f32,
                         const void* qkv, const void* a, const void* b, void* o, void* pages,
@@ -27,11 +27,6 @@ cudaError_t launch_rule(int mode, const Geom& G, const Batch& B, const Params& P
 cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const Params& P,
                          int state_bf16, int out_f32, const void* a, const void* b, void* o,
                          void* pages, int32_t* status, cudaStream_t stream);
-
-// One-page speculative verify (SPEC requests), pipelined over state tiles.
-cudaError_t launch_verify(const Geom& G, const Batch& B, const Params& P, int io_bf16,
-                          int state_bf16, int out_f32, const void* y, const void* a, const void* b,
-                          void* o, void* pages, int32_t* status, cudaStream_t stream);
 
 // Fused conv + rule for one token per request (plain requests).
 cudaError_t launch_decode(const Geom& G, const Batch& B, const Params& P, int io_bf16,

@@ -1,6 +1,6 @@
-// Token-by-token gated delta rule: gdn_seq and the slot-per-candidate layout,
-// plus the staging and token step that gdn_spec_verify (verify.cu) and the
-// fused decode (decode.cu) run too (sm_103a).
+// Token-by-token gated delta rule: gdn_seq, gdn_spec_verify and the
+// slot-per-candidate layout, plus the staging and token step that the fused
+// decode (decode.cu) runs too (sm_103a).
 //
 // r9700-stack v0.2.3, section 1 (r9k_gdn_seq: any number of tokens, the state
 // in registers, the batch's own rows); v0.2.4, "What it does" (one page per
@@ -26,15 +26,16 @@
 // which is the rule S <- alpha S; u = beta (v - S^T k^); S <- S + k^ u^T;
 // o = scale S^T q^ with the decay folded into the dot products, so S is read
 // once and written once per token. All arithmetic is explicit
-// round-to-nearest intrinsics and every kernel shares this code path, so the
-// one-page verify is bit-identical to the slot layout.
+// round-to-nearest intrinsics and the three modes share this code path (the
+// verify's replayed rows skip only the output half), so the one-page verify
+// is bit-identical to the slot layout.
 #pragma once
 
 #include "common.cuh"
 
 namespace gdn {
 
-enum RuleMode { MODE_SEQ = 0, MODE_SLOTS = 2 };
+enum RuleMode { MODE_SEQ = 0, MODE_VERIFY = 1, MODE_SLOTS = 2 };
 
 constexpr int kRuleWarps = 4;
 constexpr int kRuleThreads = kRuleWarps * 32;
@@ -410,6 +411,7 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
   }
   if (MODE == MODE_SEQ && q.spec) return;
   if (MODE == MODE_SEQ && (q.len < B.min_len || q.len > B.max_len)) return;
+  if (MODE == MODE_VERIFY && !q.spec) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cg = lane >> 3, r8 = lane & 7;
@@ -444,6 +446,81 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
                          NoAfter());
     store_state<DK, ST>(Sb, S, col, r8);
     if (q.fresh && blockIdx.x == 0 && threadIdx.x == 0) *flagp = 0u;  // empty record
+  } else if constexpr (MODE == MODE_VERIFY) {
+    char* pg = page_ptr(G, pages, q.page);
+    uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
+    SpecState ss = spec_state(G, B, q, flag);
+    if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
+    if (ss.err) {
+      if (reporter) report(status, ss.err);
+      return;
+    }
+    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
+    IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
+    load_state<DK, ST>(S, Sb, col, r8);
+    // Rows 0..a of the live record slot (the replay) and this step's
+    // candidates are at most 2 Kc <= kTC rows: stage them together, once.
+    const int n_rep = (ss.width > 0) ? ss.accepted + 1 : 0;
+    const int n_all = n_rep + q.len;
+    {
+      const int ft = threadIdx.x >> 3, fp = threadIdx.x & 7;
+      Fetch<DK, IO> f;
+      RowSrc<IO> src;
+      int tt = ft;
+      if (ft < n_rep) {
+        src.rows = rec + (size_t)ss.live * G.Kc * G.rec_row;
+        src.row_stride = G.rec_row;
+        src.a = src.rows + G.C + h;
+        src.b = src.rows + G.C + G.Hv + h;
+        src.ab_stride = G.rec_row;
+      } else {
+        src = rows_in;
+        tt = ft - n_rep;
+      }
+      fetch<DK, IO>(f, src, tt, ft < n_all ? tt + 1 : 0, fp, kh, h, cb, G);
+      publish<DK, IO>(st, f, ft, n_all, fp, h, P);
+    }
+    __syncthreads();
+    const int vcol = warp * 8 + cg * 2;
+    for (int t = 0; t < n_rep; ++t)
+      token_update_rows<DK, ST>(S, st.k[t], st.v[t], st.sc[t].x, st.sc[t].y, r8, vcol);
+    if (n_rep > 0) {
+      store_state<DK, ST>(Sb, S, col, r8);
+      // continue from exactly what was stored (a bf16 page rounds here)
+#pragma unroll
+      for (int m = 0; m < kColsPerLane; ++m)
+#pragma unroll
+        for (int j = 0; j < E / 2; ++j)
+          S.s[m][j] = make_float2(through<ST>(S.s[m][j].x), through<ST>(S.s[m][j].y));
+    }
+    // this step's candidates: outputs only, no per-candidate state
+    for (int t = 0; t < q.len; ++t) {
+      const float ov = token_step<DK, ST>(S, st, n_rep + t, r8, vcol, P.scale, t + 1 < q.len);
+      if ((r8 & 3) == 0) {
+        const size_t off = (((size_t)q.start + t) * G.Hv + h) * G.Dv + cb * kBV + vcol + (r8 >> 2);
+        store_out(o, out_f32, off, ov);
+      }
+    }
+    // the candidates' gates go next to their conv'd rows in the other slot
+    if (cb == 0 && threadIdx.x < q.len) {
+      IO* row = rec + ((size_t)(1 - ss.live) * G.Kc + threadIdx.x) * G.rec_row;
+      const size_t rn = (size_t)q.start + threadIdx.x;
+      row[G.C + h] = a_in[rn * G.Hv + h];
+      row[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
+    }
+    // last CTA of this request publishes the new flag word
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const uint32_t total = (uint32_t)(G.Hv * nCB);
+      const uint32_t old = atomicAdd(flagp, 256u);
+      if ((old >> 8) == total - 1) {
+        __threadfence();
+        const int live = (q.len > 0) ? 1 - ss.live : ss.live;
+        atomicExch(flagp, make_flag(live, 1 - ss.parity, q.len));
+      }
+    }
   } else {  // MODE_SLOTS
     const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
     if (src < 0 || src >= G.Kc) {
@@ -483,6 +560,7 @@ cudaError_t launch_rule_dk(int mode, const Geom& G, const Batch& B, const Params
       static_cast<const IO*>(b), o, out_f32, pages, status)
 #define GDN_RULE_MODES(IO, ST)                       \
   if (mode == MODE_SEQ) GDN_RULE_LAUNCH(IO, ST, MODE_SEQ);          \
+  else if (mode == MODE_VERIFY) GDN_RULE_LAUNCH(IO, ST, MODE_VERIFY); \
   else GDN_RULE_LAUNCH(IO, ST, MODE_SLOTS);
   if (io_bf16) {
     if (state_bf16) { GDN_RULE_MODES(bf16, bf16) } else { GDN_RULE_MODES(bf16, float) }

@@ -65,20 +65,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-// Or-reduction of a predicate over the COUNT threads of named barrier ID
-// (a barrier wait for all of them, like __syncthreads_or for a part of the
-// block).
-template <int ID, int COUNT>
-__device__ __forceinline__ bool bar_any(bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n"
-      " selp.u32 %0, 1, 0, q;\n}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "n"(ID), "n"(COUNT)
-      : "memory");
-  return r != 0;
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
                                             uint32_t bar) {
