@@ -392,10 +392,13 @@ struct NoAfter {
   __device__ void operator()(int) const {}
 };
 
-// The verify mode keeps its token steps short (at most 2 Kc rows, staged
-// once), so it trades registers for residency: 6 CTAs (24 warps) per SM.
+// Residency targets: the verify mode keeps its token steps short (at most
+// 2 Kc rows, staged once), so it trades registers for 6 CTAs (24 warps) per
+// SM; the other modes ask for 4, which keeps them near 120 registers (left
+// free, the compiler went past 150 and a long prefill's per-token chain
+// measured a quarter slower).
 template <class IO, class ST, int DK, int MODE>
-__global__ void __launch_bounds__(kRuleThreads, MODE == MODE_VERIFY ? 6 : 1)
+__global__ void __launch_bounds__(kRuleThreads, MODE == MODE_VERIFY ? 6 : 4)
 rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
             const IO* __restrict__ a_in, const IO* __restrict__ b_in, void* o, int out_f32,
             void* pages, int32_t* status) {
