@@ -104,6 +104,12 @@ class Layer:
         gdn.gdn_seq(self.dims, batch, self.params, qkv, a, b, o, self.pool.buf, self.status)
         return o
 
+    def prefill(self, batch, qkv, a, b, chunk_min_rows=0):
+        o = self.out(batch.num_rows)
+        gdn.gdn_prefill(self.dims, batch, self.params, qkv, a, b, o, self.pool.buf, self.status,
+                        chunk_min_rows)
+        return o
+
     def verify(self, batch, qkv, a, b):
         o = self.out(batch.num_rows)
         gdn.gdn_spec_verify(self.dims, batch, self.params, qkv, a, b, o, self.pool.buf,

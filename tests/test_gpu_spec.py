@@ -197,7 +197,10 @@ def test_commit_then_plain_decode_continues():
         assert rel(f64(L.pool.state_math(r)), S_ref[0]) <= TOL
 
 
-def test_mixed_prefill_and_spec_step_through_row_map():
+@pytest.mark.parametrize("prefill_entry", ["seq", "prefill"])
+def test_mixed_prefill_and_spec_step_through_row_map(prefill_entry):
+    """gdn_seq, or gdn_prefill (prefills of 128+ rows take the chunked form),
+    for the plain rows of a step that also verifies spec requests."""
     for shuffled in (False, True):
         d = synth.mixed(shuffled=shuffled)
         sh, n, ns, npf = d["shapes"], d["n"], d["n_spec"], d["n_prefill"]
@@ -220,7 +223,7 @@ def test_mixed_prefill_and_spec_step_through_row_map():
         B = L.batch(d["row_start"], lengths, flags=flags, n_accepted=acc, order=order)
         x, a, b = to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"])
         y = L.conv(B, x)
-        o = L.seq(B, y, a, b)
+        o = L.seq(B, y, a, b) if prefill_entry == "seq" else L.prefill(B, y, a, b)
         o2 = L.verify(B, y, a, b)
         L.ok()
         row_is_spec = np.zeros(d["T"], bool)
@@ -228,7 +231,8 @@ def test_mixed_prefill_and_spec_step_through_row_map():
             row_is_spec[d["row_start"][r]: d["row_start"][r] + lengths[r]] = spec[r]
         o = torch.where(torch.from_numpy(row_is_spec).cuda()[:, None, None], o2, o)
         # prefills: fp32 conv mirror from a zero window, bf16 rows, fp64 rule
-        for r in np.nonzero(~spec)[0][:3]:
+        # (every prefill on the dispatching entry point: both forms run)
+        for r in np.nonzero(~spec)[0][: (3 if prefill_entry == "seq" else npf)]:
             sl = slice(d["row_start"][r], d["row_start"][r] + lengths[r])
             yy, _ = oracle.conv_f32(d["x"].value[sl], np.zeros((1, 3, sh.C)), d["conv_w"].value,
                                     [0], [lengths[r]])
