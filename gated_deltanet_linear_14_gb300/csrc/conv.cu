@@ -28,11 +28,12 @@ namespace gdn {
 constexpr int kConvThreads = 128;
 // The SiLU (own exp and an exact division per element) makes the conv
 // issue-bound rather than HBM-bound, so residency matters more than wide
-// vectors: 8-byte vectors and 8 CTAs (32 warps) per SM ran a 32k-row batch in
-// 0.57 ms, against 0.68 ms with 16-byte vectors at 3 CTAs per SM.
+// vectors or deep load batches: 8-byte vectors, 4 rows in flight and 8 CTAs
+// (32 warps) per SM ran a 32k-row batch in 0.50 ms, against 0.57 ms with 8
+// rows in flight and 0.68 ms with 16-byte vectors at 3 CTAs per SM.
 constexpr int kConvVecBytes = 8;
 constexpr int kConvRows = 32;  // rows per tile (>= W-1)
-constexpr int kConvBatch = 8;  // rows whose loads are in flight together
+constexpr int kConvBatch = 4;  // rows whose loads are in flight together
 
 template <class IO, class YT, int W, bool SLOTS>
 __global__ void __launch_bounds__(kConvThreads, 8)
