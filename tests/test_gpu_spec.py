@@ -367,3 +367,45 @@ def test_one_page_bit_identical_to_slots_other_shapes_ragged(hk, hv, dk, io):
     L1.ok()
     for r in range(R):
         assert np.array_equal(bits(L1.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
+
+
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_switch_to_slot_layout_midstream(state):
+    """Prefix caching keeps the stock per-candidate pages (r9700-stack v0.2.4,
+    "What it does"): a request that ran one-page steps is committed, its
+    page's state and window are copied into slot 0 of a slot pool, and the
+    slot layout continues from there, bit-identical to a request that used
+    the slot layout from the start."""
+    d = synth.spec(R=4, steps=4)
+    R, n = 4, d["n"]
+    start, ln = d["row_start"][:R], d["row_len"][:R]
+    L1, L2, _ = make_layers(d, R, state)          # one-page; slots from the start
+    for s in range(2):
+        x, a, b = step_rows(d, s, R, n)
+        acc = d["accepted"][s][:R]
+        one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        L2.spec_slots(L2.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc), x, a, b)
+        L1.ok()
+        L2.ok()
+    # commit the one-page request, then hand its page to a fresh slot pool
+    acc = d["accepted"][2][:R]
+    zero = np.zeros(R, np.int32)
+    B = L1.batch(start, zero, flags=spec_flags(2, R), n_accepted=acc, num_rows=int(start[-1]) + n)
+    L1.conv(B, x)
+    L1.verify(B, x, a, b)
+    L1.ok()
+    L3 = Layer(d["shapes"], d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
+               num_pages=R, slots=True)
+    for r in range(R):
+        L3.slots.state(r, 0).copy_(L1.pool.state(r))
+        L3.slots.window(r, 0).copy_(L1.pool.window(r)[:3])
+    x, a, b = step_rows(d, 2, R, n)
+    y2, o2 = L2.spec_slots(L2.batch(start, ln, flags=spec_flags(2, R), n_accepted=acc), x, a, b)
+    y3, o3 = L3.spec_slots(L3.batch(start, ln, flags=spec_flags(2, R), n_accepted=zero), x, a, b)
+    L2.ok()
+    L3.ok()
+    assert np.array_equal(bits(y2), bits(y3))
+    assert np.array_equal(bits(o2), bits(o3))
+    for r in range(R):
+        for i in range(n):
+            assert np.array_equal(bits(L2.slots.state(r, i)), bits(L3.slots.state(r, i)))
