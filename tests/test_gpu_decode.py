@@ -140,3 +140,31 @@ def test_decode_skips_spec_zeroes_empty_fresh_and_refuses_open_records():
     B = L1.batch([0, 1], [1, 2], page=pages[:2], flags=[0, 0], num_rows=4, max_rows=1)
     gdn.gdn_decode(L1.dims, B, L1.params, x, L1.conv_w, a, b, o, L1.pool.buf, L1.status)
     assert L1.status_code() == gdn.CODES["GDN_DEV_BAD_ROWS"]
+
+
+def test_max_request_count_in_one_launch():
+    """65535 one-token requests (the most one launch takes; more is refused
+    on the host) through gdn_decode and through gdn_conv + gdn_seq: equal bit
+    for bit, and sampled requests within 1e-4 of the oracle."""
+    R = 65535
+    sh = synth.Shapes(Hk=2, Hv=2, Dk=32, Dv=32)
+    d = synth.decode(R=R, sh=sh, io=synth.F32)
+    (L1, L2), pages, S0 = two_layers(d, R, gdn.GDN_F32, gdn.GDN_F32)
+    x, a, b = to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"])
+    B1 = L1.batch(d["row_start"], d["row_len"], page=pages)
+    o1 = L1.out(R)
+    gdn.gdn_decode(L1.dims, B1, L1.params, x, L1.conv_w, a, b, o1, L1.pool.buf, L1.status)
+    L1.ok()
+    B2 = L2.batch(d["row_start"], d["row_len"], page=pages)
+    o2 = L2.seq(B2, L2.conv(B2, x), a, b)
+    L2.ok()
+    assert np.array_equal(bits(o1), bits(o2))
+    assert torch.equal(L1.pool.buf, L2.pool.buf)
+    for r in (0, 1, 40000, R - 1):
+        y, _ = oracle.conv_f64(d["x"].value[r:r + 1], d["hist0"].value[r:r + 1], d["conv_w"].value,
+                               [0], [1])
+        o_ref, S_ref = oracle.gdn_f64(y, d["a"].value[r:r + 1], d["b"].value[r:r + 1], d["A_log"],
+                                      d["dt_bias"], [0], [1], sh.Hk, sh.Hv, sh.Dk, sh.Dv,
+                                      S0=S0[r:r + 1])
+        assert rel(f64(o1[r]), o_ref[0]) <= 1e-4, r
+        assert rel(f64(L1.pool.state_math(int(pages[r]))), S_ref[0]) <= 1e-4, r
