@@ -514,14 +514,14 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
       row[G.C + h] = a_in[rn * G.Hv + h];
       row[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
     }
-    // last CTA of this request publishes the new flag word
-    __syncthreads();
+    // The last CTA of this request publishes the new flag word. No fence
+    // orders the page data first: only later launches read it. The counter
+    // needs none either: every CTA read the flag at its start, before its
+    // own increment of the same word, so the publish follows every read.
     if (threadIdx.x == 0) {
-      __threadfence();
       const uint32_t total = (uint32_t)(G.Hv * nCB);
       const uint32_t old = atomicAdd(flagp, 256u);
       if ((old >> 8) == total - 1) {
-        __threadfence();
         const int live = (q.len > 0) ? 1 - ss.live : ss.live;
         atomicExch(flagp, make_flag(live, 1 - ss.parity, q.len));
       }
