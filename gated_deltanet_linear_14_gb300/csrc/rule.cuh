@@ -436,16 +436,15 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
   if constexpr (MODE == MODE_SEQ) {
     char* pg = page_ptr(G, pages, q.page);
     uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+    if (!q.fresh && q.len == 0) return;  // nothing to do
+    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
+    // the state load is issued before the flag check (one round trip, not
+    // two); a refused request only discards it
+    if (q.fresh) zero_state<E>(S);
+    else load_state<DK, ST>(S, Sb, col, r8);
     if (!q.fresh && flag_width(*flagp) != 0) {
       if (reporter) report(status, GDN_DEV_RECORD_OPEN);
       return;
-    }
-    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
-    if (q.fresh) {
-      zero_state<E>(S);
-    } else {
-      if (q.len == 0) return;  // nothing to do
-      load_state<DK, ST>(S, Sb, col, r8);
     }
     run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P, true,
                          NoAfter());
@@ -455,15 +454,17 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
     char* pg = page_ptr(G, pages, q.page);
     uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
     const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
+    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
+    IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
+    // the state load is issued before the flag is checked (one round trip,
+    // not two); a refused request only discards it
+    load_state<DK, ST>(S, Sb, col, r8);
     SpecState ss = spec_state(G, B, q, flag);
     if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
     if (ss.err) {
       if (reporter) report(status, ss.err);
       return;
     }
-    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
-    IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
-    load_state<DK, ST>(S, Sb, col, r8);
     // Rows 0..a of the live record slot (the replay) and this step's
     // candidates are at most 2 Kc <= kTC rows: stage them together, once.
     const int n_rep = (ss.width > 0) ? ss.accepted + 1 : 0;
