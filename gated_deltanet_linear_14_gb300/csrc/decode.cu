@@ -32,6 +32,9 @@ using namespace umma;
 // 4 stages (70 KB, 3 CTAs per SM) the 64-request batch ran 8 % slower and
 // with 2 stages (6 CTAs per SM) no faster.
 constexpr int kDecStages = 3;
+// Item i's stage is refilled (with item i + kDecStages) at the barrier of
+// item i + 1, after its own wait: one stage would wait on a copy never issued.
+static_assert(kDecStages >= 2, "the ring needs at least two stages");
 constexpr int kDecMaxRow = 2 * 128 + 512;  // q | k | the group's v (items <= kTC)
 constexpr long long kDecWaitLimit = 1LL << 26;
 
