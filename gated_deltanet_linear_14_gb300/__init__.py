@@ -106,6 +106,7 @@ def load_library(path: str = LIB_PATH):
             "gdn_spec_slots": ([D, B, PR, P, P, P, P, P, P, P, P, P], I),
             "gdn_chunk_prefill_workspace_bytes": ([D, B], S),
             "gdn_chunk_prefill": ([D, B, PR, P, P, P, P, P, P, S, P, P], I),
+            "gdn_check_bounded_wait": ([ctypes.c_int64, P, P], I),
             "gdn_strerror": ([I], ctypes.c_char_p),
             "gdn_abi_version": ([], I),
         }
@@ -221,6 +222,11 @@ def gdn_chunk_prefill(dims, batch, params, qkv, a, b, o, pages, workspace, works
                                             _ptr(o), _ptr(pages), _ptr(workspace),
                                             int(workspace_bytes), _ptr(status), _stream(stream)),
            "gdn_chunk_prefill")
+
+
+def gdn_check_bounded_wait(limit_ns, status, stream=None):
+    _check(load_library().gdn_check_bounded_wait(int(limit_ns), _ptr(status), _stream(stream)),
+           "gdn_check_bounded_wait")
 
 
 def gdn_strerror(code: int) -> str:

@@ -10,6 +10,24 @@
 
 #include "gdn.h"
 #include "kernels.h"
+#include "umma.cuh"
+
+namespace gdn {
+
+// One thread waits on an mbarrier that nothing arrives at; the bounded wait
+// gives up after limit_ns and the kernel reports GDN_DEV_TIMEOUT, the path
+// every kernel takes when one of its own copies or MMAs does not complete.
+__global__ void wait_check_kernel(uint64_t limit_ns, int32_t* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    const uint32_t b = umma::smem_u32(&bar);
+    umma::mbar_init(b, 1);
+    umma::mbar_fence_init();
+    if (!umma::mbar_wait(b, 0, limit_ns)) report(status, GDN_DEV_TIMEOUT);
+  }
+}
+
+}  // namespace gdn
 
 namespace {
 
@@ -371,6 +389,12 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch, const
                    o, pages, status, (cudaStream_t)stream) != cudaSuccess)
     return GDN_ERR_LAUNCH;
   return GDN_OK;
+}
+
+gdn_status gdn_check_bounded_wait(int64_t limit_ns, int32_t* status, gdn_stream_t stream) {
+  if (!status || limit_ns <= 0 || limit_ns > 10000000000LL) return GDN_ERR_INVALID_ARG;
+  gdn::wait_check_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ns, status);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH;
 }
 
 const char* gdn_strerror(int32_t s) {

@@ -62,8 +62,6 @@ constexpr uint32_t kChunkSmem = OFF_VEC + 8 * 64 * 4 + 2048;  // + 1024-byte ali
 constexpr uint32_t TM_D1 = 0, TM_W = 64, TM_U = 128, TM_WS = 192, TM_S = 256, TM_OQ = 384,
                    TM_OP = 448;
 
-constexpr long long kWaitLimit = 1LL << 26;
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
   const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
   const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
@@ -268,7 +266,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   uint32_t mma_count = 0;
   bool fail = false;
   auto wait_mma = [&]() -> bool {
-    const bool ok = mbar_wait(bar_mma, mma_count & 1, kWaitLimit);
+    const bool ok = mbar_wait(bar_mma, mma_count & 1);
     ++mma_count;
     const bool any_fail = __syncthreads_or(!ok);
     tc_fence_after();
@@ -284,7 +282,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       b_t = to_f(b_in[(R0 + tid) * G.Hv + h]);
     }
     {
-      const bool ok = mbar_wait(bar_tma, c & 1, kWaitLimit);
+      const bool ok = mbar_wait(bar_tma, c & 1);
       if (__syncthreads_or(!ok)) { fail = true; break; }
     }
     if (n_c < kCL) {

@@ -36,7 +36,6 @@ constexpr int kDecStages = 3;
 // item i + 1, after its own wait: one stage would wait on a copy never issued.
 static_assert(kDecStages >= 2, "the ring needs at least two stages");
 constexpr int kDecMaxRow = 2 * 128 + 512;  // q | k | the group's v (items <= kTC)
-constexpr long long kDecWaitLimit = 1LL << 26;
 
 // What the items of one CTA share: one token's q^ and k^, and per item the
 // value block and (alpha, beta, q^.k^).
@@ -217,7 +216,7 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
     const int h = h0 + i / nCB, cb = i % nCB;
     LaneState<DK / 8> S;
     if (stream_state) {
-      const bool ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((i / kDecStages) & 1), kDecWaitLimit);
+      const bool ok = mbar_wait(smem_u32(&full[s]), (uint32_t)((i / kDecStages) & 1));
       // one barrier per item: past it every thread has also finished reading
       // the previous item's stage, which can then be refilled
       if (__syncthreads_or(!ok)) {
@@ -245,7 +244,7 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
     // let copies still in flight land before the CTA's shared memory goes away
     if (tid == 0)
       for (int j = consumed; j < issued; ++j)
-        mbar_wait(smem_u32(&full[j % kDecStages]), (uint32_t)((j / kDecStages) & 1), kDecWaitLimit);
+        mbar_wait(smem_u32(&full[j % kDecStages]), (uint32_t)((j / kDecStages) & 1));
     return;
   }
   if (q.fresh && kh == 0 && tid == 0) *flagp = 0u;  // empty record

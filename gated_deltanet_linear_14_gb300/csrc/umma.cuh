@@ -37,10 +37,27 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                : "memory");
 }
 
+// The global nanosecond timer.
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every on-chip wait gives up after this much global time: the copies and
+// MMAs a kernel waits for take microseconds, so a wait this long means one
+// of them will not complete. kWaitPolls bounds the polls as well, in case
+// the timer does not advance.
+constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr uint32_t kWaitPolls = 1u << 26;
+
 // Wait for the phase with the given parity to complete; gives up after
-// `limit` polls and returns false (the caller reports and unwinds).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
-  for (long long i = 0; i < limit; ++i) {
+// limit_ns of global time and returns false (the caller reports and
+// unwinds).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitNs) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -49,6 +66,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long lo
         : "r"(bar), "r"(parity)
         : "memory");
     if (ok) return true;
+    const uint64_t now = global_ns();
+    if (i == 0) t0 = now;
+    else if (now - t0 > limit_ns) return false;
   }
   return false;
 }

@@ -321,6 +321,19 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch,
                        int32_t chunk_min_rows, int32_t* status,
                        gdn_stream_t stream);
 
+/* Failure-detection check of the bounded on-chip waits. Every wait a
+ * kernel makes on its own bulk copies or MMAs (gdn_decode,
+ * gdn_chunk_prefill) gives up after one second of global time: the kernel
+ * then writes GDN_DEV_TIMEOUT to *status, lets its copies in flight land,
+ * frees its tensor memory and returns, so the context stays usable. This
+ * call runs that path on demand: one block waits on an mbarrier that
+ * nothing arrives at, gives up after limit_ns of global time
+ * (0 < limit_ns <= 10^10) and writes GDN_DEV_TIMEOUT to *status.
+ *   status  device int32 (first error wins, as for every entry point)
+ * Returns GDN_ERR_INVALID_ARG for a NULL status or a limit out of range. */
+gdn_status gdn_check_bounded_wait(int64_t limit_ns, int32_t* status,
+                                  gdn_stream_t stream);
+
 /* Text for a status code (host, static storage). */
 const char* gdn_strerror(int32_t status);
 

@@ -168,3 +168,10 @@ def test_strerror_covers_every_code(lib):
     for code in gdn.STATUS:
         assert gdn.gdn_strerror(code) != "unknown status"
     assert gdn.gdn_strerror(12345) == "unknown status"
+
+
+def test_bounded_wait_check_validates_arguments(lib):
+    assert lib.gdn_check_bounded_wait(1000, None, None) == -1          # no status word
+    assert lib.gdn_check_bounded_wait(0, 8, None) == -1                 # limit <= 0
+    assert lib.gdn_check_bounded_wait(-5, 8, None) == -1
+    assert lib.gdn_check_bounded_wait(10 ** 10 + 1, 8, None) == -1      # above 10 s
