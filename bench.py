@@ -377,6 +377,7 @@ def extra_workloads(device, peaks, args, only=None):
     out = {}
     for name, fn in (("spec_verify_fp32_state", lambda: bench_spec(device, peaks, "f32")),
                      ("spec_verify_bf16_state", lambda: bench_spec(device, peaks, "bf16")),
+                     ("spec_slots_fp32_state", lambda: bench_slots(device, peaks)),
                      ("mixed_prefill_spec", lambda: bench_mixed(device, peaks)),
                      ("long_prefill_token_by_token", lambda: bench_long_seq(device, peaks)),
                      ("long_prefill_chunked", lambda: bench_long_chunk(device, peaks)),
@@ -495,6 +496,62 @@ def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
             "tokens_per_s": T * K / el, "verify_gbs": gbs,
             "verify_frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
             "verify_tflops_fp32": flops / (ver_ms / 1e3) / 1e12, "status": code}
+
+
+def bench_slots(device, peaks, K=20, W=4, pools=2):
+    """The slot-per-candidate layout on the spec workload, for contrast with
+    the one-page verify: 64 requests, 1+7 candidates; each request resumes
+    from slot a and stores the state (and conv window) after every candidate,
+    so a step reads one state and writes eight."""
+    import torch
+    import gated_deltanet_linear_14_gb300 as gdn
+    from gated_deltanet_linear_14_gb300.pages import SlotPool
+    d = synth.spec(steps=2)
+    sh, R, n = d["shapes"], d["R"], d["n"]
+    dims = gdn.make_dims(sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, 8, gdn.GDN_BF16, gdn.GDN_F32,
+                         gdn.GDN_BF16)
+    A_log = torch.from_numpy(d["A_log"]).to(device)
+    dt = torch.from_numpy(d["dt_bias"]).to(device)
+    params = gdn.make_params(A_log, dt)
+    conv_w = _put_io(torch, device, d["conv_w"])
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    S_page = torch.from_numpy(d["S0"]).transpose(-1, -2).contiguous().to(device)
+    hist = _put_io(torch, device, d["hist0"])
+    pl = []
+    for _ in range(pools):   # 2 x 1.2 GB of slots: far above the 129 MB L2
+        pool = SlotPool(dims, R, device=device)
+        for r in range(R):
+            for i in range(n):
+                pool.state(r, i).copy_(S_page[r])
+                pool.window(r, i).copy_(hist[r])
+        pl.append(pool)
+    rows = d["step_rows"][0]
+    x, a, b = (_put_io(torch, device, rows[k]) for k in ("x", "a", "b"))
+    T = R * n
+    y = torch.empty(T, sh.C, dtype=torch.bfloat16, device=device)
+    o = torch.empty(T, sh.Hv, sh.Dv, dtype=torch.bfloat16, device=device)
+    rng = np.random.default_rng(2)
+    accs = rng.integers(0, n, size=(8, R))
+    flags = np.full(R, gdn.GDN_REQ_SPEC)
+    batches = [_dev_batch(gdn, torch, device, d["row_start"], d["row_len"], np.arange(R), flags,
+                          acc=accs[k]) for k in range(8)]
+
+    def launch(i):
+        gdn.gdn_spec_slots(dims, batches[i % 8], params, x, conv_w, y, a, b, o, pl[i % pools].buf,
+                           status)
+
+    for i in range(W):
+        launch(i)
+    torch.cuda.synchronize()
+    el = time_steps(lambda i: launch(W + i), K, torch)
+    code = int(status.item())
+    state_bytes = (1 + n) * R * sh.Hv * sh.Dk * sh.Dv * 4
+    gbs = state_bytes / (el / K) / 1e9
+    return {"workload": f"slot layout: {R} requests, 1+7 candidates, fp32 state, conv + rule "
+                        "(a state per candidate)",
+            "ms_per_step": el / K * 1e3, "tokens_per_s": T * K / el,
+            "state_bytes_per_step": state_bytes, "state_gbs": gbs,
+            "state_frac_of_hbm": gbs / float(peaks["hbm_gbs"]), "status": code}
 
 
 def bench_mixed(device, peaks, K=20, W=4):
@@ -758,9 +815,20 @@ def cpu_baseline(seconds=10.0, steps=None):
         el = time.perf_counter() - t0
         if (steps is not None and n >= steps) or (steps is None and el >= seconds):
             break
+    # the same oracle on one host thread, for the per-core figure
+    n1, t1 = 0, time.perf_counter()
+    while True:
+        oracle_decode_step(d, 1)
+        n1 += 1
+        el1 = time.perf_counter() - t1
+        if n1 >= (1 if steps is not None else 3) and el1 >= min(seconds, 3.0) or n1 >= 50:
+            break
     return {"value": d["R"] * n / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} full decode steps (64 requests x 1 token, fp64 conv + rule) in "
-                      f"{el:.1f} s", "steps": n}
+                      f"{el:.1f} s", "steps": n,
+            "single_thread": {"value": d["R"] * n1 / el1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"{n1} full decode steps on one host thread in "
+                                        f"{el1:.1f} s"}}
 
 
 def run_reference(args, world, rank):
@@ -799,7 +867,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--only", default=None,
                     help="run one secondary workload alone (spec_verify_fp32_state, "
-                         "spec_verify_bf16_state, mixed_prefill_spec, "
+                         "spec_verify_bf16_state, spec_slots_fp32_state, mixed_prefill_spec, "
                          "long_prefill_token_by_token, conv_long_rows)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
