@@ -28,11 +28,11 @@ def spec_flags(step, R):
     return np.full(R, SPEC | (PAR if step % 2 else 0), np.int64)
 
 
-def make_layers(d, R, state, slots=True):
+def make_layers(d, R, state, slots=True, Kc=8):
     sh = d["shapes"]
-    L1 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
+    L1 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=Kc, state=state,
                num_pages=R)
-    L2 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
+    L2 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=Kc, state=state,
                num_pages=R, slots=slots) if slots else None
     hist = to_dev(d["hist0"])[:R]
     S0 = d["S0"][:R]
@@ -322,36 +322,31 @@ def test_device_errors_page_index_and_candidate_count():
     assert L.status_code() == gdn.CODES["GDN_DEV_TOO_MANY_CANDIDATES"]
 
 
-# (Hk, Hv, Dk) spanning the verify kernel's work units: a group of 1, 3, 6 or
-# 32 (value head, 32-column block) items, cut into units of 1, 2 or 4 items
+# (Hk, Hv, Dk): GQA groups of 1, 3 and 8 value heads per q/k head, and the
+# three supported head dimensions (one, two or four 32-column blocks per head)
 OTHER_SHAPES = [(2, 2, 32), (2, 6, 32), (2, 6, 64), (1, 8, 128)]
 
 
-@pytest.mark.parametrize("io", [synth.BF16, synth.F32])
-@pytest.mark.parametrize("hk,hv,dk", OTHER_SHAPES)
-def test_one_page_bit_identical_to_slots_other_shapes_ragged(hk, hv, dk, io):
-    """Other head shapes, 1..8 candidates per request and step, packed in a
-    shuffled row order: outputs and the committed state stay bit-identical
-    to the slot-per-candidate layout."""
-    sh = synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk)
-    R, steps = 6, 5
-    rng = np.random.default_rng(100 + hk * 1000 + hv * 10 + dk)
+def _ragged_vs_slots(sh, io, seed, Kc=8, R=6, steps=5):
+    """1..Kc candidates per request and step, packed in a shuffled row order:
+    outputs and the committed state stay bit-identical to the slot layout."""
+    rng = np.random.default_rng(seed)
     d = synth.spec(seed=int(rng.integers(1 << 30)), R=R, steps=1, n=1, sh=sh, io=io)
     state = gdn.GDN_F32
-    L1, L2, _ = make_layers(d, R, state)
+    L1, L2, _ = make_layers(d, R, state, Kc=Kc)
     prev_len = np.zeros(R, np.int64)
     for s in range(steps):
-        ln = rng.integers(1, 9, size=R)
+        ln = rng.integers(1, Kc + 1, size=R)
         order = rng.permutation(R)
         start, _, T = synth.pack(ln, order)
         rows = synth.rows(rng, T, sh, io)
         x, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
         acc = np.where(prev_len > 0, rng.integers(0, np.maximum(prev_len, 1)), 0).astype(np.int32)
         flags = spec_flags(s, R)
-        B1 = L1.batch(start, ln, flags=flags, n_accepted=acc, max_rows=8)
+        B1 = L1.batch(start, ln, flags=flags, n_accepted=acc, max_rows=Kc)
         y1 = L1.conv(B1, x)
         o1 = L1.verify(B1, y1, a, b)
-        B2 = L2.batch(start, ln, flags=flags, n_accepted=acc, max_rows=8)
+        B2 = L2.batch(start, ln, flags=flags, n_accepted=acc, max_rows=Kc)
         y2, o2 = L2.spec_slots(B2, x, a, b)
         L1.ok()
         L2.ok()
@@ -367,6 +362,20 @@ def test_one_page_bit_identical_to_slots_other_shapes_ragged(hk, hv, dk, io):
     L1.ok()
     for r in range(R):
         assert np.array_equal(bits(L1.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
+
+
+@pytest.mark.parametrize("io", [synth.BF16, synth.F32])
+@pytest.mark.parametrize("hk,hv,dk", OTHER_SHAPES)
+def test_one_page_bit_identical_to_slots_other_shapes_ragged(hk, hv, dk, io):
+    _ragged_vs_slots(synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk), io,
+                     100 + hk * 1000 + hv * 10 + dk)
+
+
+@pytest.mark.parametrize("Kc", [1, 3])
+def test_one_page_bit_identical_to_slots_small_record(Kc):
+    """A record of 1 row (no drafts: every step verifies one token, so the
+    replay is always row 0) or 3 rows; the window then holds 3 + Kc columns."""
+    _ragged_vs_slots(synth.Shapes(Hk=2, Hv=4, Dk=64, Dv=64), synth.BF16, 7 + Kc, Kc=Kc)
 
 
 @pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
