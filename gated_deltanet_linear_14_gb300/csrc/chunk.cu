@@ -109,63 +109,107 @@ __device__ __forceinline__ void store_half_hilo(uint8_t* hi_tile, uint8_t* lo_ti
   }
 }
 
-// T = (I + A)^-1 for a strictly lower 64 x 64 A (row-major fp32, stride 64),
-// in 16 x 16 blocks: diagonal blocks by forward substitution (one thread per
-// block column), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj by block
-// distance. Xs: 3 x 256 floats of scratch. All 128 threads call this.
+// A and T ([64][64] fp32 in shared memory) keep the 16-byte chunk q of row r
+// at chunk q ^ (r & 15): threads that each own a row and touch the same
+// columns then hit different banks (a plain 256-byte row stride sent all of
+// them to the same four banks).
+__device__ __forceinline__ int mat_idx(int r, int c) {
+  return (r << 6) | ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
+}
+
+// T = (I + A)^-1 for a strictly lower 64 x 64 A (mat_idx layout), in 16 x 16
+// blocks: diagonal blocks by forward substitution (one thread per block
+// column), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj by block distance,
+// each thread forming 4 adjacent outputs from 16-byte loads. Xs: 3 x 256
+// floats of scratch. All threads of the CTA call this.
 __device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, float* Xs, int tid) {
   if (tid < 64) {
-    const int b = tid >> 4, cc = tid & 15;
-    const float* Ab = Am + (16 * b) * 64 + 16 * b;
+    // the block's row r + 1 is loaded (four 16-byte loads) while row r is
+    // solved, so no multiply-add waits on its own load
+    const int b = tid >> 4, cc = tid & 15, R0 = 16 * b;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.0f : 0.0f;
+    float4 nxt[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      nxt[q] = *reinterpret_cast<const float4*>(&Am[mat_idx(R0 + 1, R0 + 4 * q)]);
 #pragma unroll
     for (int r = 1; r < 16; ++r) {
+      float a[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        a[4 * q] = nxt[q].x; a[4 * q + 1] = nxt[q].y; a[4 * q + 2] = nxt[q].z; a[4 * q + 3] = nxt[q].w;
+      }
+      if (r + 1 < 16) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          nxt[q] = *reinterpret_cast<const float4*>(&Am[mat_idx(R0 + r + 1, R0 + 4 * q)]);
+      }
       float acc0 = 0.0f, acc1 = 0.0f;
 #pragma unroll
       for (int k = 0; k < r; k += 2) {
-        acc0 = __fmaf_rn(Ab[r * 64 + k], x[k], acc0);
-        if (k + 1 < r) acc1 = __fmaf_rn(Ab[r * 64 + k + 1], x[k + 1], acc1);
+        acc0 = __fmaf_rn(a[k], x[k], acc0);
+        if (k + 1 < r) acc1 = __fmaf_rn(a[k + 1], x[k + 1], acc1);
       }
       if (r > cc) x[r] = -__fadd_rn(acc0, acc1);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tm[(16 * b + r) * 64 + 16 * b + cc] = x[r];
+    for (int r = 0; r < 16; ++r) Tm[mat_idx(R0 + r, R0 + cc)] = x[r];
   } else {
     // blocks above the diagonal are zero
     for (int idx = tid - 64; idx < 6 * 256; idx += kChunkThreads - 64) {
       const int blk = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
       const int bi = (blk < 3) ? 0 : (blk < 5 ? 1 : 2);
       const int bj = (blk < 3) ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      Tm[(16 * bi + r) * 64 + 16 * bj + cc] = 0.0f;
+      Tm[mat_idx(16 * bi + r, 16 * bj + cc)] = 0.0f;
     }
   }
   __syncthreads();
+#pragma unroll
   for (int d = 1; d < 4; ++d) {
     const int nb = 4 - d;
-    // X_ij = sum_{k=j}^{i-1} A_ik T_kj, 16 terms per block step, 4 partial sums
-    for (int idx = tid; idx < nb * 256; idx += kChunkThreads) {
-      const int bj = idx >> 8, bi = bj + d, r = (idx >> 4) & 15, cc = idx & 15;
-      const float* arow = Am + (16 * bi + r) * 64;
-      const float* tcol = Tm + 16 * bj + cc;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      for (int kb = 16 * bj; kb < 16 * bi; kb += 16) {
+    // X_ij = sum_{k=j}^{i-1} A_ik T_kj: thread -> (block column bj, row r,
+    // columns 4q .. 4q+3)
+    if (tid < nb * 64) {
+      const int bj = tid >> 6, bi = bj + d, r = (tid >> 2) & 15, q = tid & 3;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k & 3] = __fmaf_rn(arow[kb + k], tcol[(kb + k) * 64], acc[k & 3]);
+      for (int it = 0; it < 4 * d; ++it) {
+        const int kb = 16 * bj + 4 * it;
+        const float4 a4 = *reinterpret_cast<const float4*>(&Am[mat_idx(16 * bi + r, kb)]);
+        const float ak[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 t4 = *reinterpret_cast<const float4*>(&Tm[mat_idx(kb + e, 16 * bj + 4 * q)]);
+          acc.x = __fmaf_rn(ak[e], t4.x, acc.x);
+          acc.y = __fmaf_rn(ak[e], t4.y, acc.y);
+          acc.z = __fmaf_rn(ak[e], t4.z, acc.z);
+          acc.w = __fmaf_rn(ak[e], t4.w, acc.w);
+        }
       }
-      Xs[idx] = __fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+      *reinterpret_cast<float4*>(&Xs[(bj << 8) + r * 16 + 4 * q]) = acc;
     }
     __syncthreads();
     // T_ij = -T_ii X_ij (T_ii is stored with zeros above its diagonal)
-    for (int idx = tid; idx < nb * 256; idx += kChunkThreads) {
-      const int bj = idx >> 8, bi = bj + d, r = (idx >> 4) & 15, cc = idx & 15;
-      const float* trow = Tm + (16 * bi + r) * 64 + 16 * bi;
-      const float* xcol = Xs + (bj << 8) + cc;
-      float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (tid < nb * 64) {
+      const int bj = tid >> 6, bi = bj + d, r = (tid >> 2) & 15, q = tid & 3;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-      for (int m = 0; m < 16; ++m) acc[m & 3] = __fmaf_rn(trow[m], xcol[m * 16], acc[m & 3]);
-      Tm[(16 * bi + r) * 64 + 16 * bj + cc] = -__fadd_rn(__fadd_rn(acc[0], acc[1]), __fadd_rn(acc[2], acc[3]));
+      for (int m0 = 0; m0 < 16; m0 += 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(&Tm[mat_idx(16 * bi + r, 16 * bi + m0)]);
+        const float tk[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(bj << 8) + (m0 + e) * 16 + 4 * q]);
+          acc.x = __fmaf_rn(tk[e], x4.x, acc.x);
+          acc.y = __fmaf_rn(tk[e], x4.y, acc.y);
+          acc.z = __fmaf_rn(tk[e], x4.z, acc.z);
+          acc.w = __fmaf_rn(tk[e], x4.w, acc.w);
+        }
+      }
+      *reinterpret_cast<float4*>(&Tm[mat_idx(16 * bi + r, 16 * bj + 4 * q)]) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
   }
@@ -391,7 +435,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
                                   expf(__fsub_rn(gt, s_gam[ss])))
                       : 0.0f;
         }
-        *reinterpret_cast<float4*>(&Am[t * 64 + 32 * wg + i]) = v;
+        *reinterpret_cast<float4*>(&Am[mat_idx(t, 32 * wg + i)]) = v;
       }
     }
     __syncthreads();
@@ -404,7 +448,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       float w[32];
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(&Tm[t * 64 + 32 * half + i]);
+        const float4 v = *reinterpret_cast<const float4*>(&Tm[mat_idx(t, 32 * half + i)]);
         w[i] = v.x; w[i + 1] = v.y; w[i + 2] = v.z; w[i + 3] = v.w;
       }
       const float* colscale = which ? s_beta : s_cw;
