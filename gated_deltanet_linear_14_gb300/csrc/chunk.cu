@@ -62,10 +62,15 @@ constexpr uint32_t kChunkSmem = OFF_VEC + 8 * 64 * 4 + 2048;  // + 1024-byte ali
 constexpr uint32_t TM_D1 = 0, TM_W = 64, TM_U = 128, TM_WS = 192, TM_S = 256, TM_OQ = 384,
                    TM_OP = 448;
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo_elem, float hi_elem) {
-  const uint32_t a = __bfloat16_as_ushort(__float2bfloat16_rn(lo_elem));
-  const uint32_t b = __bfloat16_as_ushort(__float2bfloat16_rn(hi_elem));
-  return a | (b << 16);
+// A pair of fp32 values as two bf16x2 words (element 0 in the low half):
+// hi = each value rounded to bf16, lo = the remainder rounded to bf16. One
+// paired conversion per word.
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 hb = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(hb);
+  const __nv_bfloat162 lb = __floats2bfloat162_rn(__fsub_rn(x0, hf.x), __fsub_rn(x1, hf.y));
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+  lo = *reinterpret_cast<const uint32_t*>(&lb);
 }
 
 // Write 64 fp32 values as row `row` of two [rows][64] SW128 bf16 tiles: the
@@ -77,11 +82,7 @@ __device__ __forceinline__ void store_row_hilo(uint8_t* hi_tile, uint8_t* lo_til
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float x0 = v[ch * 8 + 2 * e], x1 = v[ch * 8 + 2 * e + 1];
-      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-      h[e] = pack_bf16(h0, h1);
-      l[e] = pack_bf16(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
+      split_pair(v[ch * 8 + 2 * e], v[ch * 8 + 2 * e + 1], h[e], l[e]);
     }
     const uint32_t off = sw128_chunk(row, ch);
     *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -97,11 +98,7 @@ __device__ __forceinline__ void store_half_hilo(uint8_t* hi_tile, uint8_t* lo_ti
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float x0 = v[c * 8 + 2 * e], x1 = v[c * 8 + 2 * e + 1];
-      const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-      const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-      h[e] = pack_bf16(h0, h1);
-      l[e] = pack_bf16(__fsub_rn(x0, h0), __fsub_rn(x1, h1));
+      split_pair(v[c * 8 + 2 * e], v[c * 8 + 2 * e + 1], h[e], l[e]);
     }
     const uint32_t off = sw128_chunk(row, 4 * half + c);
     *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
