@@ -158,7 +158,22 @@ template <class T, int N>
 __device__ __forceinline__ void store_f(T* p, const float* in) {
   constexpr int BYTES = N * (int)sizeof(T);
   static_assert(BYTES % 8 == 0, "vector store of at least 8 bytes");
-  if constexpr (BYTES >= 16) {
+  if constexpr (sizeof(T) == 2) {
+    // bf16: two values per paired round-to-nearest conversion
+    uint32_t w[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const __nv_bfloat162 b = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    if constexpr (BYTES >= 16) {
+#pragma unroll
+      for (int v = 0; v < BYTES / 16; ++v)
+        reinterpret_cast<uint4*>(p)[v] = make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    } else {
+      *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+    }
+  } else if constexpr (BYTES >= 16) {
 #pragma unroll
     for (int v = 0; v < BYTES / 16; ++v) {
       uint4 u;
