@@ -114,11 +114,38 @@ __device__ __forceinline__ int mat_idx(int r, int c) {
   return (r << 6) | ((((c >> 2) ^ (r & 15)) << 2) | (c & 3));
 }
 
-// T = (I + A)^-1 for a strictly lower 64 x 64 A (mat_idx layout), in 16 x 16
-// blocks: diagonal blocks by forward substitution (one thread per block
-// column), then T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj by block distance,
-// each thread forming 4 adjacent outputs from 16-byte loads. Xs: 3 x 256
-// floats of scratch. All threads of the CTA call this.
+// acc += a4[e] * M[k0 + e][c0 .. c0+3] for e = 0..3 (M in the mat_idx layout).
+__device__ __forceinline__ void fma4_row(float4& acc, float4 a4, const float* M, int k0, int c0) {
+  const float ak[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float4 t4 = *reinterpret_cast<const float4*>(&M[mat_idx(k0 + e, c0)]);
+    acc.x = __fmaf_rn(ak[e], t4.x, acc.x);
+    acc.y = __fmaf_rn(ak[e], t4.y, acc.y);
+    acc.z = __fmaf_rn(ak[e], t4.z, acc.z);
+    acc.w = __fmaf_rn(ak[e], t4.w, acc.w);
+  }
+}
+
+// acc += t4[e] * X[m0 + e][c0 .. c0+3] for e = 0..3 (X a [16][16] scratch block).
+__device__ __forceinline__ void fma4_scratch(float4& acc, float4 t4, const float* X, int m0, int c0) {
+  const float tk[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float4 x4 = *reinterpret_cast<const float4*>(&X[(m0 + e) * 16 + c0]);
+    acc.x = __fmaf_rn(tk[e], x4.x, acc.x);
+    acc.y = __fmaf_rn(tk[e], x4.y, acc.y);
+    acc.z = __fmaf_rn(tk[e], x4.z, acc.z);
+    acc.w = __fmaf_rn(tk[e], x4.w, acc.w);
+  }
+}
+
+// T = (I + A)^-1 for a strictly lower 64 x 64 A (mat_idx layout): the four
+// 16 x 16 diagonal blocks by forward substitution (one thread per block
+// column), then the two 32 x 32 diagonal halves, [[T_a, 0], [T_c, T_b]] with
+// T_c = -T_b A_c T_a, then the lower-left 32 x 32 block the same way; each
+// thread forms 4 adjacent outputs from 16-byte loads. Xs: 4 x 256 floats of
+// scratch. All threads of the CTA call this.
 __device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, float* Xs, int tid) {
   if (tid < 64) {
     // the block's row r + 1 is loaded (four 16-byte loads) while row r is
@@ -163,53 +190,79 @@ __device__ __forceinline__ void solve_unit_lower64(const float* Am, float* Tm, f
     }
   }
   __syncthreads();
+  // Round A: the blocks next to the diagonal inside each 32 x 32 half,
+  // T_10 = -T_11 (A_10 T_00) and T_32 = -T_33 (A_32 T_22); thread ->
+  // (half, row r, columns 4q .. 4q+3).
+  if (tid < 128) {
+    const int hf = tid >> 6, bi = 2 * hf + 1, bj = 2 * hf, r = (tid >> 2) & 15, q = tid & 3;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-  for (int d = 1; d < 4; ++d) {
-    const int nb = 4 - d;
-    // X_ij = sum_{k=j}^{i-1} A_ik T_kj: thread -> (block column bj, row r,
-    // columns 4q .. 4q+3)
-    if (tid < nb * 64) {
-      const int bj = tid >> 6, bi = bj + d, r = (tid >> 2) & 15, q = tid & 3;
-      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-      for (int it = 0; it < 4 * d; ++it) {
-        const int kb = 16 * bj + 4 * it;
-        const float4 a4 = *reinterpret_cast<const float4*>(&Am[mat_idx(16 * bi + r, kb)]);
-        const float ak[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 t4 = *reinterpret_cast<const float4*>(&Tm[mat_idx(kb + e, 16 * bj + 4 * q)]);
-          acc.x = __fmaf_rn(ak[e], t4.x, acc.x);
-          acc.y = __fmaf_rn(ak[e], t4.y, acc.y);
-          acc.z = __fmaf_rn(ak[e], t4.z, acc.z);
-          acc.w = __fmaf_rn(ak[e], t4.w, acc.w);
-        }
-      }
-      *reinterpret_cast<float4*>(&Xs[(bj << 8) + r * 16 + 4 * q]) = acc;
+    for (int it = 0; it < 4; ++it) {
+      const int kb = 16 * bj + 4 * it;
+      const float4 a4 = *reinterpret_cast<const float4*>(&Am[mat_idx(16 * bi + r, kb)]);
+      fma4_row(acc, a4, Tm, kb, 16 * bj + 4 * q);
     }
-    __syncthreads();
-    // T_ij = -T_ii X_ij (T_ii is stored with zeros above its diagonal)
-    if (tid < nb * 64) {
-      const int bj = tid >> 6, bi = bj + d, r = (tid >> 2) & 15, q = tid & 3;
-      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-      for (int m0 = 0; m0 < 16; m0 += 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(&Tm[mat_idx(16 * bi + r, 16 * bi + m0)]);
-        const float tk[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 x4 = *reinterpret_cast<const float4*>(&Xs[(bj << 8) + (m0 + e) * 16 + 4 * q]);
-          acc.x = __fmaf_rn(tk[e], x4.x, acc.x);
-          acc.y = __fmaf_rn(tk[e], x4.y, acc.y);
-          acc.z = __fmaf_rn(tk[e], x4.z, acc.z);
-          acc.w = __fmaf_rn(tk[e], x4.w, acc.w);
-        }
-      }
-      *reinterpret_cast<float4*>(&Tm[mat_idx(16 * bi + r, 16 * bj + 4 * q)]) =
-          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
-    __syncthreads();
+    *reinterpret_cast<float4*>(&Xs[(hf << 8) + r * 16 + 4 * q]) = acc;
   }
+  __syncthreads();
+  if (tid < 128) {
+    const int hf = tid >> 6, bi = 2 * hf + 1, bj = 2 * hf, r = (tid >> 2) & 15, q = tid & 3;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int m0 = 0; m0 < 16; m0 += 4) {
+      const float4 t4 = *reinterpret_cast<const float4*>(&Tm[mat_idx(16 * bi + r, 16 * bi + m0)]);
+      fma4_scratch(acc, t4, Xs + (hf << 8), m0, 4 * q);
+    }
+    *reinterpret_cast<float4*>(&Tm[mat_idx(16 * bi + r, 16 * bj + 4 * q)]) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  // Round B: the lower-left 32 x 32 block, T_21 = -T_22 (A_21 T_11) in
+  // 16 x 16 blocks (i, j), i in {2, 3}, j in {0, 1}; thread -> (block,
+  // row r, columns 4q .. 4q+3), one block per pair of warps.
+  {
+    const int blk = tid >> 6, i = 2 + (blk >> 1), j = blk & 1, r = (tid >> 2) & 15, q = tid & 3;
+    // X_ij = sum_{k=16j}^{31} A_ik T_kj (16 or 32 terms), two partial sums
+    float4 acc0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), acc1 = acc0;
+    const int nit = 8 - 4 * j;
+#pragma unroll
+    for (int it = 0; it < 8; it += 2) {
+      if (it < nit) {
+        const int kb0 = 16 * j + 4 * it, kb1 = kb0 + 4;
+        const float4 a0 = *reinterpret_cast<const float4*>(&Am[mat_idx(16 * i + r, kb0)]);
+        const float4 a1 = *reinterpret_cast<const float4*>(&Am[mat_idx(16 * i + r, kb1)]);
+        fma4_row(acc0, a0, Tm, kb0, 16 * j + 4 * q);
+        fma4_row(acc1, a1, Tm, kb1, 16 * j + 4 * q);
+      }
+    }
+    *reinterpret_cast<float4*>(&Xs[(blk << 8) + r * 16 + 4 * q]) =
+        make_float4(__fadd_rn(acc0.x, acc1.x), __fadd_rn(acc0.y, acc1.y),
+                    __fadd_rn(acc0.z, acc1.z), __fadd_rn(acc0.w, acc1.w));
+  }
+  __syncthreads();
+  {
+    // T_ij = -sum_{kb=2}^{i} T_{i,kb} X_{kb,j} (T_22, T_32, T_33; X_{kb,j} is
+    // scratch block ((kb - 2) << 1) | j)
+    const int blk = tid >> 6, i = 2 + (blk >> 1), j = blk & 1, r = (tid >> 2) & 15, q = tid & 3;
+    float4 acc0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), acc1 = acc0;
+#pragma unroll
+    for (int kb = 2; kb < 4; ++kb) {
+      if (kb <= i) {
+        const float* xb = Xs + ((((kb - 2) << 1) | j) << 8);
+#pragma unroll
+        for (int m0 = 0; m0 < 16; m0 += 8) {
+          const float4 t0 = *reinterpret_cast<const float4*>(&Tm[mat_idx(16 * i + r, 16 * kb + m0)]);
+          const float4 t1 = *reinterpret_cast<const float4*>(&Tm[mat_idx(16 * i + r, 16 * kb + m0 + 4)]);
+          fma4_scratch(acc0, t0, xb, m0, 4 * q);
+          fma4_scratch(acc1, t1, xb, m0 + 4, 4 * q);
+        }
+      }
+    }
+    *reinterpret_cast<float4*>(&Tm[mat_idx(16 * i + r, 16 * j + 4 * q)]) =
+        make_float4(-__fadd_rn(acc0.x, acc1.x), -__fadd_rn(acc0.y, acc1.y),
+                    -__fadd_rn(acc0.z, acc1.z), -__fadd_rn(acc0.w, acc1.w));
+  }
+  __syncthreads();
 }
 
 template <class ST>
