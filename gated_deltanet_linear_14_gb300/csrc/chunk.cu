@@ -357,6 +357,49 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   __syncthreads();
   if (tid == 0 && nchunks > 0) issue_tma(0);
 
+  // Gates of chunk cc (threads tid < kCL, one token each): g and beta into
+  // s_g, s_beta; returns this thread's gamma scanned within its warp (the
+  // first warp's total goes to gamma_carry; after a barrier the caller adds
+  // it for the second warp and writes s_gam).
+  auto load_ab = [&](int cc, float& a_v, float& b_v) {
+    const int n = min(kCL, q.len - cc * kCL);
+    const size_t R = (size_t)q.start + (size_t)cc * kCL;
+    a_v = 0.0f;
+    b_v = 0.0f;
+    if (tid < n) {
+      a_v = to_f(a_in[(R + tid) * G.Hv + h]);
+      b_v = to_f(b_in[(R + tid) * G.Hv + h]);
+    }
+  };
+  // the head's gate constants, read once
+  const float gate_eA = (P.gate_mode == 1) ? 0.0f : expf(P.A_log[h]);
+  const float gate_dtb = (P.gate_mode == 1) ? 0.0f : P.dt_bias[h];
+  auto gates_scan = [&](int cc, float a_v, float b_v) -> float {
+    float g = 0.0f, beta = 0.0f;
+    if (tid < min(kCL, q.len - cc * kCL))
+      gate_log_c(P.gate_mode, gate_eA, gate_dtb, a_v, b_v, g, beta);
+    s_g[tid] = g;
+    s_beta[tid] = beta;
+    const int lane = tid & 31;
+#pragma unroll
+    for (int dd = 1; dd < 32; dd <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, g, dd);
+      if (lane >= dd) g = __fadd_rn(g, y);
+    }
+    if (tid == 31) gamma_carry = g;
+    return g;
+  };
+  if (nchunks > 0) {
+    float g0 = 0.0f;
+    if (tid < kCL) {
+      float a0, b0;
+      load_ab(0, a0, b0);
+      g0 = gates_scan(0, a0, b0);
+    }
+    __syncthreads();
+    if (tid < kCL) s_gam[tid] = (tid >= 32) ? __fadd_rn(g0, gamma_carry) : g0;
+  }
+
   uint32_t mma_count = 0;
   bool fail = false;
   auto wait_mma = [&]() -> bool {
@@ -370,11 +413,9 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   for (int c = 0; c < nchunks; ++c) {
     const int n_c = min(kCL, q.len - c * kCL);
     const size_t R0 = (size_t)q.start + (size_t)c * kCL;
-    float a_t = 0.0f, b_t = 0.0f;
-    if (tid < n_c) {
-      a_t = to_f(a_in[(R0 + tid) * G.Hv + h]);
-      b_t = to_f(b_in[(R0 + tid) * G.Hv + h]);
-    }
+    // the next chunk's raw gates, used while this chunk's MMA4/5 run
+    float a_n = 0.0f, b_n = 0.0f;
+    if (c + 1 < nchunks && tid < kCL) load_ab(c + 1, a_n, b_n);
     {
       const bool ok = mbar_wait(bar_tma, c & 1);
       if (__syncthreads_or(!ok)) { fail = true; break; }
@@ -403,13 +444,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       }
       mma_commit(bar_mma);
     }
-    // gates and q norms while it runs
-    float g_mine = 0.0f;
+    // q norms while it runs (this chunk's gates are in place already)
     if (tid < kCL) {
-      float beta = 0.0f;
-      if (tid < n_c) gate_log(P, h, a_t, b_t, g_mine, beta);
-      s_g[tid] = g_mine;
-      s_beta[tid] = beta;
       float qq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int a = 0; a < 2; ++a)
@@ -425,18 +461,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
           }
         }
       s_iq[tid] = rsqrtf(__fadd_rn(__fadd_rn(__fadd_rn(qq[0], qq[1]), __fadd_rn(qq[2], qq[3])), P.eps));
-      // gamma: inclusive prefix sum of g over the chunk (warp scans, then
-      // the second warp adds the first warp's total)
-      const int lane = tid & 31;
-#pragma unroll
-      for (int dd = 1; dd < 32; dd <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, g_mine, dd);
-        if (lane >= dd) g_mine = __fadd_rn(g_mine, y);
-      }
-      if (tid == 31) gamma_carry = g_mine;
     }
-    __syncthreads();
-    if (tid < kCL) s_gam[tid] = (tid >= 32) ? __fadd_rn(g_mine, gamma_carry) : g_mine;
     if (!wait_mma()) { fail = true; break; }
 
     float d1[32];   // columns [32 wg, 32 wg + 32) of this thread's row of [QK^T; KK^T]
@@ -579,7 +604,13 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
                    (pass | ks) != 0);
       mma_commit(bar_mma);
     }
+    // the next chunk's gates while they run: past this point the chunk reads
+    // none of s_g, s_beta, s_gam (its later phases use s_cv and s_co)
+    float g_nx = 0.0f;
+    if (c + 1 < nchunks && tid < kCL) g_nx = gates_scan(c + 1, a_n, b_n);
     if (!wait_mma()) { fail = true; break; }
+    if (c + 1 < nchunks && tid < kCL)
+      s_gam[tid] = (tid >= 32) ? __fadd_rn(g_nx, gamma_carry) : g_nx;
 
     // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
     {
