@@ -302,9 +302,9 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
 
 /* Default row count from which gdn_prefill uses the chunked form. Measured on
  * GB300 (16/32 heads, Dk = Dv = 128): with 8 requests per step the chunked
- * form is faster from 48 rows (1.7x at 128, 1.8x at 1024); with a single
- * request it is within 8 % of token by token at 128 rows and even at 1024. */
-#define GDN_PREFILL_CHUNK_MIN_ROWS 128
+ * form is faster from 32 rows (2.0x at 64, 2.7x at 1024); with a single
+ * request from 64 rows (1.4x at 128, 1.6x at 1024). */
+#define GDN_PREFILL_CHUNK_MIN_ROWS 64
 
 /* Prefill dispatch: the plain requests of the batch with at least
  * chunk_min_rows rows (<= 0 selects GDN_PREFILL_CHUNK_MIN_ROWS) go through
