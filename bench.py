@@ -73,6 +73,12 @@ def barrier(world: int):
 
 # ------------------------------------------------------------ measurement
 
+# FP32 FMA peak from the unit counts: 152 SMs x 128 FP32 lanes x 2 flops per
+# fused multiply-add x 2.07 GHz maximum SM clock (the packed f32x2 forms halve
+# issue slots, not the lane count).
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -495,7 +501,9 @@ def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
             "ms_per_step": el / K * 1e3, "verify_ms": ver_ms, "conv_ms": conv_ms,
             "tokens_per_s": T * K / el, "verify_gbs": gbs,
             "verify_frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
-            "verify_tflops_fp32": flops / (ver_ms / 1e3) / 1e12, "status": code}
+            "verify_tflops_fp32": flops / (ver_ms / 1e3) / 1e12,
+            "verify_frac_of_fp32": flops / (ver_ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS,
+            "fp32_peak_tflops": FP32_PEAK_TFLOPS, "status": code}
 
 
 def bench_slots(device, peaks, K=20, W=4, pools=2):
