@@ -45,7 +45,8 @@ using namespace umma;
 
 constexpr int kCL = 64;               // tokens per chunk
 constexpr int kCD = 128;              // Dk = Dv
-constexpr int kChunkThreads = 256;      // two warpgroups; warps w and w+4 share TMEM lanes
+constexpr int kChunkThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;      // two warpgroups; warps w and w+4 share TMEM lanes
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_QK = 0;        // per 64-column atom a (a*16384): Q rows 0..63, K rows 64..127
@@ -298,8 +299,8 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * kCD * kCD;
   const int kh = (int)(((long long)h * G.Hk) / G.Hv);
 
-  float* s_g = reinterpret_cast<float*>(sm + OFF_VEC);
-  float* s_beta = s_g + 64;
+  float* s_l2 = reinterpret_cast<float*>(sm + OFF_VEC);   // gamma log2(e)
+  float* s_beta = s_l2 + 64;
   float* s_gam = s_beta + 64;
   float* s_iq = s_gam + 64;
   float* s_ik = s_iq + 64;
@@ -357,10 +358,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
   __syncthreads();
   if (tid == 0 && nchunks > 0) issue_tma(0);
 
-  // Gates of chunk cc (threads tid < kCL, one token each): g and beta into
-  // s_g, s_beta; returns this thread's gamma scanned within its warp (the
-  // first warp's total goes to gamma_carry; after a barrier the caller adds
-  // it for the second warp and writes s_gam).
+  // Gates of chunk cc (threads tid < kCL, one token each): beta into s_beta;
+  // returns this thread's gamma scanned within its warp (the first warp's
+  // total goes to gamma_carry; after a barrier the caller adds it for the
+  // second warp and writes s_gam and s_l2 = gamma log2 e).
   auto load_ab = [&](int cc, float& a_v, float& b_v) {
     const int n = min(kCL, q.len - cc * kCL);
     const size_t R = (size_t)q.start + (size_t)cc * kCL;
@@ -378,7 +379,6 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     float g = 0.0f, beta = 0.0f;
     if (tid < min(kCL, q.len - cc * kCL))
       gate_log_c(P.gate_mode, gate_eA, gate_dtb, a_v, b_v, g, beta);
-    s_g[tid] = g;
     s_beta[tid] = beta;
     const int lane = tid & 31;
 #pragma unroll
@@ -397,7 +397,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       g0 = gates_scan(0, a0, b0);
     }
     __syncthreads();
-    if (tid < kCL) s_gam[tid] = (tid >= 32) ? __fadd_rn(g0, gamma_carry) : g0;
+    if (tid < kCL) {
+      s_gam[tid] = (tid >= 32) ? __fadd_rn(g0, gamma_carry) : g0;
+      s_l2[tid] = __fmul_rn(s_gam[tid], kLog2e);
+    }
   }
 
   uint32_t mma_count = 0;
@@ -485,19 +488,19 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     if (row < kCL) {
       // P row t, columns of this half: masked, gated, normalised q_t . k_s (s <= t < n_c)
       const int t = row;
-      const float iq = s_iq[t], gt = s_gam[t];
+      const float iq = s_iq[t], lt = s_l2[t];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int s = 32 * wg + i;
         d1[i] = (s <= t && t < n_c)
-                    ? __fmul_rn(__fmul_rn(__fmul_rn(d1[i], iq), s_ik[s]), expf(__fsub_rn(gt, s_gam[s])))
+                    ? __fmul_rn(__fmul_rn(__fmul_rn(d1[i], iq), s_ik[s]), exp2f(__fsub_rn(lt, s_l2[s])))
                     : 0.0f;
       }
       store_half_hilo(sm + OFF_P, sm + OFF_P + 8192, t, wg, d1);
     } else {
       // A row t: beta_t e^{gamma_t - gamma_s} k^_t . k^_s for s < t
       const int t = row - kCL;
-      const float ikt = s_ik[t], gt = s_gam[t], bt = s_beta[t];
+      const float ikt = s_ik[t], lt = s_l2[t], bt = s_beta[t];
 #pragma unroll
       for (int i = 0; i < 32; i += 4) {
         float4 v;
@@ -507,7 +510,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
           const int ss = 32 * wg + i + e;
           vp[e] = (ss < t && t < n_c)
                       ? __fmul_rn(__fmul_rn(__fmul_rn(__fmul_rn(d1[i + e], ikt), s_ik[ss]), bt),
-                                  expf(__fsub_rn(gt, s_gam[ss])))
+                                  exp2f(__fsub_rn(lt, s_l2[ss])))
                       : 0.0f;
         }
         *reinterpret_cast<float4*>(&Am[mat_idx(t, 32 * wg + i)]) = v;
@@ -605,12 +608,14 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
       mma_commit(bar_mma);
     }
     // the next chunk's gates while they run: past this point the chunk reads
-    // none of s_g, s_beta, s_gam (its later phases use s_cv and s_co)
+    // none of s_beta, s_gam, s_l2 (its later phases use s_cv and s_co)
     float g_nx = 0.0f;
     if (c + 1 < nchunks && tid < kCL) g_nx = gates_scan(c + 1, a_n, b_n);
     if (!wait_mma()) { fail = true; break; }
-    if (c + 1 < nchunks && tid < kCL)
+    if (c + 1 < nchunks && tid < kCL) {
       s_gam[tid] = (tid >= 32) ? __fadd_rn(g_nx, gamma_carry) : g_nx;
+      s_l2[tid] = __fmul_rn(s_gam[tid], kLog2e);
+    }
 
     // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
     {
@@ -674,10 +679,11 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     }
     __syncthreads();
     {
-      const int per_row = out_f32 ? kCD / 4 : kCD / 8;   // 16-byte pieces per row
+      const int lg = out_f32 ? 5 : 4;                    // log2 of 16-byte pieces per row
+      const int per_row = 1 << lg;
       const uint4* src = reinterpret_cast<const uint4*>(sm + OFF_R1);
-      for (int idx = tid; idx < n_c * per_row; idx += kChunkThreads) {
-        const int t = idx / per_row, piece = idx % per_row;
+      for (int idx = tid; idx < (n_c << lg); idx += kChunkThreads) {
+        const int t = idx >> lg, piece = idx & (per_row - 1);
         const size_t row_off = ((R0 + t) * G.Hv + h) * G.Dv;
         uint4* dst = out_f32 ? reinterpret_cast<uint4*>(reinterpret_cast<float*>(o) + row_off)
                              : reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(o) + row_off);
