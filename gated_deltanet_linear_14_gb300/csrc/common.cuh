@@ -249,6 +249,45 @@ __device__ __forceinline__ float own_silu(float z) {
   return __fdiv_rn(z, __fadd_rn(1.0f, e));
 }
 
+// own_exp on two values at once: the same operations, each rounded the same
+// way, with the floating-point steps in packed f32x2 form. The integer
+// exponent comes from t clamped to [-130, 130] (equal to t wherever the
+// result is used; it keeps the integer steps defined for the values the
+// final range selection replaces), the reduction from x itself, so a NaN
+// stays NaN as in own_exp.
+__device__ __forceinline__ float2 own_exp2(float2 x) {
+  constexpr double kLn2 = 0.693147180559945309417232121458176568;
+  const float log2e = (float)(1.0 / kLn2);
+  const float ln2_hi = __uint_as_float(0x3F317000u);
+  const float ln2_lo = (float)(kLn2 - (double)0.693115234375);
+  const float2 t = __fmul2_rn(x, make_float2(log2e, log2e));
+  const float2 n = make_float2(rintf(fminf(fmaxf(t.x, -130.0f), 130.0f)),
+                               rintf(fminf(fmaxf(t.y, -130.0f), 130.0f)));
+  const float2 mn = make_float2(-n.x, -n.y);
+  float2 r = __ffma2_rn(mn, make_float2(ln2_hi, ln2_hi), x);
+  r = __ffma2_rn(mn, make_float2(ln2_lo, ln2_lo), r);
+  float2 p = make_float2(recip_factorial(7), recip_factorial(7));
+#pragma unroll
+  for (int k = 6; k >= 0; --k)
+    p = __ffma2_rn(p, r, make_float2(recip_factorial(k), recip_factorial(k)));
+  const int nx = (int)n.x, ny = (int)n.y;
+  const int hx = nx / 2, hy = ny / 2;
+  const float2 s1 = make_float2(__int_as_float((hx + 127) << 23), __int_as_float((hy + 127) << 23));
+  const float2 s2 = make_float2(__int_as_float((nx - hx + 127) << 23),
+                                __int_as_float((ny - hy + 127) << 23));
+  float2 e = __fmul2_rn(__fmul2_rn(p, s1), s2);
+  const float inf = __int_as_float(0x7f800000);
+  e.x = (x.x >= 88.72283935546875f) ? inf : ((x.x <= -87.0f) ? 0.0f : e.x);
+  e.y = (x.y >= 88.72283935546875f) ? inf : ((x.y <= -87.0f) ? 0.0f : e.y);
+  return e;
+}
+
+// own_silu on two values at once (bit-identical to own_silu on each).
+__device__ __forceinline__ float2 own_silu2(float2 z) {
+  const float2 e = own_exp2(make_float2(-z.x, -z.y));
+  return make_float2(__fdiv_rn(z.x, __fadd_rn(1.0f, e.x)), __fdiv_rn(z.y, __fadd_rn(1.0f, e.y)));
+}
+
 // ----------------------------------------------------------------- gates
 
 // g (log decay) and beta from the raw inputs, fp32, CUDA math library.

@@ -145,14 +145,19 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
 #pragma unroll
         for (int v = 0; v < V; ++v) xv[v] = to_f(e[v]);
       }
+      // channel pairs in packed f32x2 form: each channel sees the same
+      // fused multiply-adds, in the same order, as a scalar loop would
       float yv[V];
 #pragma unroll
-      for (int v = 0; v < V; ++v) {
-        float acc = bias[v];
+      for (int v = 0; v < V; v += 2) {
+        float2 acc = make_float2(bias[v], bias[v + 1]);
 #pragma unroll
-        for (int j = 0; j < H; ++j) acc = __fmaf_rn(wt[j][v], h[j][v], acc);
-        acc = __fmaf_rn(wt[H][v], xv[v], acc);
-        yv[v] = own_silu(acc);
+        for (int j = 0; j < H; ++j)
+          acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]), make_float2(h[j][v], h[j][v + 1]), acc);
+        acc = __ffma2_rn(make_float2(wt[H][v], wt[H][v + 1]), make_float2(xv[v], xv[v + 1]), acc);
+        const float2 y2 = own_silu2(acc);
+        yv[v] = y2.x;
+        yv[v + 1] = y2.y;
       }
       store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
 #pragma unroll
