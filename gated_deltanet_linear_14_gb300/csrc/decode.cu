@@ -143,12 +143,17 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
     if (q.len == 1) load_f<IO, 4>(x + (size_t)q.start * G.C + c, xv);
     float yv[4];
 #pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      float acc = P.conv_bias ? P.conv_bias[c + v] : 0.0f;
+    for (int v = 0; v < 4; v += 2) {   // channel pairs, as the conv kernel
+      float2 acc = P.conv_bias ? make_float2(P.conv_bias[c + v], P.conv_bias[c + v + 1])
+                               : make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int j = 0; j < 3; ++j) acc = __fmaf_rn(wt[j][v], hcol[j][v], acc);
-      acc = __fmaf_rn(wt[3][v], xv[v], acc);
-      yv[v] = own_silu(acc);
+      for (int j = 0; j < 3; ++j)
+        acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]),
+                         make_float2(hcol[j][v], hcol[j][v + 1]), acc);
+      acc = __ffma2_rn(make_float2(wt[3][v], wt[3][v + 1]), make_float2(xv[v], xv[v + 1]), acc);
+      const float2 y2 = own_silu2(acc);
+      yv[v] = y2.x;
+      yv[v + 1] = y2.y;
     }
     store_f<IO, 4>(mrow + c4, yv);
     // new window: the last three columns of [history; this row]
