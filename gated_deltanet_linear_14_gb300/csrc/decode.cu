@@ -195,7 +195,7 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
       RawVec<IO, PE> rq, rk;
       rq.load(mrow + PE * p);
       rk.load(mrow + DK + PE * p);
-      const float kq = publish_qk<DK, IO>(&st.q[PE * p], &st.k[PE * p], rq, rk, P);
+      const float kq = publish_qk<DK, IO, ST>(st.q, st.k, PE * p, rq, rk, P);
       if (p == 0) st.kq = kq;
     }
     float alpha = 0.0f, beta = 0.0f;

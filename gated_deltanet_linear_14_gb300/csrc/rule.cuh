@@ -52,6 +52,21 @@ struct LaneMap {
   __device__ static int idx(int r8, int i) { return VEC * (8 * i + r8); }
 };
 
+// Where Dk entry d of a staged q^ or k^ row sits in shared memory. When a
+// lane's state entries come in runs of 8 (bf16 state: VEC = 8), the row is
+// permuted by 16-byte pieces so that the first halves of the 8 lanes' runs
+// are contiguous, then the second halves: each 16-byte load of a warp then
+// reads one 128-byte line instead of two. With VEC = 4 rows are in order.
+template <int DK, class ST>
+__device__ __forceinline__ int stage_pos(int d) {
+  if constexpr (LaneMap<DK, ST>::VEC == 8) {
+    const int m = d >> 2;  // 16-byte piece: m = 2 (8 i + r8) + half
+    return ((((m >> 4) << 4) | ((m & 1) << 3) | ((m >> 1) & 7)) << 2) | (d & 3);
+  } else {
+    return d;
+  }
+}
+
 template <int DK>
 struct Stage {
   float q[kTC][DK];       // q^ (fp32, normalised)
@@ -124,12 +139,13 @@ __device__ __forceinline__ void fetch(Fetch<DK, IO>& f, const RowSrc<IO>& src, i
 
 // q^ and k^ of one token from its raw parts, 8 threads per token (thread p
 // holds entries [PE p, PE p + PE)): 8-lane butterfly sums of q.q, k.k and
-// q.k, then 1/sqrt(x.x + eps). Writes this thread's parts of q^, k^ and
-// returns q^.k^ (the same value in all 8 threads). Every kernel that stages
+// q.k, then 1/sqrt(x.x + eps). Writes this thread's parts of q^, k^ (entries
+// d0 .. d0 + PE - 1 of the staged rows, at stage_pos) and returns q^.k^ (the same value in all 8 threads). Every kernel that stages
 // rows for the token step normalises through here, so they all see
 // bit-identical q^, k^.
-template <int DK, class IO>
-__device__ __forceinline__ float publish_qk(float* qdst, float* kdst, const RawVec<IO, DK / 8>& rq,
+template <int DK, class IO, class ST>
+__device__ __forceinline__ float publish_qk(float* qrow, float* krow, int d0,
+                                            const RawVec<IO, DK / 8>& rq,
                                             const RawVec<IO, DK / 8>& rk, const Params& P) {
   constexpr int PE = DK / 8;
   float fq[PE], fk[PE];
@@ -156,10 +172,10 @@ __device__ __forceinline__ float publish_qk(float* qdst, float* kdst, const RawV
   const float ik = rsqrtf(__fadd_rn(kk, P.eps));
 #pragma unroll
   for (int e = 0; e < PE; e += 4) {
-    *reinterpret_cast<float4*>(&qdst[e]) =
+    *reinterpret_cast<float4*>(&qrow[stage_pos<DK, ST>(d0 + e)]) =
         make_float4(__fmul_rn(fq[e], iq), __fmul_rn(fq[e + 1], iq), __fmul_rn(fq[e + 2], iq),
                     __fmul_rn(fq[e + 3], iq));
-    *reinterpret_cast<float4*>(&kdst[e]) =
+    *reinterpret_cast<float4*>(&krow[stage_pos<DK, ST>(d0 + e)]) =
         make_float4(__fmul_rn(fk[e], ik), __fmul_rn(fk[e + 1], ik), __fmul_rn(fk[e + 2], ik),
                     __fmul_rn(fk[e + 3], ik));
   }
@@ -167,12 +183,12 @@ __device__ __forceinline__ float publish_qk(float* qdst, float* kdst, const RawV
 }
 
 // Normalise and publish one fetched token (8 threads per token).
-template <int DK, class IO>
+template <int DK, class IO, class ST>
 __device__ __forceinline__ void publish(Stage<DK>& st, const Fetch<DK, IO>& f, int t, int n_t,
                                         int p, int h, const Params& P) {
   constexpr int PE = DK / 8;
   if (t >= n_t) return;  // whole 8-lane groups take this branch together
-  const float kq = publish_qk<DK, IO>(&st.q[t][PE * p], &st.k[t][PE * p], f.q, f.k, P);
+  const float kq = publish_qk<DK, IO, ST>(st.q[t], st.k[t], PE * p, f.q, f.k, P);
   *reinterpret_cast<float4*>(&st.v[t][4 * p]) =
       make_float4(f.v.get(0), f.v.get(1), f.v.get(2), f.v.get(3));
   if (p == 0) {
@@ -207,8 +223,8 @@ __device__ __forceinline__ float token_step_rows(LaneState<DK / 8>& S, const flo
   for (int i = 0; i < L::NI; ++i) {
 #pragma unroll
     for (int e = 0; e < L::VEC; e += 4) {
-      const float4 qv = *reinterpret_cast<const float4*>(&qrow[L::idx(r8, i) + e]);
-      const float4 kv = *reinterpret_cast<const float4*>(&krow[L::idx(r8, i) + e]);
+      const float4 qv = *reinterpret_cast<const float4*>(&qrow[stage_pos<DK, ST>(L::idx(r8, i) + e)]);
+      const float4 kv = *reinterpret_cast<const float4*>(&krow[stage_pos<DK, ST>(L::idx(r8, i) + e)]);
       q2[(i * L::VEC + e) / 2] = make_float2(qv.x, qv.y);
       q2[(i * L::VEC + e) / 2 + 1] = make_float2(qv.z, qv.w);
       k2[(i * L::VEC + e) / 2] = make_float2(kv.x, kv.y);
@@ -275,7 +291,7 @@ __device__ __forceinline__ void token_update_rows(LaneState<DK / 8>& S, const fl
   for (int i = 0; i < L::NI; ++i) {
 #pragma unroll
     for (int e = 0; e < L::VEC; e += 4) {
-      const float4 kv = *reinterpret_cast<const float4*>(&krow[L::idx(r8, i) + e]);
+      const float4 kv = *reinterpret_cast<const float4*>(&krow[stage_pos<DK, ST>(L::idx(r8, i) + e)]);
       k2[(i * L::VEC + e) / 2] = make_float2(kv.x, kv.y);
       k2[(i * L::VEC + e) / 2 + 1] = make_float2(kv.z, kv.w);
     }
@@ -367,7 +383,7 @@ __device__ __forceinline__ void run_rows(LaneState<DK / 8>& S, Stage<DK>& st, co
   for (int c0 = 0; c0 < n; c0 += kTC) {
     const int n_t = min(kTC, n - c0);
     __syncthreads();                                    // previous chunk fully read
-    publish<DK, IO>(st, f, ft, n_t, fp, h, P);
+    publish<DK, IO, ST>(st, f, ft, n_t, fp, h, P);
     __syncthreads();
     if (c0 + kTC < n) {                                 // prefetch the next chunk
       RowSrc<IO> nx = src;
@@ -485,7 +501,7 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
         tt = ft - n_rep;
       }
       fetch<DK, IO>(f, src, tt, ft < n_all ? tt + 1 : 0, fp, kh, h, cb, G);
-      publish<DK, IO>(st, f, ft, n_all, fp, h, P);
+      publish<DK, IO, ST>(st, f, ft, n_all, fp, h, P);
     }
     __syncthreads();
     const int vcol = warp * 8 + cg * 2;
