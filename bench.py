@@ -611,17 +611,40 @@ def bench_mixed(device, peaks, K=20, W=4):
         if ev is not None:
             ev[3].record()
 
+    # The same step with the verify on a second stream: after the conv, the
+    # prefill and the verify touch disjoint pages and output rows, so the
+    # verify's blocks can fill the SMs the chunked prefill leaves idle.
+    main = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device=device)
+    conv_done = torch.cuda.Event()
+    ver_done = torch.cuda.Event()
+
+    def launch_two_streams(i):
+        B = batches[i % 2]
+        gdn.gdn_conv(dims, B, params, x, conv_w, y, gdn.GDN_BF16, pool.buf, status, stream=main)
+        conv_done.record(main)
+        side.wait_event(conv_done)
+        gdn.gdn_spec_verify(dims, B, params, y, a, b, o, pool.buf, status, stream=side)
+        ver_done.record(side)
+        gdn.gdn_prefill(dims, B, params, y, a, b, o, pool.buf, status, stream=main)
+        main.wait_event(ver_done)
+
     for i in range(W):
         launch(i)
     torch.cuda.synchronize()
     evs = [_events(torch, 4) for _ in range(K)]
     el = time_steps(lambda i: launch(W + i, evs[i]), K, torch)
+    for i in range(W):
+        launch_two_streams(W + K + i)
+    torch.cuda.synchronize()
+    el2 = time_steps(lambda i: launch_two_streams(2 * W + K + i), K, torch)
     return {"workload": f"mixed: 8 prefills of {int(lengths[ns:].min())}..{int(lengths[ns:].max())} "
                         f"tokens + {ns} spec requests x {n} rows, {T} rows, row map longest first",
             "ms_per_step": el / K * 1e3, "tokens_per_s": T * K / el,
             "conv_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
             "prefill_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
             "verify_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+            "ms_per_step_two_streams": el2 / K * 1e3, "tokens_per_s_two_streams": T * K / el2,
             "longest_chain": int(lengths.max()), "status": int(status.item())}
 
 
