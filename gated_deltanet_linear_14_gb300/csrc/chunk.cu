@@ -11,11 +11,12 @@
 //   O  = scale (diag(e^gamma) Q^ S + (Q^ K^T o e^{gamma_t-gamma_s} o causal) Vn)
 //   S <- e^{gamma_L} S + (diag(e^{gamma_L-gamma}) K^)^T Vn
 //
-// Design. One CTA (4 warps) per (request, value head) walks the request's
+// Design. One CTA (8 warps) per (request, value head) walks the request's
 // chunks. Every contraction is an M = 128 tcgen05.mma with bf16 operands in
 // 128B-swizzled shared memory and fp32 accumulators in tensor memory; the
-// 128 rows are Dk or Dv (or the 64 q rows stacked on the 64 k rows), so each
-// thread owns one TMEM lane (one row) in every epilogue:
+// 128 rows are Dk or Dv (or the 64 q rows stacked on the 64 k rows), so in
+// every epilogue a thread owns one TMEM lane (one row) and its warpgroup
+// half of the columns:
 //   MMA1  [Q;K] K^T          -> QK^T and KK^T (raw bf16: exact products);
 //                               |k_t|^2 is the diagonal of KK^T
 //   MMA2  K^T T_W^T          -> W^T   (T_W = T diag(beta e^gamma / |k|))
@@ -29,10 +30,11 @@
 // V') is split into bf16 hi + lo and the products summed (dropping lo x lo),
 // which keeps about 2^-16 relative accuracy: fp32-grade results from the
 // bf16 tensor pipe. The 64 x 64 unit-lower-triangular inverse T is computed
-// on the CUDA cores in 16 x 16 blocks. The state stays fp32 in TMEM for the
-// whole request. Tiles arrive by TMA (SWIZZLE_128B) straight into the
-// operand layout; the next chunk's tiles are fetched while the current
-// chunk's outputs are written.
+// on the CUDA cores (16 x 16 diagonal blocks, then two 32 x 32 rounds). The
+// state stays fp32 in TMEM for the whole request. Tiles arrive by TMA
+// (SWIZZLE_128B) straight into the operand layout; the next chunk's tiles
+// are fetched while the current chunk's outputs are written, and its gates
+// are formed while this chunk's MMA4/5 run.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -45,8 +47,8 @@ using namespace umma;
 
 constexpr int kCL = 64;               // tokens per chunk
 constexpr int kCD = 128;              // Dk = Dv
-constexpr int kChunkThreads = 256;
-constexpr float kLog2e = 1.4426950408889634f;      // two warpgroups; warps w and w+4 share TMEM lanes
+constexpr int kChunkThreads = 256;      // two warpgroups; warps w and w+4 share TMEM lanes
+constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared memory map (bytes from a 1024-aligned base).
 constexpr uint32_t OFF_QK = 0;        // per 64-column atom a (a*16384): Q rows 0..63, K rows 64..127
