@@ -108,6 +108,41 @@ def test_chunk_gate_mode_precomputed():
     assert rel(f64(L.pool.state_math(0)), S_ref[0]) <= TOL
 
 
+@pytest.mark.parametrize("path", ["chunk", "seq"])
+@pytest.mark.parametrize("case", ["strong_decay", "no_decay", "beta_edges"])
+def test_gate_extremes_vs_oracle(case, path):
+    """Precomputed gates at their extremes on a ragged 150-token sequence,
+    chunked and token by token: g down to -40 per token (in-chunk decays far
+    below fp32's range), g = 0 (nothing decays), and beta exactly 0 or 1."""
+    sh = synth.Shapes(Hk=1, Hv=2, Dk=128, Dv=128)
+    rng = np.random.default_rng({"strong_decay": 11, "no_decay": 12, "beta_edges": 13}[case])
+    T = 150
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    if case == "strong_decay":
+        g = rng.uniform(-40.0, -8.0, (T, sh.Hv))
+        beta = rng.uniform(0.0, 1.0, (T, sh.Hv))
+    elif case == "no_decay":
+        g = np.zeros((T, sh.Hv))
+        beta = rng.uniform(0.0, 1.0, (T, sh.Hv))
+    else:
+        g = rng.uniform(-1.0, 0.0, (T, sh.Hv))
+        beta = rng.integers(0, 2, (T, sh.Hv)).astype(np.float64)
+    rows["a"] = synth.as_io(g, synth.BF16)
+    rows["b"] = synth.as_io(beta, synth.BF16)
+    L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], gate_mode=1)
+    B = L.batch([0], [T], flags=gdn.GDN_REQ_FRESH)
+    x, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    o = chunk_run(L, B, x, a, b) if path == "chunk" else L.seq(B, x, a, b)
+    L.ok()
+    assert bool(torch.isfinite(o.float()).all())
+    o_ref, S_ref = oracle.gdn_f64(rows["x"].value, rows["a"].value, rows["b"].value, d["A_log"],
+                                  d["dt_bias"], [0], [T], 1, 2, 128, 128, gate_mode=1)
+    assert rel(f64(o), o_ref) <= TOL
+    assert rel(f64(L.pool.state_math(0)), S_ref[0]) <= TOL
+
+
 def _head_pair(d, rows, r, kh, start, ln):
     """The oracle's inputs for value heads 2kh, 2kh+1 (q/k head kh) of request r."""
     sh = d["shapes"]
