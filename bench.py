@@ -346,7 +346,11 @@ def run_ours(args, world, rank, local):
                      "frac": achieved / hbm_peak, "traffic": traffic_from_profile("decode_fused"),
                      "kernel": "decode_kernel (gdn_decode: conv + rule, one launch)",
                      "algorithmic_bytes_per_launch": dec_bytes,
-                     "launch_ms": dec_s * 1e3, "peak_source": f"{peak_src} hbm_gbs (burst)"},
+                     "launch_ms": dec_s * 1e3, "peak_source": f"{peak_src} hbm_gbs (burst)",
+                     # the same bytes over the mean step of the timed region (one
+                     # launch per step; back-to-back launches overlap their starts)
+                     "achieved_per_step": dec_bytes / (elapsed_max / K) / 1e9,
+                     "frac_per_step": dec_bytes / (elapsed_max / K) / 1e9 / hbm_peak},
         "kernels_ms": {"gdn_decode": statistics.mean(dec_ms)},
         "two_launch_step": {"ms_per_step": el2 / K2 * 1e3, "gdn_conv_ms": statistics.mean(conv_ms),
                             "gdn_seq_ms": statistics.mean(rule_ms),

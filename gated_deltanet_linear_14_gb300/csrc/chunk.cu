@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kChunkThreads, 1)
 chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params P,
              const bf16* __restrict__ a_in, const bf16* __restrict__ b_in, void* o, int out_f32,
              void* pages, int32_t* status) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ __align__(8) uint64_t bars[2];
@@ -721,15 +722,17 @@ cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const 
   if (state_bf16) {
     cudaError_t e = ensure_smem_limit<chunk_kernel<bf16>>((int)kChunkSmem);
     if (e != cudaSuccess) return e;
-    chunk_kernel<bf16><<<grid, kChunkThreads, kChunkSmem, stream>>>(
-        tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
-        status);
+    e = launch_pdl(chunk_kernel<bf16>, grid, dim3(kChunkThreads), kChunkSmem, stream, tm, G, B, P,
+                   static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
+                   status);
+    if (e != cudaSuccess) return e;
   } else {
     cudaError_t e = ensure_smem_limit<chunk_kernel<float>>((int)kChunkSmem);
     if (e != cudaSuccess) return e;
-    chunk_kernel<float><<<grid, kChunkThreads, kChunkSmem, stream>>>(
-        tm, G, B, P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
-        status);
+    e = launch_pdl(chunk_kernel<float>, grid, dim3(kChunkThreads), kChunkSmem, stream, tm, G, B,
+                   P, static_cast<const bf16*>(a), static_cast<const bf16*>(b), o, out_f32, pages,
+                   status);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

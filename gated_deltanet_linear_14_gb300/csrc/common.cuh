@@ -335,6 +335,35 @@ __device__ __forceinline__ void gate_log_c(int gate_mode, float eA, float dtb, f
   beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
 }
 
+// ------------------------------------------------- programmatic launches
+//
+// Every kernel of the library starts with pdl_begin(): it waits until the
+// previous grid on the stream has completed and its writes are visible (so
+// stream order is kept exactly: nothing is read or written before), then lets
+// the next grid be scheduled. Launched with launch_pdl, a kernel's blocks can
+// be resident while the previous grid finishes, which hides the launch
+// latency between back-to-back kernels.
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <class... KArgs, class... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Raise a kernel's dynamic shared memory limit once per device (host side;
 // later launches, including ones being captured into a graph, skip the call).
 // One instantiation, and so one record of devices done, per kernel.

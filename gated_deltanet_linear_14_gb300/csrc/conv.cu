@@ -39,6 +39,7 @@ template <class IO, class YT, int W, bool SLOTS>
 __global__ void __launch_bounds__(kConvThreads, 8)
 conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
             const IO* __restrict__ w, YT* __restrict__ y, void* pages, int32_t* status) {
+  pdl_begin();
   constexpr int V = kConvVecBytes / (int)sizeof(IO);  // channels per thread
   constexpr int H = W - 1;
   const bool reporter = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
@@ -224,11 +225,9 @@ static cudaError_t launch_conv_t(const Geom& G, const Batch& B, const Params& P,
   constexpr int V = kConvVecBytes / (int)sizeof(IO);
   const int ctiles = (G.C + kConvThreads * V - 1) / (kConvThreads * V);
   const int rtiles = B.max_rows > 0 ? (B.max_rows + kConvRows - 1) / kConvRows : 1;
-  dim3 grid(ctiles, rtiles, B.R);
-  conv_kernel<IO, YT, 4, SLOTS><<<grid, kConvThreads, 0, stream>>>(
-      G, B, P, SG, static_cast<const IO*>(x), static_cast<const IO*>(w), static_cast<YT*>(y),
-      pages, status);
-  return cudaGetLastError();
+  return launch_pdl(conv_kernel<IO, YT, 4, SLOTS>, dim3(ctiles, rtiles, B.R), dim3(kConvThreads),
+                    0, stream, G, B, P, SG, static_cast<const IO*>(x), static_cast<const IO*>(w),
+                    static_cast<YT*>(y), pages, status);
 }
 
 cudaError_t launch_conv(const Geom& G, const Batch& B, const Params& P, int io_bf16, int y_f32,

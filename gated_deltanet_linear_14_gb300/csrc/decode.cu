@@ -70,6 +70,7 @@ decode_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x, const IO* __r
   IO* mrow = reinterpret_cast<IO*>(dsm + Lay::OFF_ROW);
   __shared__ __align__(8) uint64_t full[kDecStages];
 
+  pdl_begin();
   const int kh = blockIdx.x;
   const int tid = threadIdx.x;
   const bool reporter = (kh == 0 && tid == 0);
@@ -262,11 +263,10 @@ static cudaError_t launch_decode_t(const Geom& G, const Batch& B, const Params& 
   using Lay = DecLayout<IO, ST, DK>;
   cudaError_t e = ensure_smem_limit<decode_kernel<IO, ST, DK>>((int)Lay::BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(G.Hk, B.R);
-  decode_kernel<IO, ST, DK><<<grid, kRuleThreads, Lay::BYTES, stream>>>(
-      G, B, P, static_cast<const IO*>(x), static_cast<const IO*>(w), static_cast<const IO*>(a),
-      static_cast<const IO*>(b), o, out_f32, pages, status);
-  return cudaGetLastError();
+  return launch_pdl(decode_kernel<IO, ST, DK>, dim3(G.Hk, B.R), dim3(kRuleThreads), Lay::BYTES,
+                    stream, G, B, P, static_cast<const IO*>(x), static_cast<const IO*>(w),
+                    static_cast<const IO*>(a), static_cast<const IO*>(b), o, out_f32, pages,
+                    status);
 }
 
 template <class IO, class ST>

@@ -418,6 +418,7 @@ __global__ void __launch_bounds__(kRuleThreads, MODE == MODE_VERIFY ? 6 : 4)
 rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
             const IO* __restrict__ a_in, const IO* __restrict__ b_in, void* o, int out_f32,
             void* pages, int32_t* status) {
+  pdl_begin();
   constexpr int E = DK / 8;
   __shared__ __align__(16) Stage<DK> st;
   const int nCB = G.Dv / kBV;
@@ -577,9 +578,9 @@ cudaError_t launch_rule_dk(int mode, const Geom& G, const Batch& B, const Params
   dim3 grid(G.Hv * (G.Dv / kBV), B.R);
   dim3 block(kRuleThreads);
 #define GDN_RULE_LAUNCH(IO, ST, MODE)                                                         \
-  rule_kernel<IO, ST, DK, MODE><<<grid, block, 0, stream>>>(                                  \
-      G, B, P, SG, static_cast<const IO*>(qkv), static_cast<const IO*>(a),                   \
-      static_cast<const IO*>(b), o, out_f32, pages, status)
+  return launch_pdl(rule_kernel<IO, ST, DK, MODE>, grid, block, 0, stream, G, B, P, SG,       \
+                    static_cast<const IO*>(qkv), static_cast<const IO*>(a),                   \
+                    static_cast<const IO*>(b), o, out_f32, pages, status)
 #define GDN_RULE_MODES(IO, ST)                       \
   if (mode == MODE_SEQ) GDN_RULE_LAUNCH(IO, ST, MODE_SEQ);          \
   else if (mode == MODE_VERIFY) GDN_RULE_LAUNCH(IO, ST, MODE_VERIFY); \
