@@ -39,7 +39,10 @@
  *     The caller owns every buffer; the library allocates nothing and keeps
  *     no global state.
  *   - Every call is asynchronous on the given CUDA stream (0 = legacy
- *     default stream) and never synchronises.
+ *     default stream) and never synchronises. Kernels are launched with
+ *     programmatic stream serialization and wait for the previous work on
+ *     the stream before touching any memory, so ordering is that of plain
+ *     launches; back-to-back calls overlap only their launch latency.
  *   - Host-side problems (null pointers, bad sizes, unsupported shapes) are
  *     returned as a negative gdn_status BEFORE anything is launched or
  *     written.
