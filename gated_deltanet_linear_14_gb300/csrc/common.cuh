@@ -217,44 +217,13 @@ __host__ __device__ constexpr float recip_factorial(int k) {
 // ln 2 = 0.693147180559945309417...; its float value is 0x3F317218. The high
 // part keeps that pattern with the low 12 mantissa bits cleared (0x3F317000),
 // the low part is ln 2 minus the high part, rounded to float.
-__device__ __forceinline__ float own_exp(float x) {
-  constexpr double kLn2 = 0.693147180559945309417232121458176568;
-  const float log2e = (float)(1.0 / kLn2);
-  const float ln2_hi = __uint_as_float(0x3F317000u);
-  const float ln2_lo = (float)(kLn2 - (double)0.693115234375);  // 0x3F317000 == 0.693115234375
-  if (x >= 88.72283935546875f) return __int_as_float(0x7f800000);
-  if (x <= -87.0f) return 0.0f;
-  const float t = __fmul_rn(x, log2e);
-  const float n = rintf(t);
-  float r = __fmaf_rn(-n, ln2_hi, x);
-  r = __fmaf_rn(-n, ln2_lo, r);
-  float p = recip_factorial(7);
-  p = __fmaf_rn(p, r, recip_factorial(6));
-  p = __fmaf_rn(p, r, recip_factorial(5));
-  p = __fmaf_rn(p, r, recip_factorial(4));
-  p = __fmaf_rn(p, r, recip_factorial(3));
-  p = __fmaf_rn(p, r, recip_factorial(2));
-  p = __fmaf_rn(p, r, recip_factorial(1));
-  p = __fmaf_rn(p, r, recip_factorial(0));
-  const int ni = (int)n;
-  const int h1 = ni / 2;
-  const int h2 = ni - h1;
-  const float s1 = __int_as_float((h1 + 127) << 23);
-  const float s2 = __int_as_float((h2 + 127) << 23);
-  return __fmul_rn(__fmul_rn(p, s1), s2);
-}
-
-__device__ __forceinline__ float own_silu(float z) {
-  const float e = own_exp(-z);
-  return __fdiv_rn(z, __fadd_rn(1.0f, e));
-}
-
-// own_exp on two values at once: the same operations, each rounded the same
-// way, with the floating-point steps in packed f32x2 form. The integer
-// exponent comes from t clamped to [-130, 130] (equal to t wherever the
-// result is used; it keeps the integer steps defined for the values the
-// final range selection replaces), the reduction from x itself, so a NaN
-// stays NaN as in own_exp.
+//
+// own_exp2 evaluates that exp on two values at once, the floating-point steps
+// in packed f32x2 form (each value sees exactly the roundings of the method
+// above, step by step, which is what a CPU program reproduces). The integer exponent
+// comes from t clamped to [-130, 130] (equal to t wherever the result is
+// used; it keeps the integer steps defined for the values the final range
+// selection replaces), the reduction from x itself, so a NaN stays NaN.
 __device__ __forceinline__ float2 own_exp2(float2 x) {
   constexpr double kLn2 = 0.693147180559945309417232121458176568;
   const float log2e = (float)(1.0 / kLn2);
@@ -282,7 +251,8 @@ __device__ __forceinline__ float2 own_exp2(float2 x) {
   return e;
 }
 
-// own_silu on two values at once (bit-identical to own_silu on each).
+// SiLU(z) = z / (1 + e^{-z}) on two values, with own_exp2 and a correctly
+// rounded division.
 __device__ __forceinline__ float2 own_silu2(float2 z) {
   const float2 e = own_exp2(make_float2(-z.x, -z.y));
   return make_float2(__fdiv_rn(z.x, __fadd_rn(1.0f, e.x)), __fdiv_rn(z.y, __fadd_rn(1.0f, e.y)));
@@ -305,23 +275,10 @@ __device__ __forceinline__ void gates(const Params& P, int h, float a_in, float 
   beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
 }
 
-// g (the log decay) and beta, for the chunked form (which works with
-// prefix sums of g rather than with e^g).
-__device__ __forceinline__ void gate_log(const Params& P, int h, float a_in, float b_in, float& g,
-                                         float& beta) {
-  if (P.gate_mode == 1) {
-    g = a_in;
-    beta = b_in;
-    return;
-  }
-  const float x = __fadd_rn(a_in, P.dt_bias[h]);
-  const float sp = (x > 20.0f) ? x : log1pf(expf(x));
-  g = -__fmul_rn(expf(P.A_log[h]), sp);
-  beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
-}
-
-// gate_log with the head's constants already in registers: eA = e^{A_log[h]}
-// (expf of the same value) and dtb = dt_bias[h]; the same results bit for bit.
+// g (the log decay) and beta, for the chunked form (which works with prefix
+// sums of g rather than with e^g), with the head's constants already in
+// registers: eA = e^{A_log[h]} and dtb = dt_bias[h]. The same arithmetic as
+// gates() up to e^g.
 __device__ __forceinline__ void gate_log_c(int gate_mode, float eA, float dtb, float a_in,
                                            float b_in, float& g, float& beta) {
   if (gate_mode == 1) {
