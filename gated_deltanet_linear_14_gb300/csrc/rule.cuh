@@ -410,7 +410,7 @@ struct NoAfter {
 
 // Residency targets: the verify mode keeps its token steps short (at most
 // 2 Kc rows, staged once), so it trades registers for 6 CTAs (24 warps) per
-// SM (7 or 8 forced spills and measured slower); the other modes ask for 4, which keeps them near 120 registers (left
+// SM (5, 7 and 8 measured slower; 7 and 8 force spills); the other modes ask for 4, which keeps them near 120 registers (left
 // free, the compiler went past 150 and a long prefill's per-token chain
 // measured a quarter slower).
 template <class IO, class ST, int DK, int MODE>
