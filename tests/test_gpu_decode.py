@@ -75,12 +75,13 @@ def test_decode_vs_oracle_and_repeated_steps():
 
 
 @pytest.mark.parametrize("shape", [(4, 8, 64), (2, 2, 32), (1, 4, 128)])
-def test_decode_other_head_shapes(shape):
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_decode_other_head_shapes(shape, state):
     Hk, Hv, D = shape
     sh = synth.Shapes(Hk=Hk, Hv=Hv, Dk=D, Dv=D)
     io = synth.F32 if D == 32 else synth.BF16
     d = synth.decode(R=6, sh=sh, io=io)
-    (L1, L2), pages, _ = two_layers(d, 6, gdn.GDN_F32, gdn.GDN_F32)
+    (L1, L2), pages, _ = two_layers(d, 6, state, gdn.GDN_F32)
     x, a, b = to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"])
     B1 = L1.batch(d["row_start"], d["row_len"], page=pages)
     o1 = L1.out(6)

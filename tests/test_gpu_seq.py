@@ -146,11 +146,16 @@ def test_bf16_outputs_within_one_ulp_of_rounded_oracle():
     assert rel(got, o_ref) <= 4e-3          # bf16 storage: 2^-9 relative at most
 
 
-def test_bf16_state_rounds_once_per_call():
+@pytest.mark.parametrize("shape", [(16, 32, 128), (4, 8, 64), (2, 2, 32)])
+def test_bf16_state_rounds_once_per_call(shape):
     """A bf16 page is read to fp32, advanced, and rounded once when stored:
     the result is the oracle's state rounded to bf16, up to the rounding of
-    an fp32 value that is itself within 1e-4."""
-    d = synth.decode(R=8)
+    an fp32 value that is itself within 1e-4. Head dimensions 128 and 64 stage
+    q^/k^ in the permuted order a bf16 state's 8-entry lane runs use; 32 in
+    plain order."""
+    Hk, Hv, D = shape
+    sh = synth.Shapes(Hk=Hk, Hv=Hv, Dk=D, Dv=D)
+    d = synth.decode(R=8, sh=sh)
     rows = {"x": d["x"], "a": d["a"], "b": d["b"]}
     S0 = oracle.round_bf16(d["S0"]).astype(np.float32)
     o, S, _ = gpu_seq(d, rows, d["row_start"], d["row_len"], S0, d["fresh"], state=gdn.GDN_BF16)

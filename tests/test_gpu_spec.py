@@ -327,12 +327,11 @@ def test_device_errors_page_index_and_candidate_count():
 OTHER_SHAPES = [(2, 2, 32), (2, 6, 32), (2, 6, 64), (1, 8, 128)]
 
 
-def _ragged_vs_slots(sh, io, seed, Kc=8, R=6, steps=5):
+def _ragged_vs_slots(sh, io, seed, Kc=8, R=6, steps=5, state=gdn.GDN_F32):
     """1..Kc candidates per request and step, packed in a shuffled row order:
     outputs and the committed state stay bit-identical to the slot layout."""
     rng = np.random.default_rng(seed)
     d = synth.spec(seed=int(rng.integers(1 << 30)), R=R, steps=1, n=1, sh=sh, io=io)
-    state = gdn.GDN_F32
     L1, L2, _ = make_layers(d, R, state, Kc=Kc)
     prev_len = np.zeros(R, np.int64)
     for s in range(steps):
@@ -369,6 +368,12 @@ def _ragged_vs_slots(sh, io, seed, Kc=8, R=6, steps=5):
 def test_one_page_bit_identical_to_slots_other_shapes_ragged(hk, hv, dk, io):
     _ragged_vs_slots(synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk), io,
                      100 + hk * 1000 + hv * 10 + dk)
+
+
+@pytest.mark.parametrize("hk,hv,dk", OTHER_SHAPES)
+def test_one_page_bit_identical_to_slots_other_shapes_bf16_state(hk, hv, dk):
+    _ragged_vs_slots(synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk), synth.BF16,
+                     200 + hk * 1000 + hv * 10 + dk, state=gdn.GDN_BF16)
 
 
 @pytest.mark.parametrize("Kc", [1, 3])
