@@ -336,16 +336,20 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_p
   const Geom G = make_geom(dims);
   const Params P = make_params(params, dims);
   const cudaStream_t s = (cudaStream_t)stream;
+  // the chunked launch's row map is encoded before anything is launched, so
+  // that a failure to encode it still leaves nothing launched or written
+  CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  if (any_long) {
+    const gdn_status te = encode_rows_tmap(&tmap, qkv, batch->num_rows, dims);
+    if (te != GDN_OK) return te;
+  }
   Batch Bs = make_batch(batch);
   if (any_long) Bs.max_len = threshold - 1;
   SlotGeom SG{};
   if (rule(0, G, Bs, P, SG, dims, qkv, a, b, o, pages, status, s) != cudaSuccess)
     return GDN_ERR_LAUNCH;
   if (!any_long) return GDN_OK;
-  CUtensorMap tmap;
-  std::memset(&tmap, 0, sizeof(tmap));
-  const gdn_status te = encode_rows_tmap(&tmap, qkv, batch->num_rows, dims);
-  if (te != GDN_OK) return te;
   Batch Bc = make_batch(batch);
   Bc.min_len = threshold;
   if (launch_chunk(&tmap, G, Bc, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a,
