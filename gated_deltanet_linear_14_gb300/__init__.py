@@ -8,7 +8,8 @@ never falls back to another implementation.
 Entry points (same names as the C ABI): ``gdn_conv``, ``gdn_seq``,
 ``gdn_decode``, ``gdn_prefill``, ``gdn_spec_verify``, ``gdn_spec_slots``, ``gdn_chunk_prefill``,
 ``gdn_chunk_prefill_workspace_bytes``, ``gdn_page_layout``,
-``gdn_slot_layout``, ``gdn_strerror``, ``gdn_abi_version``.
+``gdn_slot_layout``, ``gdn_check_bounded_wait``, ``gdn_strerror``,
+``gdn_abi_version``.
 """
 from __future__ import annotations
 
