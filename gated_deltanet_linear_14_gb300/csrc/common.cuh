@@ -199,15 +199,30 @@ __device__ __forceinline__ float through(float x) { return to_f(from_f<T>(x)); }
 // ----------------------------------------------------------- own exp, SiLU
 //
 // The conv's SiLU must be reproducible bit for bit by a plain CPU program, so
-// it does not use the CUDA math library. exp is computed with Cody and
-// Waite's argument reduction (Cody & Waite, "Software Manual for the
-// Elementary Functions", 1980): x = n ln2 + r, n = round-to-even(x log2 e),
-// ln2 split into a 12-bit-trimmed high part and a low correction; e^r from
-// the Taylor series through r^7 (coefficients 1/k!), Horner's rule with
-// fused multiply-adds; scaling by 2^n as two exact power-of-two factors.
-// x at or above the float nearest ln(FLT_MAX) = 88.7228390520684 (that float,
-// 88.72283935546875, lies just above it, so every smaller x has a finite
-// result) gives +inf; x <= -87 gives 0.
+// it uses no CUDA math-library function and no division or reciprocal of the
+// compiler: only IEEE additions, multiplications and fused multiply-adds,
+// rounded to nearest even, in a fixed order.
+//
+// SiLU(z) = z sigmoid(z). With t = e^{-|z|} in [0, 1] and d = 1 + t in
+// [1, 2], sigmoid(z) is 1/d for z >= 0 and t/d for z < 0, so exp is only
+// taken of a non-positive argument and the reciprocal only of a number in
+// [1, 2].
+//
+// exp of a <= 0: Cody and Waite's argument reduction (Cody & Waite, "Software
+// Manual for the Elementary Functions", 1980): a = n ln2 + r, n =
+// round-to-even(a log2 e), ln2 split into a 12-bit-trimmed high part and a
+// low correction; e^r from the Taylor series through r^7 (coefficients 1/k!),
+// Horner's rule with fused multiply-adds; then p 2^n as (p 2^(n+64)) 2^-64:
+// the first product is exact (a normal number) and the second rounds once,
+// which matters only where e^a is subnormal. a is first raised to -104,
+// below which e^a is under half the smallest subnormal and rounds to 0.
+//
+// 1/d: the Newton-Raphson reciprocal iteration of Newton-Raphson division:
+// the linear seed 24/17 - (8/17) d (relative error at most 1/17 on [1, 2]),
+// then two steps r <- r + r (1 - d r), each squaring the relative error
+// (about 4, 8, then 16 bits). The quotient q = num r (num = 1 or t) is then
+// corrected once, q <- q + r (num - d q), which squares the error again
+// (about 33 bits before rounding).
 __host__ __device__ constexpr float recip_factorial(int k) {
   double f = 1.0;
   for (int i = 2; i <= k; ++i) f *= i;
@@ -218,44 +233,50 @@ __host__ __device__ constexpr float recip_factorial(int k) {
 // part keeps that pattern with the low 12 mantissa bits cleared (0x3F317000),
 // the low part is ln 2 minus the high part, rounded to float.
 //
-// own_exp2 evaluates that exp on two values at once, the floating-point steps
-// in packed f32x2 form (each value sees exactly the roundings of the method
-// above, step by step, which is what a CPU program reproduces). The integer exponent
-// comes from t clamped to [-130, 130] (equal to t wherever the result is
-// used; it keeps the integer steps defined for the values the final range
-// selection replaces), the reduction from x itself, so a NaN stays NaN.
-__device__ __forceinline__ float2 own_exp2(float2 x) {
+// own_exp2_nonpos evaluates that exp on two values a <= 0 at once, the
+// floating-point steps in packed f32x2 form (each value sees exactly the
+// roundings of the method above, which is what a CPU program reproduces).
+// n = round-to-even(t) comes from m = t + 1.5 2^23: for |t| <= 151, m lies
+// where the spacing of floats is 1, so the addition rounds t to the nearest
+// integer, ties to even; n = m - 1.5 2^23 exactly, and the low 9 bits of m's
+// pattern are n mod 512, so adding 127 + 64 and shifting them into the
+// exponent field gives the pattern of 2^(n+64).
+__device__ __forceinline__ float2 own_exp2_nonpos(float2 a) {
   constexpr double kLn2 = 0.693147180559945309417232121458176568;
   const float log2e = (float)(1.0 / kLn2);
   const float ln2_hi = __uint_as_float(0x3F317000u);
   const float ln2_lo = (float)(kLn2 - (double)0.693115234375);
-  const float2 t = __fmul2_rn(x, make_float2(log2e, log2e));
-  const float2 n = make_float2(rintf(fminf(fmaxf(t.x, -130.0f), 130.0f)),
-                               rintf(fminf(fmaxf(t.y, -130.0f), 130.0f)));
+  const float kRound = 12582912.0f;  // 1.5 2^23
+  a = make_float2(fmaxf(a.x, -104.0f), fmaxf(a.y, -104.0f));
+  const float2 t = __fmul2_rn(a, make_float2(log2e, log2e));
+  const float2 m = __fadd2_rn(t, make_float2(kRound, kRound));
+  const float2 n = __fadd2_rn(m, make_float2(-kRound, -kRound));
   const float2 mn = make_float2(-n.x, -n.y);
-  float2 r = __ffma2_rn(mn, make_float2(ln2_hi, ln2_hi), x);
+  float2 r = __ffma2_rn(mn, make_float2(ln2_hi, ln2_hi), a);
   r = __ffma2_rn(mn, make_float2(ln2_lo, ln2_lo), r);
   float2 p = make_float2(recip_factorial(7), recip_factorial(7));
 #pragma unroll
   for (int k = 6; k >= 0; --k)
     p = __ffma2_rn(p, r, make_float2(recip_factorial(k), recip_factorial(k)));
-  const int nx = (int)n.x, ny = (int)n.y;
-  const int hx = nx / 2, hy = ny / 2;
-  const float2 s1 = make_float2(__int_as_float((hx + 127) << 23), __int_as_float((hy + 127) << 23));
-  const float2 s2 = make_float2(__int_as_float((nx - hx + 127) << 23),
-                                __int_as_float((ny - hy + 127) << 23));
-  float2 e = __fmul2_rn(__fmul2_rn(p, s1), s2);
-  const float inf = __int_as_float(0x7f800000);
-  e.x = (x.x >= 88.72283935546875f) ? inf : ((x.x <= -87.0f) ? 0.0f : e.x);
-  e.y = (x.y >= 88.72283935546875f) ? inf : ((x.y <= -87.0f) ? 0.0f : e.y);
-  return e;
+  const float2 s = make_float2(__uint_as_float((__float_as_uint(m.x) + 191u) << 23),
+                               __uint_as_float((__float_as_uint(m.y) + 191u) << 23));
+  return __fmul2_rn(__fmul2_rn(p, s), make_float2(0x1p-64f, 0x1p-64f));
 }
 
-// SiLU(z) = z / (1 + e^{-z}) on two values, with own_exp2 and a correctly
-// rounded division.
+// SiLU on two values (the method above).
 __device__ __forceinline__ float2 own_silu2(float2 z) {
-  const float2 e = own_exp2(make_float2(-z.x, -z.y));
-  return make_float2(__fdiv_rn(z.x, __fadd_rn(1.0f, e.x)), __fdiv_rn(z.y, __fadd_rn(1.0f, e.y)));
+  const float2 one = make_float2(1.0f, 1.0f);
+  const float2 t = own_exp2_nonpos(make_float2(-fabsf(z.x), -fabsf(z.y)));
+  const float2 d = __fadd2_rn(one, t);
+  const float2 nd = make_float2(-d.x, -d.y);
+  const float s0 = (float)(24.0 / 17.0), s1 = (float)(8.0 / 17.0);
+  float2 r = __ffma2_rn(make_float2(-s1, -s1), d, make_float2(s0, s0));
+#pragma unroll
+  for (int i = 0; i < 2; ++i) r = __ffma2_rn(r, __ffma2_rn(nd, r, one), r);
+  const float2 num = make_float2(z.x >= 0.0f ? 1.0f : t.x, z.y >= 0.0f ? 1.0f : t.y);
+  float2 q = __fmul2_rn(num, r);
+  q = __ffma2_rn(r, __ffma2_rn(nd, q, num), q);
+  return __fmul2_rn(z, q);
 }
 
 // ----------------------------------------------------------------- gates

@@ -32,7 +32,9 @@
 // oracle_conv_f64 is IEEE double. oracle_conv_f32 is the one deliberate
 // exception: it is the fp32-accumulate conv that the GPU conv must match bit
 // for bit, so it fixes the accumulation order (bias, then taps j = 0..W-1,
-// each a fused multiply-add) and evaluates SiLU with its own exp (below).
+// each a fused multiply-add) and evaluates SiLU with its own exp and
+// reciprocal (below), from IEEE additions, multiplications and fused
+// multiply-adds only.
 // Build with -ffp-contract=off so the compiler adds no contractions.
 
 #include <cfloat>
@@ -185,19 +187,31 @@ void parallel_for(long n, int threads, F f) {
 
 // ------------------------------------------------------- fp32 conv mirror
 //
-// Own single-precision exp used by the fp32 conv mirror. Method: Cody & Waite
-// argument reduction (W. J. Cody and W. Waite, "Software Manual for the
-// Elementary Functions", 1980): x = n ln2 + r with n = round(x / ln2) and
-// ln2 split into a short high part and a low correction so n*ln2_hi is exact;
-// then e^r from its Taylor series, truncated after the r^7 term and evaluated
-// by Horner's rule with fused multiply-adds; then scaling by 2^n, built from
-// two exact power-of-two factors so no intermediate leaves the normal range.
-// Inputs at or above the float nearest ln(FLT_MAX) (which lies just above
-// it, so every smaller input has a finite result) give +inf; inputs <= -87
-// give 0 (the result would leave the normal range).
+// SiLU(x) = x sigmoid(x), evaluated as the GPU conv does, step for step.
+// With t = e^{-|x|} in [0, 1] and d = 1 + t in [1, 2], sigmoid(x) is 1/d for
+// x >= 0 and t/d for x < 0: exp is only taken of a non-positive argument and
+// the reciprocal only of a number in [1, 2].
+//
+// exp of a <= 0: Cody & Waite argument reduction (W. J. Cody and W. Waite,
+// "Software Manual for the Elementary Functions", 1980): a = n ln2 + r with
+// n = round(a / ln2) and ln2 split into a short high part and a low
+// correction so n*ln2_hi is exact; e^r from its Taylor series, truncated
+// after the r^7 term and evaluated by Horner's rule with fused multiply-adds;
+// then p 2^n as (p 2^(n+64)) 2^-64, where the first product is exact (a
+// normal number) and the second rounds once (only where e^a is subnormal).
+// a is first raised to -104, below which e^a is under half the smallest
+// subnormal and rounds to 0.
+//
+// 1/d: Newton-Raphson reciprocal iteration (the textbook Newton-Raphson
+// division method): the linear seed 24/17 - (8/17) d, within relative error
+// 1/17 of 1/d on [1, 2], then two steps r <- r + r (1 - d r), each of which
+// squares the relative error (about 4, 8, then 16 bits). The quotient
+// q = num * r (num = 1 or t) is corrected once, q <- q + r (num - d q), which
+// squares it again (about 33 bits before rounding).
 struct OwnExpConsts {
   float log2e, ln2_hi, ln2_lo;
   float c[8];  // 1/k!, k = 0..7
+  float seed0, seed1;  // 24/17, 8/17
   OwnExpConsts() {
     const double ln2 = std::log(2.0);
     log2e = (float)(1.0 / ln2);
@@ -215,6 +229,8 @@ struct OwnExpConsts {
       if (k > 0) f *= k;
       c[k] = (float)(1.0 / f);
     }
+    seed0 = (float)(24.0 / 17.0);
+    seed1 = (float)(8.0 / 17.0);
   }
 };
 const OwnExpConsts kExp;
@@ -226,35 +242,39 @@ float pow2_exact(int n) {  // 2^n for -126 <= n <= 127, built from the bits
   return f;
 }
 
-float own_exp_f32(float x) {
-  static const float kOverflow = (float)std::log((double)FLT_MAX);
-  if (x >= kOverflow) return INFINITY;
-  if (x <= -87.0f) return 0.0f;
-  const float t = x * kExp.log2e;        // one rounding, no contraction
+// e^a for a <= 0 (a NaN is treated as -104, like the GPU's fmaxf).
+float own_exp_nonpos_f32(float a) {
+  a = std::fmax(a, -104.0f);
+  const float t = a * kExp.log2e;        // one rounding, no contraction
   const float n = std::nearbyint(t);     // round half to even (default mode)
-  float r = std::fma(-n, kExp.ln2_hi, x);
+  float r = std::fma(-n, kExp.ln2_hi, a);
   r = std::fma(-n, kExp.ln2_lo, r);
   float p = kExp.c[7];
   for (int k = 6; k >= 0; --k) p = std::fma(p, r, kExp.c[k]);
-  const int ni = (int)n;
-  const int h1 = ni / 2;                 // truncation toward zero
-  const int h2 = ni - h1;
-  return (p * pow2_exact(h1)) * pow2_exact(h2);
+  return (p * pow2_exact((int)n + 64)) * pow2_exact(-64);
 }
 
 float silu_own_f32(float x) {
-  // x * sigmoid(x) written as x / (1 + e^-x), one IEEE division.
-  const float e = own_exp_f32(-x);
-  const float d = 1.0f + e;
-  return x / d;
+  const float t = own_exp_nonpos_f32(-std::fabs(x));
+  const float d = 1.0f + t;
+  float r = std::fma(-kExp.seed1, d, kExp.seed0);
+  for (int i = 0; i < 2; ++i) {
+    const float e = std::fma(-d, r, 1.0f);
+    r = std::fma(r, e, r);
+  }
+  const float num = (x >= 0.0f) ? 1.0f : t;
+  float q = num * r;
+  const float e = std::fma(-d, q, num);
+  q = std::fma(r, e, q);
+  return x * q;
 }
 
 }  // namespace
 
 extern "C" {
 
-// Own fp32 exp, exposed for its own pins.
-float oracle_exp_f32(float x) { return own_exp_f32(x); }
+// Own fp32 exp (of a <= 0), exposed for its own pins.
+float oracle_exp_f32(float x) { return own_exp_nonpos_f32(x); }
 float oracle_silu_f32(float x) { return silu_own_f32(x); }
 
 // Causal depthwise conv + SiLU, fp32 accumulate, fixed order.

@@ -234,32 +234,41 @@ def test_conv_f32_within_fp32_bound_of_f64():
 
 
 def test_own_exp_within_two_ulp():
-    xs = np.concatenate([np.linspace(-86.9, 88.4, 20001), np.linspace(-1, 1, 2001),
-                         [0.0, -0.0, 1e-8, -1e-8, 0.5 * math.log(2), -0.5 * math.log(2)]])
+    """The conv's own exp, taken only of arguments a <= 0: within 2 ulp of
+    e^a wherever e^a is a normal float, within one subnormal spacing below,
+    and 0 from -104 down (e^-104 is under half the smallest subnormal)."""
+    xs = np.concatenate([np.linspace(-87.3, 0.0, 20001), np.linspace(-1, 0, 2001),
+                         [-0.0, -1e-8, -0.5 * math.log(2), -math.log(2), -87.0]])
     for x in xs.astype(np.float32):
         got = oracle.exp_f32(float(x))
         ref = math.exp(float(x))
         ulp = np.spacing(np.float32(ref))
         assert abs(got - ref) <= 2 * ulp, (x, got, ref)
-    assert oracle.exp_f32(100.0) == math.inf
-    assert oracle.exp_f32(-100.0) == 0.0
-    # the largest float with a finite e^x overflows nothing; the next one does
-    top = np.float32(math.log(float(np.finfo(np.float32).max)))
-    below = np.nextafter(top, np.float32(0))
-    assert math.exp(float(top)) > float(np.finfo(np.float32).max) > math.exp(float(below))
-    got = oracle.exp_f32(float(below))
-    assert math.isfinite(got) and abs(got - math.exp(float(below))) <= 2 * np.spacing(np.float32(got))
-    assert oracle.exp_f32(float(top)) == math.inf
-    for x in np.linspace(88.4, float(below), 200).astype(np.float32):
-        ref = math.exp(float(x))
-        assert abs(oracle.exp_f32(float(x)) - ref) <= 2 * np.spacing(np.float32(ref))
+    assert oracle.exp_f32(0.0) == 1.0 and oracle.exp_f32(-0.0) == 1.0
+    tiny = 2.0 ** -149
+    for x in np.linspace(-103.9, -87.4, 2001).astype(np.float32):
+        assert abs(oracle.exp_f32(float(x)) - math.exp(float(x))) <= tiny, x
+    for x in (-104.0, -150.0, -1e30, -math.inf):
+        assert oracle.exp_f32(x) == 0.0
 
 
 def test_own_silu_within_four_ulp():
-    for x in np.linspace(-60, 60, 12001).astype(np.float32):
+    """SiLU(x) = x sigmoid(x) through the own exp and the Newton reciprocal:
+    within 4 ulp of the exact value where it is a normal float of at least
+    2^-124, and within 2^-140 absolutely below that (x < -87, where e^x is
+    subnormal)."""
+    xs = np.concatenate([np.linspace(-87, 87, 34801), np.linspace(-1, 1, 4001),
+                         [0.0, -0.0, 1e-30, -1e-30, 1e-6, -1e-6, 100.0, 1e30]])
+    for x in xs.astype(np.float32):
         got = oracle.silu_f32(float(x))
         ref = float(x) / (1.0 + math.exp(-float(x)))
-        assert abs(got - ref) <= 4 * np.spacing(np.float32(abs(ref))) + 1e-37, (x, got, ref)
+        assert abs(got - ref) <= 4 * np.spacing(np.float32(abs(ref))) + 1e-45, (x, got, ref)
+    for x in np.linspace(-104, -87, 3401).astype(np.float32):
+        ref = float(x) * math.exp(float(x)) / (1.0 + math.exp(float(x)))
+        assert abs(oracle.silu_f32(float(x)) - ref) <= 2.0 ** -140, x
+    assert oracle.silu_f32(-200.0) == 0.0 and math.copysign(1, oracle.silu_f32(-200.0)) < 0
+    assert oracle.silu_f32(math.inf) == math.inf
+    assert math.isnan(oracle.silu_f32(math.nan))
 
 
 # ----------------------------------------------------------- slot simulation
