@@ -212,10 +212,11 @@ __device__ __forceinline__ float through(float x) { return to_f(from_f<T>(x)); }
 // Manual for the Elementary Functions", 1980): a = n ln2 + r, n =
 // round-to-even(a log2 e), ln2 split into a 12-bit-trimmed high part and a
 // low correction; e^r from the Taylor series through r^7 (coefficients 1/k!),
-// Horner's rule with fused multiply-adds; then p 2^n as (p 2^(n+64)) 2^-64:
-// the first product is exact (a normal number) and the second rounds once,
-// which matters only where e^a is subnormal. a is first raised to -104,
-// below which e^a is under half the smallest subnormal and rounds to 0.
+// Horner's rule with fused multiply-adds, the coefficients scaled by 2^-64
+// (exactly, so the polynomial comes out as p 2^-64 with p's own roundings);
+// then one product with 2^(n+64), which rounds once, and only where e^a is
+// subnormal. a is first raised to -104, below which e^a is under half the
+// smallest subnormal and rounds to 0.
 //
 // 1/d: the Newton-Raphson reciprocal iteration of Newton-Raphson division:
 // the linear seed 24/17 - (8/17) d (relative error at most 1/17 on [1, 2]),
@@ -251,16 +252,18 @@ __device__ __forceinline__ float2 own_exp2_nonpos(float2 a) {
   const float2 t = __fmul2_rn(a, make_float2(log2e, log2e));
   const float2 m = __fadd2_rn(t, make_float2(kRound, kRound));
   const float2 n = __fadd2_rn(m, make_float2(-kRound, -kRound));
-  const float2 mn = make_float2(-n.x, -n.y);
-  float2 r = __ffma2_rn(mn, make_float2(ln2_hi, ln2_hi), a);
-  r = __ffma2_rn(mn, make_float2(ln2_lo, ln2_lo), r);
-  float2 p = make_float2(recip_factorial(7), recip_factorial(7));
+  float2 r = __ffma2_rn(n, make_float2(-ln2_hi, -ln2_hi), a);
+  r = __ffma2_rn(n, make_float2(-ln2_lo, -ln2_lo), r);
+  const float c7 = recip_factorial(7) * 0x1p-64f;
+  float2 p = make_float2(c7, c7);
 #pragma unroll
-  for (int k = 6; k >= 0; --k)
-    p = __ffma2_rn(p, r, make_float2(recip_factorial(k), recip_factorial(k)));
+  for (int k = 6; k >= 0; --k) {
+    const float ck = recip_factorial(k) * 0x1p-64f;
+    p = __ffma2_rn(p, r, make_float2(ck, ck));
+  }
   const float2 s = make_float2(__uint_as_float((__float_as_uint(m.x) + 191u) << 23),
                                __uint_as_float((__float_as_uint(m.y) + 191u) << 23));
-  return __fmul2_rn(__fmul2_rn(p, s), make_float2(0x1p-64f, 0x1p-64f));
+  return __fmul2_rn(p, s);
 }
 
 // SiLU on two values (the method above).

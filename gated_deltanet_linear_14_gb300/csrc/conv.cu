@@ -19,18 +19,21 @@
 //     window and another writes the final one).
 //   * accumulation is fp32 in a fixed order: bias (or 0), then taps
 //     j = 0..W-1 oldest first, each a fused multiply-add; SiLU uses the
-//     library's own exp. The CPU fp32 conv reproduces this bit for bit.
+//     library's own exp and Newton reciprocal (additions, multiplications
+//     and fused multiply-adds only). The CPU fp32 conv reproduces this bit
+//     for bit.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace gdn {
 
 constexpr int kConvThreads = 128;
-// The SiLU (own exp and an exact division per element) makes the conv
-// issue-bound rather than HBM-bound, so residency matters more than wide
-// vectors or deep load batches: 8-byte vectors, 4 rows in flight and 8 CTAs
-// (32 warps) per SM ran a 32k-row batch in 0.50 ms, against 0.57 ms with 8
-// rows in flight and 0.68 ms with 16-byte vectors at 3 CTAs per SM.
+// The exact SiLU (own exp and reciprocal per element) makes the conv bound
+// by its floating-point pipe rather than by HBM, so residency matters more
+// than wide vectors or deep load batches: 8-byte vectors, 4 rows in flight
+// and 8 CTAs (32 warps) per SM ran a 32k-row batch in 0.50 ms, against
+// 0.57 ms with 8 rows in flight and 0.68 ms with 16-byte vectors at 3 CTAs
+// per SM (with the earlier, division-based SiLU).
 constexpr int kConvVecBytes = 8;
 constexpr int kConvRows = 32;  // rows per tile (>= W-1)
 constexpr int kConvBatch = 4;  // rows whose loads are in flight together

@@ -196,11 +196,11 @@ void parallel_for(long n, int threads, F f) {
 // "Software Manual for the Elementary Functions", 1980): a = n ln2 + r with
 // n = round(a / ln2) and ln2 split into a short high part and a low
 // correction so n*ln2_hi is exact; e^r from its Taylor series, truncated
-// after the r^7 term and evaluated by Horner's rule with fused multiply-adds;
-// then p 2^n as (p 2^(n+64)) 2^-64, where the first product is exact (a
-// normal number) and the second rounds once (only where e^a is subnormal).
-// a is first raised to -104, below which e^a is under half the smallest
-// subnormal and rounds to 0.
+// after the r^7 term and evaluated by Horner's rule with fused multiply-adds,
+// its coefficients scaled by 2^-64 (exactly: the result is p 2^-64 with p's
+// own roundings); then one product with 2^(n+64), which rounds once, and
+// only where e^a is subnormal. a is first raised to -104, below which e^a is
+// under half the smallest subnormal and rounds to 0.
 //
 // 1/d: Newton-Raphson reciprocal iteration (the textbook Newton-Raphson
 // division method): the linear seed 24/17 - (8/17) d, within relative error
@@ -249,9 +249,10 @@ float own_exp_nonpos_f32(float a) {
   const float n = std::nearbyint(t);     // round half to even (default mode)
   float r = std::fma(-n, kExp.ln2_hi, a);
   r = std::fma(-n, kExp.ln2_lo, r);
-  float p = kExp.c[7];
-  for (int k = 6; k >= 0; --k) p = std::fma(p, r, kExp.c[k]);
-  return (p * pow2_exact((int)n + 64)) * pow2_exact(-64);
+  const float s = pow2_exact(-64);
+  float p = kExp.c[7] * s;
+  for (int k = 6; k >= 0; --k) p = std::fma(p, r, kExp.c[k] * s);
+  return p * pow2_exact((int)n + 64);
 }
 
 float silu_own_f32(float x) {
