@@ -13,10 +13,10 @@ from tests.gpu_util import Layer, bits, f64, rel, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def two_layers(d, R, state, out, Kc=0):
+def two_layers(d, R, state, out, Kc=0, gate_mode=0):
     sh = d["shapes"]
     Ls = [Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=Kc, state=state, out=out,
-                num_pages=R + 3) for _ in range(2)]
+                num_pages=R + 3, gate_mode=gate_mode) for _ in range(2)]
     S0 = d["S0"][:R]
     if state == gdn.GDN_BF16:
         S0 = oracle.round_bf16(S0).astype(np.float32)
@@ -45,6 +45,32 @@ def test_decode_bitwise_equals_conv_then_seq(state, out):
     L2.ok()
     assert np.array_equal(bits(o1), bits(o2))
     assert torch.equal(L1.pool.buf, L2.pool.buf)          # states, windows, flags
+
+
+def test_decode_gate_mode_precomputed_bitwise_equals_conv_then_seq():
+    """With precomputed gates (a = g <= 0, b = beta in [0, 1]) the fused step
+    still equals gdn_conv + gdn_seq bit for bit (gdn_seq's precomputed-gate
+    path is pinned to the oracle in test_gpu_seq.py)."""
+    d = synth.decode()
+    R = d["R"]
+    sh = d["shapes"]
+    rng = np.random.default_rng(11)
+    g = synth.as_io(-np.abs(rng.standard_normal((R, sh.Hv))) * 0.7, synth.BF16)
+    beta = synth.as_io(rng.uniform(0, 1, (R, sh.Hv)), synth.BF16)
+    (L1, L2), pages, _ = two_layers(d, R, gdn.GDN_F32, gdn.GDN_F32, gate_mode=1)
+    fresh = np.array([r % 7 == 0 for r in range(R)])
+    flags = np.where(fresh, gdn.GDN_REQ_FRESH, 0)
+    x, a, b = to_dev(d["x"]), to_dev(g), to_dev(beta)
+    B1 = L1.batch(d["row_start"], d["row_len"], page=pages, flags=flags)
+    o1 = L1.out(R)
+    gdn.gdn_decode(L1.dims, B1, L1.params, x, L1.conv_w, a, b, o1, L1.pool.buf, L1.status)
+    L1.ok()
+    B2 = L2.batch(d["row_start"], d["row_len"], page=pages, flags=flags)
+    y = L2.conv(B2, x)
+    o2 = L2.seq(B2, y, a, b)
+    L2.ok()
+    assert np.array_equal(bits(o1), bits(o2))
+    assert torch.equal(L1.pool.buf, L2.pool.buf)
 
 
 def test_decode_vs_oracle_and_repeated_steps():

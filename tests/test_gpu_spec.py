@@ -423,3 +423,36 @@ def test_switch_to_slot_layout_midstream(state):
     for r in range(R):
         for i in range(n):
             assert np.array_equal(bits(L2.slots.state(r, i)), bits(L3.slots.state(r, i)))
+
+
+def test_one_page_bit_identical_to_slots_gate_mode_precomputed():
+    """Precomputed gates (a = g <= 0, b = beta in [0, 1]): the record carries
+    them as given and the replay reads them back, so the one-page verify
+    still equals the slot layout bit for bit over several steps."""
+    d = synth.spec(R=8, steps=5)
+    R, n, steps = d["R"], d["n"], d["steps"]
+    sh = d["shapes"]
+    rng = np.random.default_rng(12)
+    start, ln = d["row_start"][:R], d["row_len"][:R]
+    L1 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=R,
+               gate_mode=1)
+    L2 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=R,
+               slots=True, gate_mode=1)
+    hist = to_dev(d["hist0"])[:R]
+    S0 = d["S0"][:R]
+    L1.seed(range(R), S0=S0, hist=hist)
+    for r in range(R):
+        L2.slots.state(r, 0).copy_(torch.from_numpy(S0[r]).transpose(-1, -2))
+        L2.slots.window(r, 0).copy_(hist[r])
+    for s in range(steps):
+        x = to_dev(d["step_rows"][s]["x"])[: R * n]
+        g = synth.as_io(-np.abs(rng.standard_normal((R * n, sh.Hv))) * 0.7, synth.BF16)
+        beta = synth.as_io(rng.uniform(0, 1, (R * n, sh.Hv)), synth.BF16)
+        a, b = to_dev(g), to_dev(beta)
+        acc = d["accepted"][s][:R]
+        _, o1 = one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        B2 = L2.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc)
+        _, o2 = L2.spec_slots(B2, x, a, b)
+        L1.ok()
+        L2.ok()
+        assert np.array_equal(bits(o1), bits(o2)), f"outputs differ at step {s}"
