@@ -171,6 +171,15 @@ def test_chunk_long_prefill_full_size_sampled_heads():
     o = chunk_run(L, B, to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"]))
     L.ok()
     assert torch.isfinite(o).all()
+    # the benchmark's bf16 outputs: exactly the fp32 outputs rounded to nearest even
+    Lb = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], num_pages=d["R"],
+               out=gdn.GDN_BF16)
+    Bb = Lb.batch(start, ln, flags=gdn.GDN_REQ_FRESH)
+    ob = chunk_run(Lb, Bb, to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"]), o_dtype=torch.bfloat16)
+    Lb.ok()
+    assert ob.dtype == torch.bfloat16 and torch.equal(ob, o.to(torch.bfloat16))
+    assert torch.equal(Lb.pool.buf, L.pool.buf)
+    del Lb, Bb, ob
     for r, kh in ((0, 0), (1, 7), (2, 11), (3, 15)):
         qkv, a, b, h0 = _head_pair(d, rows, r, kh, start, ln)
         o_ref, S_ref = oracle.gdn_f64(qkv, a, b, d["A_log"][h0:h0 + 2], d["dt_bias"][h0:h0 + 2],

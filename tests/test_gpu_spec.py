@@ -456,3 +456,51 @@ def test_one_page_bit_identical_to_slots_gate_mode_precomputed():
         L1.ok()
         L2.ok()
         assert np.array_equal(bits(o1), bits(o2)), f"outputs differ at step {s}"
+
+
+def test_bench_configuration_bf16_outputs_vs_slots_and_oracle():
+    """The configuration the benchmark times: 64 pages x (1+7) candidates,
+    fp32 state, bf16 rows and bf16 outputs. Bit-identical to the slot layout
+    over 5 steps; for 4 of the requests, each output is the oracle's slot
+    simulation rounded to bf16 or its neighbour (the fp32 result sits
+    within 1e-4 of the oracle, so it can cross a rounding boundary)."""
+    d = synth.spec()
+    R, n = d["R"], d["n"]
+    steps = 5
+    sh = d["shapes"]
+    start, ln = d["row_start"], d["row_len"]
+    L1 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=R,
+               out=gdn.GDN_BF16)
+    L2 = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=R,
+               out=gdn.GDN_BF16, slots=True)
+    hist = to_dev(d["hist0"])[:R]
+    S0 = d["S0"][:R]
+    L1.seed(range(R), S0=S0, hist=hist)
+    for r in range(R):
+        L2.slots.state(r, 0).copy_(torch.from_numpy(S0[r]).transpose(-1, -2))
+        L2.slots.window(r, 0).copy_(hist[r])
+    k = 4
+    sim = oracle.SlotSim(k, sh.Hk, sh.Hv, sh.Dk, sh.Dv, sh.W, d["conv_w"].value, d["A_log"],
+                         d["dt_bias"], S0=S0[:k], hist0=d["hist0"].value[:k],
+                         row_store=oracle.round_bf16)
+    for s in range(steps):
+        x, a, b = step_rows(d, s, R, n)
+        acc = d["accepted"][s]
+        _, o1 = one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        B2 = L2.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc)
+        _, o2 = L2.spec_slots(B2, x, a, b)
+        L1.ok()
+        L2.ok()
+        assert np.array_equal(bits(o1), bits(o2)), f"outputs differ at step {s}"
+        rows = d["step_rows"][s]
+        xs = rows["x"].value[: k * n].reshape(k, n, -1)
+        As = rows["a"].value[: k * n].reshape(k, n, -1)
+        Bs = rows["b"].value[: k * n].reshape(k, n, -1)
+        _, o_ref = sim.step(xs, As, Bs, acc[:k])
+        o_ref = o_ref.reshape(k * n, sh.Hv, sh.Dv)
+        got = f64(o1)[: k * n]
+        ref_round = oracle.round_bf16(o_ref)
+        spacing = np.spacing(np.abs(ref_round).astype(np.float32)).astype(np.float64) * 2.0 ** 16
+        rms = np.sqrt(np.mean(o_ref ** 2))
+        assert np.all(np.abs(got - o_ref) <= spacing + 1e-4 * rms), f"step {s}"
+        assert np.mean(got != ref_round) < 0.05
