@@ -16,7 +16,7 @@ import torch
 import gated_deltanet_linear_14_gb300 as gdn
 import oracle
 import synth
-from tests.gpu_util import Layer, f64, rel, to_dev
+from tests.gpu_util import Layer, assert_close, f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -49,4 +49,4 @@ def test_wait_runs_out_reports_timeout_and_context_stays_usable():
     o_ref, _ = oracle.gdn_f64(d["x"].value, d["a"].value, d["b"].value, d["A_log"],
                               d["dt_bias"], d["row_start"], d["row_len"], sh.Hk, sh.Hv, sh.Dk,
                               sh.Dv, S0=None)
-    assert rel(f64(o), o_ref) <= 1e-4
+    assert_close(f64(o), o_ref, 1e-4, what="o")

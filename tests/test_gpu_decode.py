@@ -8,7 +8,7 @@ import torch
 import gated_deltanet_linear_14_gb300 as gdn
 import oracle
 import synth
-from tests.gpu_util import Layer, bits, f64, rel, to_dev
+from tests.gpu_util import Layer, assert_close, bits, f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -95,9 +95,9 @@ def test_decode_vs_oracle_and_repeated_steps():
                                   d["A_log"], d["dt_bias"], np.arange(R), np.ones(R), sh.Hk,
                                   sh.Hv, sh.Dk, sh.Dv, S0=S)
         hist = hist.astype(np.float64)
-        assert rel(f64(o), o_ref) <= 1e-4, step
+        assert_close(f64(o), o_ref, 1e-4, what=f"o step {step}")
     Sg = np.stack([f64(L.pool.state_math(r)) for r in range(R)])
-    assert rel(Sg, S) <= 1e-4
+    assert_close(Sg, S, 1e-4, inner=2, what="S")
 
 
 @pytest.mark.parametrize("shape", [(4, 8, 64), (2, 2, 32), (1, 4, 128)])
@@ -193,5 +193,6 @@ def test_max_request_count_in_one_launch():
         o_ref, S_ref = oracle.gdn_f64(y, d["a"].value[r:r + 1], d["b"].value[r:r + 1], d["A_log"],
                                       d["dt_bias"], [0], [1], sh.Hk, sh.Hv, sh.Dk, sh.Dv,
                                       S0=S0[r:r + 1])
-        assert rel(f64(o1[r]), o_ref[0]) <= 1e-4, r
-        assert rel(f64(L1.pool.state_math(int(pages[r]))), S_ref[0]) <= 1e-4, r
+        assert_close(f64(o1[r]), o_ref[0], 1e-4, what=f"o request {r}")
+        assert_close(f64(L1.pool.state_math(int(pages[r]))), S_ref[0], 1e-4, inner=2,
+                     what=f"S request {r}")
