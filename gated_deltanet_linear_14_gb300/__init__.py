@@ -6,7 +6,8 @@ device memory and streams. The binding raises if the library is missing; it
 never falls back to another implementation.
 
 Entry points (same names as the C ABI): ``gdn_conv``, ``gdn_seq``,
-``gdn_decode``, ``gdn_prefill``, ``gdn_spec_verify``, ``gdn_spec_slots``, ``gdn_chunk_prefill``,
+``gdn_decode``, ``gdn_prefill``, ``gdn_spec_verify``, ``gdn_spec_step``, ``gdn_spec_slots``,
+``gdn_chunk_prefill``,
 ``gdn_chunk_prefill_workspace_bytes``, ``gdn_page_layout``,
 ``gdn_slot_layout``, ``gdn_check_bounded_wait``, ``gdn_strerror``,
 ``gdn_abi_version``.
@@ -102,6 +103,7 @@ def load_library(path: str = LIB_PATH):
             "gdn_conv": ([D, B, PR, P, P, P, I, P, P, P], I),
             "gdn_seq": ([D, B, PR, P, P, P, P, P, P, P], I),
             "gdn_spec_verify": ([D, B, PR, P, P, P, P, P, P, P], I),
+            "gdn_spec_step": ([D, B, PR, P, P, P, P, P, P, P, P], I),
             "gdn_decode": ([D, B, PR, P, P, P, P, P, P, P, P], I),
             "gdn_prefill": ([D, B, PR, P, P, P, P, P, I, P, P], I),
             "gdn_spec_slots": ([D, B, PR, P, P, P, P, P, P, P, P, P], I),
@@ -202,6 +204,13 @@ def gdn_spec_verify(dims, batch, params, qkv, a, b, o, pages, status, stream=Non
                                           ctypes.byref(params), _ptr(qkv), _ptr(a), _ptr(b),
                                           _ptr(o), _ptr(pages), _ptr(status), _stream(stream)),
            "gdn_spec_verify")
+
+
+def gdn_spec_step(dims, batch, params, x, conv_w, a, b, o, pages, status, stream=None):
+    _check(load_library().gdn_spec_step(ctypes.byref(dims), ctypes.byref(batch),
+                                        ctypes.byref(params), _ptr(x), _ptr(conv_w), _ptr(a),
+                                        _ptr(b), _ptr(o), _ptr(pages), _ptr(status),
+                                        _stream(stream)), "gdn_spec_step")
 
 
 def gdn_spec_slots(dims, batch, params, x, conv_w, y, a, b, o, slots, status, stream=None):

@@ -10,6 +10,7 @@
 
 #include "gdn.h"
 #include "kernels.h"
+#include "spec.cuh"
 #include "umma.cuh"
 
 namespace gdn {
@@ -150,34 +151,90 @@ Params make_params(const gdn_params* p, const gdn_dims* d) {
   return P;
 }
 
-cudaError_t rule(int mode, const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
-                 const gdn_dims* d, const void* qkv, const void* a, const void* b, void* o,
-                 void* pages, int32_t* status, cudaStream_t s) {
+cudaError_t rule(const Geom& G, const Batch& B, const Params& P, const gdn_dims* d,
+                 const void* qkv, const void* a, const void* b, void* o, void* pages,
+                 int32_t* status, cudaStream_t s) {
   const int io = d->io_dtype == GDN_BF16, st = d->state_dtype == GDN_BF16,
             of = d->out_dtype == GDN_F32;
   switch (d->head_k_dim) {
-    case 32: return launch_rule_d32(mode, G, B, P, SG, io, st, of, qkv, a, b, o, pages, status, s);
-    case 64: return launch_rule_d64(mode, G, B, P, SG, io, st, of, qkv, a, b, o, pages, status, s);
-    default: return launch_rule_d128(mode, G, B, P, SG, io, st, of, qkv, a, b, o, pages, status, s);
+    case 32: return launch_rule_d32(G, B, P, io, st, of, qkv, a, b, o, pages, status, s);
+    case 64: return launch_rule_d64(G, B, P, io, st, of, qkv, a, b, o, pages, status, s);
+    default: return launch_rule_d128(G, B, P, io, st, of, qkv, a, b, o, pages, status, s);
   }
 }
 
-gdn_status rule_entry(int mode, const gdn_dims* dims, const gdn_batch* batch,
-                      const gdn_params* params, const void* qkv, const void* a, const void* b,
-                      void* o, void* pages, int32_t* status, gdn_stream_t stream) {
+// SMs of the current device (looked up once per device).
+int device_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev < 0 || dev >= 64) return 152;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
+// CTAs per (request, q/k head) for the closed-form spec kernel: one unless
+// the batch would leave SMs idle; then the group's items are split in halves
+// (as long as they divide evenly) until there are two CTAs per SM.
+int spec_splits(const gdn_dims* d, int R, int mode) {
+  if (mode == SPEC_FUSED) return 1;
+  const int Gh = d->num_v_heads / d->num_k_heads;
+  const int bvi = d->head_v_dim < kSpecBV ? d->head_v_dim : kSpecBV;
+  const int items = Gh * (d->head_v_dim / bvi);
+  const long long ctas = (long long)d->num_k_heads * R;
+  const long long want = 2LL * device_sms();
+  int s = 1;
+  while (ctas * s < want && items % (2 * s) == 0) s *= 2;
+  return s;
+}
+
+// The shared memory the spec kernel needs fits (else the shape is not
+// supported: a very wide group of value heads).
+bool spec_fits(const gdn_dims* d) {
+  const int Gh = d->num_v_heads / d->num_k_heads;
+  const SpecSmem L = spec_smem(d->head_k_dim, d->head_v_dim, Gh, (int)dsize(d->io_dtype),
+                               (int)dsize(d->state_dtype));
+  return (int)L.total <= kSpecSmemMax;
+}
+
+cudaError_t spec(int mode, const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
+                 const gdn_dims* d, const void* rows, const void* conv_w, const void* a,
+                 const void* b, void* o, void* pages, int32_t* status, cudaStream_t s) {
+  const int io = d->io_dtype == GDN_BF16, st = d->state_dtype == GDN_BF16,
+            of = d->out_dtype == GDN_F32;
+  const int splits = spec_splits(d, B.R, mode);
+  switch (d->head_k_dim) {
+    case 32:
+      return launch_spec_d32(mode, G, B, P, SG, io, st, of, rows, conv_w, a, b, o, pages, status,
+                             splits, s);
+    case 64:
+      return launch_spec_d64(mode, G, B, P, SG, io, st, of, rows, conv_w, a, b, o, pages, status,
+                             splits, s);
+    default:
+      return launch_spec_d128(mode, G, B, P, SG, io, st, of, rows, conv_w, a, b, o, pages, status,
+                              splits, s);
+  }
+}
+
+gdn_status seq_entry(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                     const void* qkv, const void* a, const void* b, void* o, void* pages,
+                     int32_t* status, gdn_stream_t stream) {
   gdn_status e = check_dims(dims);
   if (e != GDN_OK) return e;
-  if ((e = check_batch(batch, mode == 0)) != GDN_OK) return e;
+  if ((e = check_batch(batch, true)) != GDN_OK) return e;
   if ((e = check_params(params, true)) != GDN_OK) return e;
-  if (mode == 1 && dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
   if (batch->num_requests == 0) return GDN_OK;
   if (!status || !pages) return GDN_ERR_INVALID_ARG;
   if (batch->num_rows > 0 && (!qkv || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
   const Geom G = make_geom(dims);
   const Batch B = make_batch(batch);
   const Params P = make_params(params, dims);
-  SlotGeom SG{};
-  if (rule(mode, G, B, P, SG, dims, qkv, a, b, o, pages, status, (cudaStream_t)stream) != cudaSuccess)
+  if (rule(G, B, P, dims, qkv, a, b, o, pages, status, (cudaStream_t)stream) != cudaSuccess)
     return GDN_ERR_LAUNCH;
   return GDN_OK;
 }
@@ -262,13 +319,51 @@ gdn_status gdn_conv(const gdn_dims* dims, const gdn_batch* batch, const gdn_para
 gdn_status gdn_seq(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
                    const void* qkv, const void* a, const void* b, void* o, void* pages,
                    int32_t* status, gdn_stream_t stream) {
-  return rule_entry(0, dims, batch, params, qkv, a, b, o, pages, status, stream);
+  return seq_entry(dims, batch, params, qkv, a, b, o, pages, status, stream);
 }
 
 gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
                            const void* qkv, const void* a, const void* b, void* o, void* pages,
                            int32_t* status, gdn_stream_t stream) {
-  return rule_entry(1, dims, batch, params, qkv, a, b, o, pages, status, stream);
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, false)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
+  if (!spec_fits(dims)) return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!qkv || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  SlotGeom SG{};
+  if (spec(SPEC_VERIFY, G, B, P, SG, dims, qkv, nullptr, a, b, o, pages, status,
+           (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
+gdn_status gdn_spec_step(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
+                         const void* x, const void* conv_w, const void* a, const void* b, void* o,
+                         void* pages, int32_t* status, gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, false)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
+  if (!spec_fits(dims)) return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages || !conv_w) return GDN_ERR_INVALID_ARG;
+  if (batch->num_rows > 0 && (!x || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  SlotGeom SG{};
+  if (spec(SPEC_FUSED, G, B, P, SG, dims, x, conv_w, a, b, o, pages, status,
+           (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
 }
 
 gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
@@ -279,6 +374,7 @@ gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gd
   if ((e = check_batch(batch, false)) != GDN_OK) return e;
   if ((e = check_params(params, true)) != GDN_OK) return e;
   if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
+  if (!spec_fits(dims)) return GDN_ERR_UNSUPPORTED;
   if (batch->num_requests == 0) return GDN_OK;
   if (!status || !slots || !conv_w) return GDN_ERR_INVALID_ARG;
   if (batch->num_rows > 0 && (!x || !y || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
@@ -292,7 +388,8 @@ gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gd
   const int io = dims->io_dtype == GDN_BF16;
   if (launch_conv_slots(G, B, P, SG, io, x, conv_w, y, slots, status, s) != cudaSuccess)
     return GDN_ERR_LAUNCH;
-  if (rule(2, G, B, P, SG, dims, y, a, b, o, slots, status, s) != cudaSuccess) return GDN_ERR_LAUNCH;
+  if (spec(SPEC_SLOTS, G, B, P, SG, dims, y, nullptr, a, b, o, slots, status, s) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
   return GDN_OK;
 }
 
@@ -346,9 +443,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_p
   }
   Batch Bs = make_batch(batch);
   if (any_long) Bs.max_len = threshold - 1;
-  SlotGeom SG{};
-  if (rule(0, G, Bs, P, SG, dims, qkv, a, b, o, pages, status, s) != cudaSuccess)
-    return GDN_ERR_LAUNCH;
+  if (rule(G, Bs, P, dims, qkv, a, b, o, pages, status, s) != cudaSuccess) return GDN_ERR_LAUNCH;
   if (!any_long) return GDN_OK;
   Batch Bc = make_batch(batch);
   Bc.min_len = threshold;

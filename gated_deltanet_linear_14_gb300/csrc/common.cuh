@@ -191,6 +191,12 @@ __device__ __forceinline__ void store_f(T* p, const float* in) {
   }
 }
 
+// One output value, fp32 or bf16 (round to nearest even).
+__device__ __forceinline__ void store_out(void* o, int out_f32, size_t off, float v) {
+  if (out_f32) reinterpret_cast<float*>(o)[off] = v;
+  else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
+}
+
 // Round-trip through the storage type (what a store followed by a load
 // returns).
 template <class T>

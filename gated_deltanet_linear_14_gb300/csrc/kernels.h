@@ -15,12 +15,6 @@ cudaError_t launch_conv_slots(const Geom& G, const Batch& B, const Params& P, co
                               int io_bf16, const void* x, const void* w, void* y, void* slots,
                               int32_t* status, cudaStream_t stream);
 
-// mode: 0 = token-by-token rule (plain requests), 1 = one-page verify (SPEC
-// requests), 2 = slot-per-candidate layout (every request).
-cudaError_t launch_rule(int mode, const Geom& G, const Batch& B, const Params& P,
-                        const SlotGeom& SG, int io_bf16, int state_bf16, int out_f32,
-                        const void* qkv, const void* a, const void* b, void* o, void* pages,
-                        int32_t* status, cudaStream_t stream);
 
 // Chunked prefill on the tensor cores; tmap points to the CUtensorMap of
 // the packed qkv rows ([num_rows][C] bf16, box 64 x 64, 128B swizzle).
@@ -34,15 +28,30 @@ cudaError_t launch_decode(const Geom& G, const Batch& B, const Params& P, int io
                           const void* b, void* o, void* pages, int32_t* status,
                           cudaStream_t stream);
 
-// per head dimension (one translation unit each)
-cudaError_t launch_rule_d32(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
-                            int, int, int, const void*, const void*, const void*, void*, void*,
-                            int32_t*, cudaStream_t);
-cudaError_t launch_rule_d64(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
-                            int, int, int, const void*, const void*, const void*, void*, void*,
-                            int32_t*, cudaStream_t);
-cudaError_t launch_rule_d128(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
-                             int, int, int, const void*, const void*, const void*, void*, void*,
-                             int32_t*, cudaStream_t);
+// Speculative decode in closed form (spec.cuh). mode: 0 = one-page verify
+// (rows = conv'd qkv), 1 = the same with the conv fused in (rows = raw x),
+// 2 = slot-per-candidate layout (rows = conv'd qkv, pages = slot pools).
+// splits: CTAs per (request, q/k head) (1 for mode 1).
+cudaError_t launch_spec_d32(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
+                            int, int, int, const void*, const void*, const void*, const void*,
+                            void*, void*, int32_t*, int, cudaStream_t);
+cudaError_t launch_spec_d64(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
+                            int, int, int, const void*, const void*, const void*, const void*,
+                            void*, void*, int32_t*, int, cudaStream_t);
+cudaError_t launch_spec_d128(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
+                             int, int, int, const void*, const void*, const void*, const void*,
+                             void*, void*, int32_t*, int, cudaStream_t);
+
+// Token-by-token rule (rule.cuh) for the plain requests of a batch, per head
+// dimension (one translation unit each).
+cudaError_t launch_rule_d32(const Geom&, const Batch&, const Params&, int io_bf16, int state_bf16,
+                            int out_f32, const void* qkv, const void* a, const void* b, void* o,
+                            void* pages, int32_t* status, cudaStream_t);
+cudaError_t launch_rule_d64(const Geom&, const Batch&, const Params&, int io_bf16, int state_bf16,
+                            int out_f32, const void* qkv, const void* a, const void* b, void* o,
+                            void* pages, int32_t* status, cudaStream_t);
+cudaError_t launch_rule_d128(const Geom&, const Batch&, const Params&, int io_bf16, int state_bf16,
+                             int out_f32, const void* qkv, const void* a, const void* b, void* o,
+                             void* pages, int32_t* status, cudaStream_t);
 
 }  // namespace gdn

@@ -1,12 +1,9 @@
-// Token-by-token gated delta rule: gdn_seq, gdn_spec_verify and the
-// slot-per-candidate layout, plus the staging and token step that the fused
-// decode (decode.cu) runs too (sm_103a).
+// Token-by-token gated delta rule (gdn_seq), plus the staging and token step
+// that the fused decode (decode.cu) runs too (sm_103a).
 //
 // r9700-stack v0.2.3, section 1 (r9k_gdn_seq: any number of tokens, the state
-// in registers, the batch's own rows); v0.2.4, "What it does" (one page per
-// request: replay the accepted rows from the record, checkpoint, run the
-// candidates; bit-identical to the slot design); vllm.cpp PR #155 (q/k L2
-// norm and gates fused per token).
+// in registers, the batch's own rows); vllm.cpp PR #155 (q/k L2 norm and
+// gates fused per token).
 //
 // Work decomposition. One CTA = (request, value head h, block of BV = 32
 // value columns); 4 warps of 8 columns; inside a warp 4 column groups of 8
@@ -26,16 +23,13 @@
 // which is the rule S <- alpha S; u = beta (v - S^T k^); S <- S + k^ u^T;
 // o = scale S^T q^ with the decay folded into the dot products, so S is read
 // once and written once per token. All arithmetic is explicit
-// round-to-nearest intrinsics and the three modes share this code path (the
-// verify's replayed rows skip only the output half), so the one-page verify
-// is bit-identical to the slot layout.
+// round-to-nearest intrinsics, so the fused decode, which runs the same
+// staging and step, is bit-identical to gdn_conv followed by gdn_seq.
 #pragma once
 
 #include "common.cuh"
 
 namespace gdn {
-
-enum RuleMode { MODE_SEQ = 0, MODE_VERIFY = 1, MODE_SLOTS = 2 };
 
 constexpr int kRuleWarps = 4;
 constexpr int kRuleThreads = kRuleWarps * 32;
@@ -276,52 +270,6 @@ __device__ __forceinline__ float token_step_rows(LaneState<DK / 8>& S, const flo
   return o;
 }
 
-// A token that only advances the state (no output), for rows replayed from
-// a record. Its S^T k^ sums pair the lanes exactly as token_step_rows does
-// (lane bit 2, then bit 1, then bit 0; fp32 addition is commutative), so the
-// state it leaves is bit-identical, without the S^T q^ half of the work.
-template <int DK, class ST>
-__device__ __forceinline__ void token_update_rows(LaneState<DK / 8>& S, const float* krow,
-                                                  const float* vrow, float alpha, float beta,
-                                                  int r8, int vcol) {
-  using L = LaneMap<DK, ST>;
-  constexpr int E = DK / 8;
-  float2 k2[E / 2];
-#pragma unroll
-  for (int i = 0; i < L::NI; ++i) {
-#pragma unroll
-    for (int e = 0; e < L::VEC; e += 4) {
-      const float4 kv = *reinterpret_cast<const float4*>(&krow[stage_pos<DK, ST>(L::idx(r8, i) + e)]);
-      k2[(i * L::VEC + e) / 2] = make_float2(kv.x, kv.y);
-      k2[(i * L::VEC + e) / 2 + 1] = make_float2(kv.z, kv.w);
-    }
-  }
-  const float2 vv = *reinterpret_cast<const float2*>(&vrow[vcol]);
-  float2 ak0 = make_float2(0.f, 0.f), ak1 = ak0;
-#pragma unroll
-  for (int j = 0; j < E / 2; ++j) {
-    ak0 = __ffma2_rn(S.s[0][j], k2[j], ak0);
-    ak1 = __ffma2_rn(S.s[1][j], k2[j], ak1);
-  }
-  const float v0 = __fadd_rn(ak0.x, ak0.y), v2 = __fadd_rn(ak1.x, ak1.y);
-  const bool b2 = (r8 & 4) != 0;
-  // lanes with bit 2 = m reduce column m
-  float sk = __fadd_rn(b2 ? v2 : v0, __shfl_xor_sync(0xffffffffu, b2 ? v0 : v2, 4));
-  sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, 2));
-  sk = __fadd_rn(sk, __shfl_xor_sync(0xffffffffu, sk, 1));
-  const float vm = b2 ? vv.y : vv.x;
-  const float u = __fmul_rn(beta, __fsub_rn(vm, __fmul_rn(alpha, sk)));
-  const float u_x = __shfl_xor_sync(0xffffffffu, u, 4);
-  const float u0 = b2 ? u_x : u, u1 = b2 ? u : u_x;
-  const float2 al = make_float2(alpha, alpha);
-  const float2 uu0 = make_float2(u0, u0), uu1 = make_float2(u1, u1);
-#pragma unroll
-  for (int j = 0; j < E / 2; ++j) {
-    S.s[0][j] = __ffma2_rn(k2[j], uu0, __fmul2_rn(al, S.s[0][j]));
-    S.s[1][j] = __ffma2_rn(k2[j], uu1, __fmul2_rn(al, S.s[1][j]));
-  }
-}
-
 template <int DK, class ST>
 __device__ __forceinline__ float token_step(LaneState<DK / 8>& S, const Stage<DK>& st, int t, int r8,
                                             int vcol, float scale, bool update) {
@@ -358,11 +306,6 @@ __device__ __forceinline__ void zero_state(LaneState<E>& S) {
   for (int m = 0; m < kColsPerLane; ++m)
 #pragma unroll
     for (int j = 0; j < E / 2; ++j) S.s[m][j] = make_float2(0.f, 0.f);
-}
-
-__device__ __forceinline__ void store_out(void* o, int out_f32, size_t off, float v) {
-  if (out_f32) reinterpret_cast<float*>(o)[off] = v;
-  else reinterpret_cast<bf16*>(o)[off] = __float2bfloat16_rn(v);
 }
 
 // Run n rows from `src` through the rule. Outputs go to o rows starting at
@@ -408,16 +351,13 @@ struct NoAfter {
   __device__ void operator()(int) const {}
 };
 
-// Residency targets: the verify mode keeps its token steps short (at most
-// 2 Kc rows, staged once), so it trades registers for 6 CTAs (24 warps) per
-// SM (5, 7 and 8 measured slower; 7 and 8 force spills); the other modes ask for 4, which keeps them near 120 registers (left
-// free, the compiler went past 150 and a long prefill's per-token chain
-// measured a quarter slower).
-template <class IO, class ST, int DK, int MODE>
-__global__ void __launch_bounds__(kRuleThreads, MODE == MODE_VERIFY ? 6 : 4)
-rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
-            const IO* __restrict__ a_in, const IO* __restrict__ b_in, void* o, int out_f32,
-            void* pages, int32_t* status) {
+// 4 CTAs per SM keep the token-by-token kernel near 120 registers (left free,
+// the compiler went past 150 and a long prefill's per-token chain measured a
+// quarter slower).
+template <class IO, class ST, int DK>
+__global__ void __launch_bounds__(kRuleThreads, 4)
+rule_kernel(Geom G, Batch B, Params P, const IO* __restrict__ qkv, const IO* __restrict__ a_in,
+            const IO* __restrict__ b_in, void* o, int out_f32, void* pages, int32_t* status) {
   pdl_begin();
   constexpr int E = DK / 8;
   __shared__ __align__(16) Stage<DK> st;
@@ -431,9 +371,8 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
     if (reporter) report(status, q.err);
     return;
   }
-  if (MODE == MODE_SEQ && q.spec) return;
-  if (MODE == MODE_SEQ && (q.len < B.min_len || q.len > B.max_len)) return;
-  if (MODE == MODE_VERIFY && !q.spec) return;
+  if (q.spec) return;
+  if (q.len < B.min_len || q.len > B.max_len) return;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cg = lane >> 3, r8 = lane & 7;
@@ -450,149 +389,41 @@ rule_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ qkv,
   rows_in.b = b_in + (size_t)q.start * G.Hv + h;
   rows_in.ab_stride = G.Hv;
 
-  if constexpr (MODE == MODE_SEQ) {
-    char* pg = page_ptr(G, pages, q.page);
-    uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
-    if (!q.fresh && q.len == 0) return;  // nothing to do
-    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
-    // the state load is issued before the flag check (one round trip, not
-    // two); a refused request only discards it
-    if (q.fresh) zero_state<E>(S);
-    else load_state<DK, ST>(S, Sb, col, r8);
-    if (!q.fresh && flag_width(*flagp) != 0) {
-      if (reporter) report(status, GDN_DEV_RECORD_OPEN);
-      return;
-    }
-    run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P, true,
-                         NoAfter());
-    store_state<DK, ST>(Sb, S, col, r8);
-    if (q.fresh && blockIdx.x == 0 && threadIdx.x == 0) *flagp = 0u;  // empty record
-  } else if constexpr (MODE == MODE_VERIFY) {
-    char* pg = page_ptr(G, pages, q.page);
-    uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
-    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
-    ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
-    IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
-    // the state load is issued before the flag is checked (one round trip,
-    // not two); a refused request only discards it
-    load_state<DK, ST>(S, Sb, col, r8);
-    SpecState ss = spec_state(G, B, q, flag);
-    if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
-    if (ss.err) {
-      if (reporter) report(status, ss.err);
-      return;
-    }
-    // Rows 0..a of the live record slot (the replay) and this step's
-    // candidates are at most 2 Kc <= kTC rows: stage them together, once.
-    const int n_rep = (ss.width > 0) ? ss.accepted + 1 : 0;
-    const int n_all = n_rep + q.len;
-    {
-      const int ft = threadIdx.x >> 3, fp = threadIdx.x & 7;
-      Fetch<DK, IO> f;
-      RowSrc<IO> src;
-      int tt = ft;
-      if (ft < n_rep) {
-        src.rows = rec + (size_t)ss.live * G.Kc * G.rec_row;
-        src.row_stride = G.rec_row;
-        src.a = src.rows + G.C + h;
-        src.b = src.rows + G.C + G.Hv + h;
-        src.ab_stride = G.rec_row;
-      } else {
-        src = rows_in;
-        tt = ft - n_rep;
-      }
-      fetch<DK, IO>(f, src, tt, ft < n_all ? tt + 1 : 0, fp, kh, h, cb, G);
-      publish<DK, IO, ST>(st, f, ft, n_all, fp, h, P);
-    }
-    __syncthreads();
-    const int vcol = warp * 8 + cg * 2;
-    for (int t = 0; t < n_rep; ++t)
-      token_update_rows<DK, ST>(S, st.k[t], st.v[t], st.sc[t].x, st.sc[t].y, r8, vcol);
-    if (n_rep > 0) {
-      store_state<DK, ST>(Sb, S, col, r8);
-      // continue from exactly what was stored (a bf16 page rounds here)
-#pragma unroll
-      for (int m = 0; m < kColsPerLane; ++m)
-#pragma unroll
-        for (int j = 0; j < E / 2; ++j)
-          S.s[m][j] = make_float2(through<ST>(S.s[m][j].x), through<ST>(S.s[m][j].y));
-    }
-    // this step's candidates: outputs only, no per-candidate state
-    for (int t = 0; t < q.len; ++t) {
-      const float ov = token_step<DK, ST>(S, st, n_rep + t, r8, vcol, P.scale, t + 1 < q.len);
-      if ((r8 & 3) == 0) {
-        const size_t off = (((size_t)q.start + t) * G.Hv + h) * G.Dv + cb * kBV + vcol + (r8 >> 2);
-        store_out(o, out_f32, off, ov);
-      }
-    }
-    // the candidates' gates go next to their conv'd rows in the other slot
-    if (cb == 0 && threadIdx.x < q.len) {
-      IO* row = rec + ((size_t)(1 - ss.live) * G.Kc + threadIdx.x) * G.rec_row;
-      const size_t rn = (size_t)q.start + threadIdx.x;
-      row[G.C + h] = a_in[rn * G.Hv + h];
-      row[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
-    }
-    // The last CTA of this request publishes the new flag word. No fence
-    // orders the page data first: only later launches read it. The counter
-    // needs none either: every CTA read the flag at its start, before its
-    // own increment of the same word, so the publish follows every read.
-    if (threadIdx.x == 0) {
-      const uint32_t total = (uint32_t)(G.Hv * nCB);
-      const uint32_t old = atomicAdd(flagp, 256u);
-      if ((old >> 8) == total - 1) {
-        const int live = (q.len > 0) ? 1 - ss.live : ss.live;
-        atomicExch(flagp, make_flag(live, 1 - ss.parity, q.len));
-      }
-    }
-  } else {  // MODE_SLOTS
-    const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
-    if (src < 0 || src >= G.Kc) {
-      if (reporter) report(status, GDN_DEV_BAD_ACCEPTED);
-      return;
-    }
-    if (q.len > G.Kc) {
-      if (reporter) report(status, GDN_DEV_TOO_MANY_CANDIDATES);
-      return;
-    }
-    char* pool = reinterpret_cast<char*>(pages) + (size_t)q.page * SG.pool_bytes;
-    const size_t slot_bytes = SG.slot_bytes, state_off = SG.state_off;
-    const size_t head_off = (size_t)h * G.Dv * DK;
-    load_state<DK, ST>(S, reinterpret_cast<ST*>(pool + (size_t)src * slot_bytes + state_off) + head_off,
-                       col, r8);
-    // store after every candidate: the same kernel instance stores rows in
-    // order, so a slot is written by the CTA that owns its columns only
-    auto keep = [&](int i) {
-      store_state<DK, ST>(reinterpret_cast<ST*>(pool + (size_t)i * slot_bytes + state_off) + head_off,
-                          S, col, r8);
-    };
-    run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P, true,
-                         keep);
+  char* pg = page_ptr(G, pages, q.page);
+  uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+  if (!q.fresh && q.len == 0) return;  // nothing to do
+  ST* Sb = reinterpret_cast<ST*>(pg + G.state_off) + (size_t)h * G.Dv * DK;
+  // the state load is issued before the flag check (one round trip, not
+  // two); a refused request only discards it
+  if (q.fresh) zero_state<E>(S);
+  else load_state<DK, ST>(S, Sb, col, r8);
+  if (!q.fresh && flag_width(*flagp) != 0) {
+    if (reporter) report(status, GDN_DEV_RECORD_OPEN);
+    return;
   }
+  run_rows<DK, IO, ST>(S, st, rows_in, q.len, o, out_f32, (size_t)q.start, h, cb, kh, G, P, true,
+                       NoAfter());
+  store_state<DK, ST>(Sb, S, col, r8);
+  if (q.fresh && blockIdx.x == 0 && threadIdx.x == 0) *flagp = 0u;  // empty record
 }
 
 template <int DK>
-cudaError_t launch_rule_dk(int mode, const Geom& G, const Batch& B, const Params& P,
-                           const SlotGeom& SG, int io_bf16, int state_bf16, int out_f32,
-                           const void* qkv, const void* a, const void* b, void* o, void* pages,
-                           int32_t* status, cudaStream_t stream) {
+cudaError_t launch_rule_dk(const Geom& G, const Batch& B, const Params& P, int io_bf16,
+                           int state_bf16, int out_f32, const void* qkv, const void* a,
+                           const void* b, void* o, void* pages, int32_t* status,
+                           cudaStream_t stream) {
   dim3 grid(G.Hv * (G.Dv / kBV), B.R);
   dim3 block(kRuleThreads);
-#define GDN_RULE_LAUNCH(IO, ST, MODE)                                                         \
-  return launch_pdl(rule_kernel<IO, ST, DK, MODE>, grid, block, 0, stream, G, B, P, SG,       \
-                    static_cast<const IO*>(qkv), static_cast<const IO*>(a),                   \
+#define GDN_RULE_LAUNCH(IO, ST)                                                              \
+  return launch_pdl(rule_kernel<IO, ST, DK>, grid, block, 0, stream, G, B, P,               \
+                    static_cast<const IO*>(qkv), static_cast<const IO*>(a),                 \
                     static_cast<const IO*>(b), o, out_f32, pages, status)
-#define GDN_RULE_MODES(IO, ST)                       \
-  if (mode == MODE_SEQ) GDN_RULE_LAUNCH(IO, ST, MODE_SEQ);          \
-  else if (mode == MODE_VERIFY) GDN_RULE_LAUNCH(IO, ST, MODE_VERIFY); \
-  else GDN_RULE_LAUNCH(IO, ST, MODE_SLOTS);
   if (io_bf16) {
-    if (state_bf16) { GDN_RULE_MODES(bf16, bf16) } else { GDN_RULE_MODES(bf16, float) }
+    if (state_bf16) GDN_RULE_LAUNCH(bf16, bf16); else GDN_RULE_LAUNCH(bf16, float);
   } else {
-    if (state_bf16) { GDN_RULE_MODES(float, bf16) } else { GDN_RULE_MODES(float, float) }
+    if (state_bf16) GDN_RULE_LAUNCH(float, bf16); else GDN_RULE_LAUNCH(float, float);
   }
-#undef GDN_RULE_MODES
 #undef GDN_RULE_LAUNCH
-  return cudaGetLastError();
 }
 
 }  // namespace gdn

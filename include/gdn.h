@@ -245,11 +245,39 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch,
  *   5. the last block to finish sets L <- 1-L (if row_len > 0), n <-
  *      row_len, P <- 1-P, counter <- 0.
  * row_len == 0 is the commit: replay, checkpoint, close the record.
- * Arguments as gdn_seq. Bit-identical to gdn_spec_slots on the same rows. */
+ * Arguments as gdn_seq. Bit-identical to gdn_spec_slots on the same rows.
+ * Each run of rows (the replay, then the candidates) is evaluated in closed
+ * form from the state it starts at: with decay products R[t][s] =
+ * e^{g_{s+1}} ... e^{g_t} and G_t = e^{g_0} ... e^{g_t},
+ *   u_t = beta_t (v_t - G_t S^T k^_t - sum_{s<t} R[t][s] (k^_s.k^_t) u_s),
+ *   o_t = scale (G_t S^T q^_t + sum_{s<=t} R[t][s] (k^_s.q^_t) u_s),
+ *   checkpoint S_a = G_a S + sum_{s<=a} R[a][s] k^_s u_s^T,
+ * which equals the token-by-token rule in exact arithmetic. Returns
+ * GDN_ERR_UNSUPPORTED when a q/k head's group of value heads is too wide for
+ * the kernel's shared memory (about (Hv/Hk) Dv > 4000 at bf16 rows). */
 gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch,
                            const gdn_params* params, const void* qkv,
                            const void* a, const void* b, void* o, void* pages,
                            int32_t* status, gdn_stream_t stream);
+
+/* Fused speculative step: gdn_conv (io-dtype output) followed by
+ * gdn_spec_verify for the SPEC requests of the batch, in one launch, with the
+ * same results bit for bit (outputs, states, conv windows, record slots and
+ * flag words; the conv'd rows are written only into the record, as the next
+ * step's replay needs them). Plain requests are skipped. This is the one
+ * launch per layer step that the r9700-stack v0.2.3 notes (section 1) credit
+ * for the short-step speed-up, applied to the verify of v0.2.4 ("What it
+ * does"): per (request, q/k head) one CTA convolves the group's q, k and v
+ * channels for this step's candidates, rolls the window by the accepted
+ * count, replays, checkpoints and runs the candidates.
+ *   x       device [num_rows][C] io dtype (raw conv inputs, candidate rows)
+ *   conv_w  device [C][W];  a, b, o, pages, status as gdn_spec_verify.
+ * Returns GDN_ERR_UNSUPPORTED where gdn_spec_verify does. */
+gdn_status gdn_spec_step(const gdn_dims* dims, const gdn_batch* batch,
+                         const gdn_params* params, const void* x,
+                         const void* conv_w, const void* a, const void* b,
+                         void* o, void* pages, int32_t* status,
+                         gdn_stream_t stream);
 
 /* Slot-per-candidate speculative decode: the stock layout the one-page
  * verify replaces (r9700-stack v0.2.4, "What it does": a state page per
