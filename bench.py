@@ -494,28 +494,61 @@ def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
         if ev is not None:
             ev[2].record()
 
+    def launch_fused(i, ev=None):
+        p = i % pools
+        B = batches[(steps_done[p] % 2, i % 8)]
+        steps_done[p] += 1
+        if ev is not None:
+            ev[0].record()
+        gdn.gdn_spec_step(dims, B, params, x, conv_w, a, b, o, pl[p].buf, status)
+        if ev is not None:
+            ev[1].record()
+
     for i in range(W):
         launch(i)
     torch.cuda.synchronize()
     evs = [_events(torch, 3) for _ in range(K)]
     el = time_steps(lambda i: launch(W + i, evs[i]), K, torch)
+    # the same steps as one launch each (conv fused into the verify); the
+    # pools' parities carry on from the two-launch steps
+    for i in range(W):
+        launch_fused(W + K + i)
+    torch.cuda.synchronize()
+    evf = [_events(torch, 2) for _ in range(K)]
+    el_f = time_steps(lambda i: launch_fused(2 * W + K + i, evf[i]), K, torch)
+    el_f_plain = time_steps(lambda i: launch_fused(2 * W + 2 * K + i), K, torch)
     code = int(status.item())
     ver_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    fused_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evf)
     ssz = 4 if state == "f32" else 2
     state_bytes = 2 * R * sh.Hv * sh.Dk * sh.Dv * ssz
     mean_acc = float(np.mean(accs)) + 1.0
     rec_row = (sh.C + 2 * sh.Hv) * 2
+    # verify: replayed record rows read, candidate rows and gates read, their
+    # gates written to the record, outputs written
     other = int(R * mean_acc * rec_row + T * (sh.C + 2 * sh.Hv) * 2 + T * sh.Hv * sh.Dv * 2)
+    # the fused step also reads the raw rows instead of conv'd ones (same
+    # size), writes the conv'd rows into the record, and reads the W-1 history
+    # columns and writes W-1+8 window columns
+    fused_other = other + T * sh.C * 2 + R * (sh.W - 1 + sh.W - 1 + n) * sh.C * 2
     flops = R * sh.Hv * sh.Dk * sh.Dv * (mean_acc + n) * 7
     gbs = (state_bytes + other) / (ver_ms / 1e3) / 1e9
+    f_gbs = (state_bytes + fused_other) / (el_f_plain / K) / 1e9
     return {"workload": f"spec verify: {R} pages, 1+7 candidates, {state} state, conv + verify",
             "ms_per_step": el / K * 1e3, "verify_ms": ver_ms, "conv_ms": conv_ms,
             "tokens_per_s": T * K / el, "verify_gbs": gbs,
+            "verify_bytes": state_bytes + other,
             "verify_frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
             "verify_tflops_fp32": flops / (ver_ms / 1e3) / 1e12,
             "verify_frac_of_fp32": flops / (ver_ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS,
-            "fp32_peak_tflops": FP32_PEAK_TFLOPS, "status": code}
+            "fp32_peak_tflops": FP32_PEAK_TFLOPS,
+            "fused_step": {"entry": "gdn_spec_step (conv + verify, one launch)",
+                           "ms_per_step": el_f_plain / K * 1e3,
+                           "ms_per_step_event_bracketed": fused_ms,
+                           "tokens_per_s": T * K / el_f_plain, "bytes": state_bytes + fused_other,
+                           "gbs": f_gbs, "frac_of_hbm": f_gbs / float(peaks["hbm_gbs"])},
+            "status": code}
 
 
 def bench_slots(device, peaks, K=20, W=4, pools=2):

@@ -65,7 +65,10 @@ void layout(const gdn_dims* d, gdn_page_layout_t* L, int* rec_row_elems) {
   L->window_offset = align_up(L->state_offset + L->state_bytes, kAlign);
   L->window_bytes = (size_t)(d->conv_width - 1 + d->max_candidates) * C * io;
   L->record_offset = align_up(L->window_offset + L->window_bytes, kAlign);
-  L->record_bytes = 2 * (size_t)d->max_candidates * rec_row * io;
+  // both slots' rows, then both slots' run coefficients (fp32, one block of
+  // kRunCoefBytes per value head and slot)
+  L->record_bytes = 2 * (size_t)d->max_candidates * rec_row * io +
+                    (d->max_candidates > 0 ? 2 * (size_t)d->num_v_heads * kRunCoefBytes : 0);
   L->flag_offset = align_up(L->record_offset + L->record_bytes, kAlign);
   L->page_bytes = align_up(L->flag_offset + sizeof(uint32_t), kAlign);
   if (rec_row_elems) *rec_row_elems = (int)rec_row;
@@ -99,6 +102,7 @@ Geom make_geom(const gdn_dims* d) {
   G.window_off = L.window_offset;
   G.state_off = L.state_offset;
   G.record_off = L.record_offset;
+  G.rcoef_off = L.record_offset + 2 * (size_t)d->max_candidates * rec_row * dsize(d->io_dtype);
   G.flag_off = L.flag_offset;
   return G;
 }
@@ -180,14 +184,14 @@ int device_sms() {
 
 // CTAs per (request, q/k head) for the closed-form spec kernel: one unless
 // the batch would leave SMs idle; then the group's items are split in halves
-// (as long as they divide evenly) until there are two CTAs per SM.
+// (as long as they divide evenly) until there are three CTAs per SM.
 int spec_splits(const gdn_dims* d, int R, int mode) {
   if (mode == SPEC_FUSED) return 1;
   const int Gh = d->num_v_heads / d->num_k_heads;
   const int bvi = d->head_v_dim < kSpecBV ? d->head_v_dim : kSpecBV;
   const int items = Gh * (d->head_v_dim / bvi);
   const long long ctas = (long long)d->num_k_heads * R;
-  const long long want = 2LL * device_sms();
+  const long long want = 3LL * device_sms();
   int s = 1;
   while (ctas * s < want && items % (2 * s) == 0) s *= 2;
   return s;
@@ -277,7 +281,7 @@ gdn_status encode_rows_tmap(CUtensorMap* tm, const void* rows, int num_rows, con
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return (1 << 16) | 0; }
+int32_t gdn_abi_version(void) { return (1 << 16) | 1; }
 
 gdn_status gdn_page_layout(const gdn_dims* dims, gdn_page_layout_t* out) {
   gdn_status e = check_dims(dims);

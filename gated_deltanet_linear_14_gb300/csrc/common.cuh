@@ -19,7 +19,15 @@ struct Geom {
   int C;              // 2*Hk*Dk + Hv*Dv
   int rec_row;        // record row stride in elements (16-byte padded)
   size_t page_bytes, window_off, state_off, record_off, flag_off;
+  size_t rcoef_off;   // the record's run-coefficient blocks ([2][Hv], kRunCoefBytes each)
 };
+
+// Run coefficients of one value head for the rows of one record slot, kept
+// so that the next step's replay need not derive them again: G_t / |k_t|,
+// G_t, R[t][s] / |k_s| and M = (I - L)^-1 diag(beta), fp32, 8 + 8 + 64 + 64
+// values (see spec.cuh).
+constexpr size_t kRunCoefFloats = 8 + 8 + 64 + 64;
+constexpr size_t kRunCoefBytes = kRunCoefFloats * 4;
 
 struct Batch {
   int R, num_rows, max_rows, num_pages;

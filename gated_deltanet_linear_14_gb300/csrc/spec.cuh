@@ -17,28 +17,44 @@
 //   u_t = beta_t (v_t - G_t S^T k^_t - sum_{s<t} R[t][s] (k^_s.k^_t) u_s)
 //   o_t = scale (G_t S^T q^_t + sum_{s<=t} R[t][s] (k^_s.q^_t) u_s)
 //   S_t = G_t S + sum_{s<=t} R[t][s] k^_s u_s^T           (state after row t)
-// so a run costs one read of S for all its dot products, a short scalar
-// recurrence per value column, and (only where a state is kept) one rank-n
-// update. The verify runs two such runs: the replayed rows (state only: the
-// checkpoint is S_a) and the candidates (outputs only). The slot layout runs
-// the candidates and stores every S_t. Both compute each quantity with the
-// same code and in the same order from the same inputs (a replayed row and
-// the candidate row it was are the same bits, its dot products come from the
-// same stored state), so the one-page checkpoint equals the slot that was
-// kept for it, bit for bit, and so do all outputs.
+// The recurrence for u is a unit lower-triangular system in the run's rows:
+// with c_t = v_t - G_t S^T k^_t and L[t][s] = -beta_t R[t][s] (k^_s.k^_t),
+// u = (I - L)^-1 diag(beta) c =: M c, and the outputs are
+// o = scale (G S^T q^ + N c) with N = B M, B[t][s] = R[t][s] (k^_s.q^_t).
+// M and N depend only on the rows (not on S or the value column), so a CTA
+// forms them once per value head; every column then needs only independent
+// short dot products with its c. A run so costs one read of S for all its
+// dot products and (only where a state is kept) one rank-n update. M's
+// leading block is the inverse of L's leading block, so a run of the first
+// a + 1 rows sees exactly the coefficients the longer run had; the record
+// keeps the candidates' G/|k|, G, R/|k| and M beside their rows, and the
+// next step's replay uses them as they are. The verify runs two such runs:
+// the replayed rows (state only: the checkpoint is S_a) and the candidates
+// (outputs only). The slot layout runs the candidates and stores every S_t.
+// Both compute each quantity with the same code and in the same order from
+// the same inputs (a replayed row and the candidate row it was are the same
+// bits, its dot products come from the same stored state), so the one-page
+// checkpoint equals the slot that was kept for it, bit for bit, and so do
+// all outputs.
 //
 // Work decomposition. One CTA per (request, q/k head kh, split): the Hv/Hk
 // value heads that read q/k head kh, in items of 64 value columns; a
 // request's items may be split over several CTAs when the batch alone would
 // not fill the GPU (not with the conv fused in: every CTA of a group reads
 // the q/k window columns that the group's writer rolls, so the fused step
-// runs one CTA per group). A CTA normalises the group's q/k rows, forms their Gram
-// products and the gates once, and derives the run coefficients per head in
-// shared memory. Items then run with no block-wide barrier: 4 warps x 16
-// columns; inside a warp, 8 column pairs x 4 lanes, a lane holding 2 columns
-// x Dk/4 entries of S in registers (16-byte chunks at Dk index
-// VEC (4 i + r4), so a warp's accesses are contiguous per column). The next
-// item's state is loaded into registers while the current one is computed.
+// runs one CTA per group). A CTA stages the group's rows, forms the
+// candidates' Gram products and gates once, and derives their run
+// coefficients per head in shared memory. Items then run with no block-wide
+// barrier: 4 warps x 16 columns; inside a warp, 4 groups of 4 columns x 8
+// lanes, a lane holding 4 columns x Dk/8 entries of S in registers (chunks
+// of 16 bytes at Dk index VEC (8 i + r8)). Each 16-byte shared load of a q/k
+// row by an 8-lane quarter of the warp reads 128 distinct bytes and feeds 4
+// columns. The per-column scalar work (c, u = M c, the outputs) goes through
+// a small per-warp scratch: the dot products land there, then each lane
+// takes one column and half of the rows, which keeps the per-column arrays
+// out of registers (161 of them, 3 CTAs per SM). The next item's state is
+// copied into shared memory by the thread that will read it (cp.async)
+// while the current one is computed.
 #pragma once
 
 #include "common.cuh"
@@ -50,21 +66,35 @@ enum SpecMode { SPEC_VERIFY = 0, SPEC_FUSED = 1, SPEC_SLOTS = 2 };
 constexpr int kSpecThreads = 128;
 constexpr int kSpecBV = 64;   // value columns per item
 constexpr int kSpecK = 8;     // rows in a run at most (max_candidates)
+constexpr int kSpecScr = 3 * kSpecK * 16;   // per-warp scratch floats
 
 template <int DK, class ST>
 struct SpecMap {
-  static constexpr int E = DK / 4;                      // entries per column per lane
+  static constexpr int E = DK / 8;                      // entries per column per lane
   static constexpr int VEC0 = 16 / (int)sizeof(ST);
   static constexpr int VEC = (E < VEC0) ? E : VEC0;     // contiguous entries per chunk
   static constexpr int NI = E / VEC;                    // chunks per column
   static constexpr int P = E / 2;                       // float2 pairs per column
-  __device__ static int idx(int r4, int i) { return VEC * (4 * i + r4); }
+  static constexpr int CB = VEC * (int)sizeof(ST);      // bytes per chunk (8 or 16)
+  __device__ static int idx(int r8, int i) { return VEC * (8 * i + r8); }
+  // where a q/k row keeps the 4 entries a lane multiplies with pair p0 .. p0+1
+  // of chunk i (piece h = 0 .. VEC/4-1): the rows are stored so that the 8
+  // lanes of a quarter-warp read 128 contiguous bytes
+  __device__ static int xoff(int r8, int i, int h) { return 4 * (8 * (VEC / 4) * i + 8 * h + r8); }
 };
 
-// A lane's part of S: 2 columns x E entries, as float2 pairs.
+// Storage position of Dk entry d in a staged q/k row (see SpecMap::xoff).
+template <int DK, class ST>
+__device__ __forceinline__ int spec_xpos(int d) {
+  using M = SpecMap<DK, ST>;
+  const int i = d / (8 * M::VEC), r8 = (d / M::VEC) % 8, e = d % M::VEC;
+  return M::xoff(r8, i, e / 4) + (d % 4);
+}
+
+// A lane's part of S: 4 columns x E entries, as float2 pairs.
 template <int DK>
 struct SpecS {
-  float2 s[2][DK / 8];
+  float2 s[4][DK / 16];
 };
 
 // Coefficients of one run (one value head): see the header comment.
@@ -73,10 +103,19 @@ struct RunCoef {
   float gq[kSpecK];            // G_t / |q_t|
   float gam[kSpecK];           // G_t
   float beta[kSpecK];          // beta_t
-  float aneg[kSpecK][kSpecK];  // -R[t][s] k^_s.k^_t   (s < t)
-  float bco[kSpecK][kSpecK];   //  R[t][s] k^_s.q^_t   (s <= t)
-  float rk[kSpecK][kSpecK];    //  R[t][s] / |k_s|     (s <= t)
+  float l[kSpecK][kSpecK];     // L[t][s] = -beta_t R[t][s] k^_s.k^_t   (s < t)
+  float bco[kSpecK][kSpecK];   // B[t][s] = R[t][s] k^_s.q^_t          (s <= t)
+  float rk[kSpecK][kSpecK];    // R[t][s] / |k_s|                       (s <= t)
+  float m[kSpecK][kSpecK];     // M = (I - L)^-1 diag(beta)             (s <= t)
+  float nq[kSpecK][kSpecK];    // N = B M                               (s <= t)
 };
+
+// The record keeps, per value head, the fields the next step's replay needs
+// (gk, gam, rk, m: kRunCoefFloats values) in this order.
+static_assert(offsetof(RunCoef, gk) == 0 && offsetof(RunCoef, gam) == 64 &&
+                  offsetof(RunCoef, rk) == 640 && offsetof(RunCoef, m) == 896,
+              "record coefficient copy offsets");
+static_assert(kRunCoefFloats == 8 + 8 + 64 + 64, "record coefficient block");
 
 // Raw dot products of a CTA's rows (k_s.k_t with s <= t, k_s.q_t, q_t.q_t).
 struct RunDots {
@@ -96,6 +135,7 @@ struct SpecSmem {
   uint32_t gates;   // [Gh][2 runs][2][Kc] float: alpha, beta
   uint32_t coef;    // RunCoef [Gh][2 runs]
   uint32_t stage;   // [NC][threads] 16-byte chunks: one item's state per thread
+  uint32_t scr;     // per warp: [2 Kc][16] dot products, [Kc][16] u of its columns
   uint32_t total;
   int RW, DKP;
 };
@@ -115,28 +155,31 @@ __host__ __device__ inline SpecSmem spec_smem(int DK, int DV, int Gh, int io_byt
   L.dots = off;  off = spec_al16(off + (uint32_t)sizeof(RunDots));
   L.gates = off; off = spec_al16(off + (uint32_t)(Gh * 2 * 2 * kSpecK * 4));
   L.coef = off;  off = spec_al16(off + (uint32_t)(Gh * 2 * sizeof(RunCoef)));
-  L.stage = off; off = spec_al16(off + (uint32_t)(2 * DK * st_bytes / 4 * kSpecThreads));
+  L.stage = off; off = spec_al16(off + (uint32_t)(DK / 2 * st_bytes * kSpecThreads));
+  L.scr = off;   off = spec_al16(off + (uint32_t)((kSpecThreads / 32) * kSpecScr * 4));
   L.total = off;
   return L;
 }
 
-// A lane's state chunks are 16 bytes each: (column m, chunk i) is chunk
-// c = m NI + i. They are staged in shared memory thread-major (chunk c of
-// thread t at (c threads + t) 16 bytes), so a warp's 16-byte accesses are
-// contiguous, and each thread reads back only what it copied itself: its own
-// cp.async wait is the only synchronisation.
+// A lane's state chunks (column m, chunk i) are c = m NI + i. They are
+// staged in shared memory thread-major (chunk c of thread t at (c threads +
+// t) CB bytes), so a warp's accesses are contiguous, and each thread reads
+// back only what it copied itself: its own cp.async wait is the only
+// synchronisation.
 template <int DK, class ST>
-__device__ __forceinline__ void spec_stage_async(uint8_t* stage, const ST* col0, int r4, int tid) {
+__device__ __forceinline__ void spec_stage_async(uint8_t* stage, const ST* col0, int r8, int tid) {
   using M = SpecMap<DK, ST>;
-  static_assert(M::VEC * sizeof(ST) == 16, "state chunks are 16 bytes");
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+  for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int i = 0; i < M::NI; ++i) {
       const uint32_t dst = (uint32_t)__cvta_generic_to_shared(
-          stage + ((size_t)(m * M::NI + i) * kSpecThreads + tid) * 16);
-      const ST* src = col0 + (size_t)m * DK + M::idx(r4, i);
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+          stage + ((size_t)(m * M::NI + i) * kSpecThreads + tid) * M::CB);
+      const ST* src = col0 + (size_t)m * DK + M::idx(r8, i);
+      if constexpr (M::CB == 16)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+      else
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
     }
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
@@ -149,112 +192,117 @@ template <int DK, class ST>
 __device__ __forceinline__ void spec_unstage(SpecS<DK>& S, const uint8_t* stage, int tid) {
   using M = SpecMap<DK, ST>;
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+  for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int i = 0; i < M::NI; ++i)
       load_f<ST, M::VEC>(reinterpret_cast<const ST*>(
-                             stage + ((size_t)(m * M::NI + i) * kSpecThreads + tid) * 16),
+                             stage + ((size_t)(m * M::NI + i) * kSpecThreads + tid) * M::CB),
                          reinterpret_cast<float*>(&S.s[m][0]) + i * M::VEC);
 }
 
 template <int DK, class ST>
-__device__ __forceinline__ void spec_store(ST* col0, const SpecS<DK>& S, int r4) {
+__device__ __forceinline__ void spec_store(ST* col0, const SpecS<DK>& S, int r8) {
   using M = SpecMap<DK, ST>;
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+  for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int i = 0; i < M::NI; ++i)
-      store_f<ST, M::VEC>(col0 + (size_t)m * DK + M::idx(r4, i),
+      store_f<ST, M::VEC>(col0 + (size_t)m * DK + M::idx(r8, i),
                           reinterpret_cast<const float*>(&S.s[m][0]) + i * M::VEC);
 }
 
-// The complete dot products of the lane's column (column b1 of its pair)
-// with NG rows of X (fp32, rows at x[g]): per-lane partial sums over its
-// entries, then across the 4 lanes of the pair: lane bit 1 first (which also
-// hands each lane its column), then lane bit 0. Every dot product, whichever
-// rows it is grouped with, is summed in this one order.
+// The complete dot products of the lane's column (column 2 b2 + b1 of its
+// group of 4) with NG rows of X (fp32, rows at x[g], stored by spec_xpos):
+// per-lane partial sums over its entries, then across the 8 lanes of the
+// group: lane bit 2 first (it also hands each lane a pair of columns), then
+// bit 1 (one column), then bit 0. Every dot product, whichever rows it is
+// grouped with, is summed in this one order.
 template <int DK, class ST, int NG>
-__device__ __forceinline__ void spec_dots(const SpecS<DK>& S, const float* const (&x)[NG], int r4,
-                                          bool b1, float (&out)[NG]) {
+__device__ __forceinline__ void spec_dots(const SpecS<DK>& S, const float* const (&x)[NG], int r8,
+                                          bool b2, bool b1, float (&out)[NG]) {
   using M = SpecMap<DK, ST>;
-  float2 acc[2][NG];
+  float2 acc[4][NG];
 #pragma unroll
-  for (int g = 0; g < NG; ++g) acc[0][g] = acc[1][g] = make_float2(0.f, 0.f);
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) acc[m][g] = make_float2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < M::NI; ++i)
 #pragma unroll
-    for (int e = 0; e < M::VEC; e += 4) {
-      const int p = (i * M::VEC + e) / 2;
+    for (int h = 0; h < M::VEC / 4; ++h) {
+      const int p = (i * M::VEC + 4 * h) / 2;
+      // the rows' loads first, then every low-half product, then every
+      // high-half one: products into one accumulator are 4 NG apart
+      float4 v[NG];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        const float4 v = *reinterpret_cast<const float4*>(x[g] + M::idx(r4, i) + e);
-        const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
-        acc[0][g] = __ffma2_rn(S.s[0][p], lo, acc[0][g]);
-        acc[1][g] = __ffma2_rn(S.s[1][p], lo, acc[1][g]);
-        acc[0][g] = __ffma2_rn(S.s[0][p + 1], hi, acc[0][g]);
-        acc[1][g] = __ffma2_rn(S.s[1][p + 1], hi, acc[1][g]);
-      }
+      for (int g = 0; g < NG; ++g) v[g] = *reinterpret_cast<const float4*>(x[g] + M::xoff(r8, i, h));
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          acc[m][g] = __ffma2_rn(S.s[m][p], make_float2(v[g].x, v[g].y), acc[m][g]);
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          acc[m][g] = __ffma2_rn(S.s[m][p + 1], make_float2(v[g].z, v[g].w), acc[m][g]);
     }
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
-    const float p0 = __fadd_rn(acc[0][g].x, acc[0][g].y);
-    const float p1 = __fadd_rn(acc[1][g].x, acc[1][g].y);
-    const float keep = b1 ? p1 : p0, send = b1 ? p0 : p1;
-    float v = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, 1));
-    out[g] = v;
-  }
-}
-
-// u_t of a run for one value column: v holds v_t, dk the raw S^T k_t.
-__device__ __forceinline__ void spec_u(const RunCoef& C, int n, const float (&v)[kSpecK],
-                                       const float (&dk)[kSpecK], float (&u)[kSpecK]) {
+    float pm[4];
 #pragma unroll
-  for (int t = 0; t < kSpecK; ++t) {
-    u[t] = 0.0f;
-    if (t < n) {
-      float acc = __fmaf_rn(-C.gk[t], dk[t], v[t]);
-#pragma unroll
-      for (int s = 0; s < t; ++s) acc = __fmaf_rn(C.aneg[t][s], u[s], acc);
-      u[t] = __fmul_rn(C.beta[t], acc);
-    }
+    for (int m = 0; m < 4; ++m) pm[m] = __fadd_rn(acc[m][g].x, acc[m][g].y);
+    const float k0 = b2 ? pm[2] : pm[0], s0 = b2 ? pm[0] : pm[2];
+    const float k1 = b2 ? pm[3] : pm[1], s1 = b2 ? pm[1] : pm[3];
+    const float v0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, s0, 4));
+    const float v1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, s1, 4));
+    const float kk = b1 ? v1 : v0, ss = b1 ? v0 : v1;
+    float w = __fadd_rn(kk, __shfl_xor_sync(0xffffffffu, ss, 2));
+    w = __fadd_rn(w, __shfl_xor_sync(0xffffffffu, w, 1));
+    out[g] = w;
   }
 }
 
 // S <- the state after row a of a run that started from S:
 //   G_a S + sum_{s<=a} k_s (R[a][s] / |k_s|) u_s^T,
-// k rows (raw, fp32) at kx + s * kstride; u0/u1 hold u_s of the lane's two
-// columns.
+// k rows (raw, fp32, stored by spec_xpos) at kx + s * kstride; us[s * 16 +
+// m] holds u_s of the lane's column m (its warp's scratch).
 template <int DK, class ST>
 __device__ __forceinline__ void spec_advance(SpecS<DK>& S, const RunCoef& C, int a,
-                                             const float* kx, int kstride,
-                                             const float (&u0)[kSpecK],
-                                             const float (&u1)[kSpecK], int r4) {
+                                             const float* kx, int kstride, const float* us,
+                                             int r8) {
   using M = SpecMap<DK, ST>;
-  const float g = C.gam[a];
-  const float2 g2 = make_float2(g, g);
+  const float gm = C.gam[a];
+  const float2 g2 = make_float2(gm, gm);
 #pragma unroll
-  for (int m = 0; m < 2; ++m)
+  for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int p = 0; p < M::P; ++p) S.s[m][p] = __fmul2_rn(g2, S.s[m][p]);
 #pragma unroll
   for (int s = 0; s < kSpecK; ++s) {
     if (s <= a) {
       const float c = C.rk[a][s];
-      const float w0 = __fmul_rn(c, u0[s]), w1 = __fmul_rn(c, u1[s]);
-      const float2 w02 = make_float2(w0, w0), w12 = make_float2(w1, w1);
+      const float4 u4 = *reinterpret_cast<const float4*>(us + s * 16);
+      const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+      float2 w2[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float w = __fmul_rn(c, uu[m]);
+        w2[m] = make_float2(w, w);
+      }
       const float* xr = kx + s * kstride;
 #pragma unroll
       for (int i = 0; i < M::NI; ++i)
 #pragma unroll
-        for (int e = 0; e < M::VEC; e += 4) {
-          const int p = (i * M::VEC + e) / 2;
-          const float4 v = *reinterpret_cast<const float4*>(xr + M::idx(r4, i) + e);
+        for (int h = 0; h < M::VEC / 4; ++h) {
+          const int p = (i * M::VEC + 4 * h) / 2;
+          const float4 v = *reinterpret_cast<const float4*>(xr + M::xoff(r8, i, h));
           const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
-          S.s[0][p] = __ffma2_rn(lo, w02, S.s[0][p]);
-          S.s[1][p] = __ffma2_rn(lo, w12, S.s[1][p]);
-          S.s[0][p + 1] = __ffma2_rn(hi, w02, S.s[0][p + 1]);
-          S.s[1][p + 1] = __ffma2_rn(hi, w12, S.s[1][p + 1]);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            S.s[m][p] = __ffma2_rn(lo, w2[m], S.s[m][p]);
+            S.s[m][p + 1] = __ffma2_rn(hi, w2[m], S.s[m][p + 1]);
+          }
         }
     }
   }
@@ -286,14 +334,31 @@ __device__ __forceinline__ void spec_tri(int k, int& s, int& t) {
   s = k;
 }
 
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// All of this thread's copy groups but the most recent one have landed.
+__device__ __forceinline__ void cp_async_wait_all_but_one() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// 3 CTAs per SM (161 registers): measured faster than 2 (the item loop is
+// bound by latency, not by a pipe) and than 4 (which spills).
 template <class IO, class ST, int DK, int MODE>
-__global__ void __launch_bounds__(kSpecThreads, 2)
+__global__ void __launch_bounds__(kSpecThreads, 3)
 spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_in,
             const IO* __restrict__ conv_w, const IO* __restrict__ a_in,
             const IO* __restrict__ b_in, void* o, int out_f32, void* pages, int32_t* status,
             int splits) {
   using M = SpecMap<DK, ST>;
   constexpr int DV = DK;
+  constexpr int CR = kSpecK;                       // first row of the candidates
+  constexpr int VE = 16 / (int)sizeof(IO);         // io elements per 16-byte piece
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_begin();
 
@@ -306,9 +371,10 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
   const int it0 = split * per, it1 = min(n_items, it0 + per);
   const int h0 = kh * Gh;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r4 = lane & 3, cg = lane >> 2;
-  const bool b1 = (r4 & 2) != 0, b0 = (r4 & 1) != 0;
-  const int colw = 16 * warp + 2 * cg;             // the lane's first column in an item
+  const int r8 = lane & 7, cg = lane >> 3;
+  const bool b2 = (r8 & 4) != 0, b1 = (r8 & 2) != 0, b0 = (r8 & 1) != 0;
+  const int colw = 16 * warp + 4 * cg;             // the lane's first column in an item
+  const int cown = 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0); // the column its dot products end in
   const bool active = colw < BVI;
   const bool reporter = (blockIdx.x == 0 && tid == 0);
 
@@ -319,53 +385,7 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
   }
   if (MODE != SPEC_SLOTS && !q.spec) return;
 
-  // where the starting state lives: the page (one-page modes) or the slot
-  // the request resumes from
-  char* pg = page_ptr(G, pages, q.page);
-  ST* Sbase;
-  int n_r = 0, live = 0, parity = 0;
-  uint32_t* flagp = nullptr;
-  if constexpr (MODE == SPEC_SLOTS) {
-    const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
-    if (src < 0 || src >= G.Kc) {
-      if (reporter) report(status, GDN_DEV_BAD_ACCEPTED);
-      return;
-    }
-    if (q.len > G.Kc) {
-      if (reporter) report(status, GDN_DEV_TOO_MANY_CANDIDATES);
-      return;
-    }
-    pg = reinterpret_cast<char*>(pages) + (size_t)q.page * SG.pool_bytes;
-    Sbase = reinterpret_cast<ST*>(pg + (size_t)src * SG.slot_bytes + SG.state_off);
-  } else {
-    Sbase = reinterpret_cast<ST*>(pg + G.state_off);
-  }
-  auto item_col0 = [&](int it) -> ST* {
-    const int h = h0 + it / nCB, cb = it % nCB;
-    return Sbase + ((size_t)h * DV + (size_t)cb * BVI + colw) * DK;
-  };
   const SpecSmem L = spec_smem(DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST));
-  uint8_t* stage = smem + L.stage;
-  // the first item's state is requested before the flag is checked (one
-  // round trip, not two); a refused request only lets the copy land
-  if (active && it0 < it1) spec_stage_async<DK, ST>(stage, item_col0(it0), r4, tid);
-
-  if constexpr (MODE != SPEC_SLOTS) {
-    flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
-    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
-    SpecState ss = spec_state(G, B, q, flag);
-    if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
-    if (ss.err) {
-      if (reporter) report(status, ss.err);
-      spec_stage_wait();   // the copy lands before the CTA's shared memory goes away
-      return;
-    }
-    n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
-    live = ss.live;
-    parity = ss.parity;
-  }
-  const int n_c = q.len;
-  const int n_all = n_r + n_c;
   IO* raw = reinterpret_cast<IO*>(smem + L.raw);
   float* abs_ = reinterpret_cast<float*>(smem + L.ab);
   float* kx = reinterpret_cast<float*>(smem + L.kx);
@@ -373,69 +393,130 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
   RunDots& D = *reinterpret_cast<RunDots*>(smem + L.dots);
   float* gts = reinterpret_cast<float*>(smem + L.gates);
   RunCoef* coef = reinterpret_cast<RunCoef*>(smem + L.coef);
+  uint8_t* stage = smem + L.stage;
   const int RW = L.RW, DKP = L.DKP;
-  IO* rec = reinterpret_cast<IO*>(pg + G.record_off);   // one-page modes only
   const int g_lo = it0 / nCB, g_hi = (it1 > it0) ? (it1 - 1) / nCB + 1 : g_lo;  // own heads
+  const int ng = g_hi - g_lo;
   const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK, v_off = 2 * G.Hk * DK + h0 * DV;
+  const int n_c = q.len;
+  // channel of row element c (q | k | v of the group's heads) in a packed row
+  auto chan = [&](int c) {
+    return (c < DK) ? q_off + c : (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
+  };
+  const int row_els = 2 * DK + Gh * DV;
+  const int pieces = row_els / VE;
+
+  // ---- 1. this step's candidate rows start copying (they do not depend on
+  // the page), then the page is checked ---------------------------------
+  if constexpr (MODE != SPEC_FUSED) {
+    if (q.len <= G.Kc) {
+      for (int idx = tid; idx < n_c * pieces; idx += kSpecThreads) {
+        const int t = idx / pieces, c = (idx % pieces) * VE;
+        cp_async16(raw + (size_t)(CR + t) * RW + c, rows_in + (size_t)(q.start + t) * G.C + chan(c));
+      }
+    }
+  }
+  cp_async_commit();
+
+  char* pg = page_ptr(G, pages, q.page);
+  ST* Sbase;
+  int n_r = 0, live = 0, parity = 0;
+  uint32_t* flagp = nullptr;
+  int err = 0;
+  if constexpr (MODE == SPEC_SLOTS) {
+    const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
+    if (src < 0 || src >= G.Kc) err = GDN_DEV_BAD_ACCEPTED;
+    else if (q.len > G.Kc) err = GDN_DEV_TOO_MANY_CANDIDATES;
+    pg = reinterpret_cast<char*>(pages) + (size_t)q.page * SG.pool_bytes;
+    Sbase = reinterpret_cast<ST*>(pg + (size_t)(err ? 0 : src) * SG.slot_bytes + SG.state_off);
+  } else {
+    Sbase = reinterpret_cast<ST*>(pg + G.state_off);
+    flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
+    SpecState ss = spec_state(G, B, q, flag);
+    if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
+    err = ss.err;
+    n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
+    live = ss.live;
+    parity = ss.parity;
+  }
+  if (err) {
+    if (reporter) report(status, err);
+    asm volatile("cp.async.wait_all;" ::: "memory");   // nothing lands after the CTA is gone
+    return;
+  }
+  const int n_all = n_r + n_c;
+  IO* rec = reinterpret_cast<IO*>(pg + G.record_off);   // one-page modes only
   // head g's record gates and conv channels are written by the CTA holding
   // its first item; the q/k channels by split 0
   auto owns_head = [&](int g) { return (g * nCB) / per == split; };
+  auto item_col0 = [&](int it) -> ST* {
+    const int h = h0 + it / nCB, cb = it % nCB;
+    return Sbase + ((size_t)h * DV + (size_t)cb * BVI + colw) * DK;
+  };
 
-  // ---- 1. the group's rows into shared memory (raw, io dtype) ----------
-  {
-    constexpr int VE = 16 / (int)sizeof(IO);          // elements per 16-byte piece
-    const int pieces = RW / VE;
-    // replayed rows: k and v from the live record slot (their q is not used)
-    for (int idx = tid; idx < n_r * pieces; idx += kSpecThreads) {
-      const int t = idx / pieces, c = (idx % pieces) * VE;
-      if (c < DK) continue;
-      const int ch = (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
-      if (c >= 2 * DK + Gh * DV) continue;
-      const IO* src = rec + ((size_t)live * G.Kc + t) * G.rec_row + ch;
-      *reinterpret_cast<uint4*>(raw + (size_t)t * RW + c) = *reinterpret_cast<const uint4*>(src);
+  // ---- 2. replayed rows (k and v from the live record slot), the fused
+  // conv, gate inputs; the first item's state starts copying last ---------
+  for (int idx = tid; idx < n_r * pieces; idx += kSpecThreads) {
+    const int t = idx / pieces, c = (idx % pieces) * VE;
+    if (c < DK) continue;                            // a replayed row's q is not used
+    cp_async16(raw + (size_t)t * RW + c, rec + ((size_t)live * G.Kc + t) * G.rec_row + chan(c));
+  }
+  // the replay's run coefficients: those the previous step derived for the
+  // same rows as its candidates (the leading block is the same whatever the
+  // run's length), kept in the record slot beside them
+  if (n_r > 0) {
+    const float* rc = reinterpret_cast<const float*>(pg + G.rcoef_off) + (size_t)live * G.Hv * kRunCoefFloats;
+    for (int idx = tid; idx < ng * 36; idx += kSpecThreads) {
+      const int g = g_lo + idx / 36, k = idx % 36;
+      const float* src = rc + (size_t)(h0 + g) * kRunCoefFloats;
+      float* dst = reinterpret_cast<float*>(&coef[g * 2 + 0]);
+      // pieces 0-1: gk, 2-3: gam, 4-19: rk, 20-35: m (4 floats each)
+      const int so = 4 * k;
+      const int dofs = (k < 2) ? so : (k < 4) ? 16 + (so - 8) : (k < 20) ? 160 + (so - 16) : 224 + (so - 80);
+      cp_async16(dst + dofs, src + so);
     }
-    if constexpr (MODE != SPEC_FUSED) {
-      for (int idx = tid; idx < n_c * pieces; idx += kSpecThreads) {
-        const int t = idx / pieces, c = (idx % pieces) * VE;
-        if (c >= 2 * DK + Gh * DV) continue;
-        const int ch = (c < DK) ? q_off + c : (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
-        const IO* src = rows_in + (size_t)(q.start + t) * G.C + ch;
-        *reinterpret_cast<uint4*>(raw + (size_t)(n_r + t) * RW + c) =
-            *reinterpret_cast<const uint4*>(src);
+  }
+  cp_async_commit();
+  if (active && it0 < it1) spec_stage_async<DK, ST>(stage, item_col0(it0), r8, tid);
+  else cp_async_commit();   // keep "all but the newest group" meaning the rows
+
+  if constexpr (MODE == SPEC_FUSED) {
+    // the conv of the group's channels for this step's candidates, exactly
+    // as gdn_conv computes it for a spec request: history = window columns
+    // n_r .. n_r+W-2 (the record's accepted rows rolled out), taps oldest
+    // first, own SiLU, rounded to the io dtype. Every load of a channel
+    // vector is issued before its arithmetic.
+    const int nvec = row_els / 4;
+    IO* win = reinterpret_cast<IO*>(pg + G.window_off);
+    IO* rec_out = rec + (size_t)(1 - live) * G.Kc * G.rec_row;
+    for (int vi = tid; vi < nvec; vi += kSpecThreads) {
+      const int c4 = 4 * vi;
+      const int gg = (c4 < 2 * DK) ? -1 : (c4 - 2 * DK) / DV;
+      if (gg >= 0 && (gg < g_lo || gg >= g_hi)) continue;   // another split's head
+      const bool owner = (gg < 0) ? (split == 0) : owns_head(gg);
+      const int ch = chan(c4);
+      float wt[4][4], hcol[3][4], h0c[3][4], xr[kSpecK][4];
+      {
+        float tmp[16];
+        load_f<IO, 16>(conv_w + (size_t)ch * 4, tmp);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) wt[j][v] = tmp[v * 4 + j];
       }
-    } else {
-      // the conv of the group's channels for this step's candidates, exactly
-      // as gdn_conv computes it for a spec request: history = window
-      // columns n_r .. n_r+W-2 (the record's accepted rows rolled out),
-      // taps oldest first, own SiLU, rounded to the io dtype
-      const int nvec = (2 * DK + Gh * DV) / 4;
-      IO* win = reinterpret_cast<IO*>(pg + G.window_off);
-      IO* rec_out = rec + (size_t)(1 - live) * G.Kc * G.rec_row;
-      for (int vi = tid; vi < nvec; vi += kSpecThreads) {
-        const int c4 = 4 * vi;
-        const int gg = (c4 < 2 * DK) ? -1 : (c4 - 2 * DK) / DV;
-        if (gg >= 0 && (gg < g_lo || gg >= g_hi)) continue;   // another split's head
-        const bool owner = (gg < 0) ? (split == 0) : owns_head(gg);
-        const int ch = (c4 < DK) ? q_off + c4 : (c4 < 2 * DK) ? k_off + (c4 - DK) : v_off + (c4 - 2 * DK);
-        float wt[4][4];
-        {
-          float tmp[16];
-          load_f<IO, 16>(conv_w + (size_t)ch * 4, tmp);
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
+      for (int j = 0; j < 3; ++j) load_f<IO, 4>(win + (size_t)(n_r + j) * G.C + ch, hcol[j]);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) wt[j][v] = tmp[v * 4 + j];
-        }
-        float hcol[3][4], h0c[3][4];
+      for (int t = 0; t < kSpecK; ++t)
+        if (t < n_c) load_f<IO, 4>(rows_in + (size_t)(q.start + t) * G.C + ch, xr[t]);
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          load_f<IO, 4>(win + (size_t)(n_r + j) * G.C + ch, hcol[j]);
+      for (int j = 0; j < 3; ++j)
 #pragma unroll
-          for (int v = 0; v < 4; ++v) h0c[j][v] = hcol[j][v];
-        }
-        for (int t = 0; t < n_c; ++t) {
-          float xv[4];
-          load_f<IO, 4>(rows_in + (size_t)(q.start + t) * G.C + ch, xv);
+        for (int v = 0; v < 4; ++v) h0c[j][v] = hcol[j][v];
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) {
+        if (t < n_c) {
           float yv[4];
 #pragma unroll
           for (int v = 0; v < 4; v += 2) {
@@ -445,73 +526,85 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
             for (int j = 0; j < 3; ++j)
               acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]),
                                make_float2(hcol[j][v], hcol[j][v + 1]), acc);
-            acc = __ffma2_rn(make_float2(wt[3][v], wt[3][v + 1]), make_float2(xv[v], xv[v + 1]), acc);
+            acc = __ffma2_rn(make_float2(wt[3][v], wt[3][v + 1]),
+                             make_float2(xr[t][v], xr[t][v + 1]), acc);
             const float2 y2 = own_silu2(acc);
             yv[v] = y2.x;
             yv[v + 1] = y2.y;
           }
-          store_f<IO, 4>(raw + (size_t)(n_r + t) * RW + c4, yv);
+          store_f<IO, 4>(raw + (size_t)(CR + t) * RW + c4, yv);
           if (owner) {
             store_f<IO, 4>(rec_out + (size_t)t * G.rec_row + ch, yv);
-            store_f<IO, 4>(win + (size_t)(3 + t) * G.C + ch, xv);
+            store_f<IO, 4>(win + (size_t)(3 + t) * G.C + ch, xr[t]);
           }
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             hcol[0][v] = hcol[1][v];
             hcol[1][v] = hcol[2][v];
-            hcol[2][v] = xv[v];
+            hcol[2][v] = xr[t][v];
           }
         }
-        if (owner) {
-          // window columns 0..2: the history this step started from
+      }
+      if (owner) {
+        // window columns 0..2: the history this step started from
 #pragma unroll
-          for (int j = 0; j < 3; ++j) store_f<IO, 4>(win + (size_t)j * G.C + ch, h0c[j]);
-        }
+        for (int j = 0; j < 3; ++j) store_f<IO, 4>(win + (size_t)j * G.C + ch, h0c[j]);
       }
-    }
-    // gate inputs per row and own head: record rows, then this step's rows
-    for (int idx = tid; idx < n_all * (g_hi - g_lo); idx += kSpecThreads) {
-      const int t = idx / (g_hi - g_lo), g = g_lo + idx % (g_hi - g_lo), h = h0 + g;
-      float av, bv;
-      if (t < n_r) {
-        const IO* row = rec + ((size_t)live * G.Kc + t) * G.rec_row;
-        av = to_f(row[G.C + h]);
-        bv = to_f(row[G.C + G.Hv + h]);
-      } else {
-        const size_t rn = (size_t)q.start + (t - n_r);
-        av = to_f(a_in[rn * G.Hv + h]);
-        bv = to_f(b_in[rn * G.Hv + h]);
-        if (MODE != SPEC_SLOTS && owns_head(g)) {
-          // the candidates' gates go next to their conv'd rows in the other slot
-          IO* row = rec + ((size_t)(1 - live) * G.Kc + (t - n_r)) * G.rec_row;
-          row[G.C + h] = a_in[rn * G.Hv + h];
-          row[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
-        }
-      }
-      abs_[t * 2 * Gh + g] = av;
-      abs_[t * 2 * Gh + Gh + g] = bv;
     }
   }
-  __syncthreads();
-
-  // ---- 2. fp32 copies of the k rows (all) and q rows (candidates) -------
-  for (int idx = tid; idx < (n_all + n_c) * (DK / 4); idx += kSpecThreads) {
-    const int r = idx / (DK / 4), d = (idx % (DK / 4)) * 4;
-    float f[4];
-    if (r < n_all) {
-      load_f<IO, 4>(raw + (size_t)r * RW + DK + d, f);
-      *reinterpret_cast<float4*>(kx + r * DKP + d) = make_float4(f[0], f[1], f[2], f[3]);
+  // gate inputs per row and own head: record rows, then this step's rows
+  for (int idx = tid; idx < n_all * ng; idx += kSpecThreads) {
+    const int t = idx / ng, g = g_lo + idx % ng, h = h0 + g;
+    const int row = (t < n_r) ? t : CR + (t - n_r);
+    float av, bv;
+    if (t < n_r) {
+      const IO* rr = rec + ((size_t)live * G.Kc + t) * G.rec_row;
+      av = to_f(rr[G.C + h]);
+      bv = to_f(rr[G.C + G.Hv + h]);
     } else {
-      const int t = r - n_all;
-      load_f<IO, 4>(raw + (size_t)(n_r + t) * RW + d, f);
-      *reinterpret_cast<float4*>(qx + t * DKP + d) = make_float4(f[0], f[1], f[2], f[3]);
+      const size_t rn = (size_t)q.start + (t - n_r);
+      av = to_f(a_in[rn * G.Hv + h]);
+      bv = to_f(b_in[rn * G.Hv + h]);
+      if (MODE != SPEC_SLOTS && owns_head(g)) {
+        // the candidates' gates go next to their conv'd rows in the other slot
+        IO* rr = rec + ((size_t)(1 - live) * G.Kc + (t - n_r)) * G.rec_row;
+        rr[G.C + h] = a_in[rn * G.Hv + h];
+        rr[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
+      }
+    }
+    abs_[row * 2 * Gh + g] = av;
+    abs_[row * 2 * Gh + Gh + g] = bv;
+  }
+  cp_async_wait_all_but_one();   // the rows (not the state) have landed
+  __syncthreads();
+
+  // ---- 3. fp32 copies of the k rows (all) and q rows (candidates), each
+  // in the order the lanes read it (spec_xpos); the Gram products below sum
+  // over that order too ---------------------------------------------------
+  {
+    constexpr int Q4 = DK / 4;
+    const int nk = n_all * Q4;
+    for (int idx = tid; idx < nk + n_c * Q4; idx += kSpecThreads) {
+      float f[4];
+      if (idx < nk) {
+        const int r = idx / Q4, d = (idx % Q4) * 4;
+        const int row = (r < n_r) ? r : CR + (r - n_r);
+        load_f<IO, 4>(raw + (size_t)row * RW + DK + d, f);
+        *reinterpret_cast<float4*>(kx + row * DKP + spec_xpos<DK, ST>(d)) =
+            make_float4(f[0], f[1], f[2], f[3]);
+      } else {
+        const int t = (idx - nk) / Q4, d = ((idx - nk) % Q4) * 4;
+        load_f<IO, 4>(raw + (size_t)(CR + t) * RW + d, f);
+        *reinterpret_cast<float4*>(qx + t * DKP + spec_xpos<DK, ST>(d)) =
+            make_float4(f[0], f[1], f[2], f[3]);
+      }
     }
   }
   __syncthreads();
 
-  // ---- 3. Gram products and norms (one per thread), gates ---------------
+  // ---- 4. Gram products and norms (one per thread), gates ---------------
   {
-    const int A = n_r * (n_r + 1) / 2, Bc = n_c * (n_c + 1) / 2;
+    const int A = 0, Bc = n_c * (n_c + 1) / 2;   // (the replay's come from the record)
     int k = tid;
     if (k < A) {
       int s, t;
@@ -520,72 +613,153 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
     } else if ((k -= A) < Bc) {
       int s, t;
       spec_tri(k, s, t);
-      D.kkc[t][s] = spec_rowdot<DK>(kx + (n_r + s) * DKP, kx + (n_r + t) * DKP);
+      D.kkc[t][s] = spec_rowdot<DK>(kx + (CR + s) * DKP, kx + (CR + t) * DKP);
     } else if ((k -= Bc) < Bc) {
       int s, t;
       spec_tri(k, s, t);
-      D.kqc[t][s] = spec_rowdot<DK>(kx + (n_r + s) * DKP, qx + t * DKP);
+      D.kqc[t][s] = spec_rowdot<DK>(kx + (CR + s) * DKP, qx + t * DKP);
     } else if ((k -= Bc) < n_c) {
       D.qqc[k] = spec_rowdot<DK>(qx + k * DKP, qx + k * DKP);
     }
-    // gates of own heads: thread -> (head, row)
-    const int ng = g_hi - g_lo;
-    for (int idx = tid; idx < ng * n_all; idx += kSpecThreads) {
-      const int g = g_lo + idx / n_all, t = idx % n_all;
+    // gates of own heads for the candidates: thread -> (head, row); and the
+    // candidate run's coefficient blocks start from zero (the entries past
+    // the run stay zero wherever they are stored)
+    for (int idx = tid; idx < ng * n_c; idx += kSpecThreads) {
+      const int g = g_lo + idx / n_c, t = idx % n_c;
+      const int row = CR + t;
       float alpha, beta;
-      gates(P, h0 + g, abs_[t * 2 * Gh + g], abs_[t * 2 * Gh + Gh + g], alpha, beta);
-      const int run = (t < n_r) ? 0 : 1, tr = (t < n_r) ? t : t - n_r;
-      gts[((g * 2 + run) * 2 + 0) * kSpecK + tr] = alpha;
-      gts[((g * 2 + run) * 2 + 1) * kSpecK + tr] = beta;
+      gates(P, h0 + g, abs_[row * 2 * Gh + g], abs_[row * 2 * Gh + Gh + g], alpha, beta);
+      gts[((g * 2 + 1) * 2 + 0) * kSpecK + t] = alpha;
+      gts[((g * 2 + 1) * 2 + 1) * kSpecK + t] = beta;
+    }
+    for (int idx = tid; idx < ng * (int)(sizeof(RunCoef) / 16); idx += kSpecThreads) {
+      const int g = g_lo + idx / (int)(sizeof(RunCoef) / 16), k = idx % (int)(sizeof(RunCoef) / 16);
+      reinterpret_cast<float4*>(&coef[g * 2 + 1])[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   __syncthreads();
 
-  // ---- 4. run coefficients: thread -> (own head, run, column s = -1..n-1)
+  // ---- 5. run coefficients per own head and run --------------------------
   {
-    const int ng = g_hi - g_lo;
-    for (int idx = tid; idx < ng * 2 * (kSpecK + 1); idx += kSpecThreads) {
-      const int g = g_lo + idx / (2 * (kSpecK + 1));
-      const int run = (idx / (kSpecK + 1)) & 1;
+    // (a) thread -> (head, run, column s = -1..7): decay products R[.][s], G,
+    // and the columns of L, B and R/|k|. Loops run to kSpecK with guards, so
+    // every array index is a compile-time constant.
+    for (int idx = tid; idx < ng * (kSpecK + 1); idx += kSpecThreads) {
+      const int g = g_lo + idx / (kSpecK + 1);
+      const int run = 1;
       const int s = idx % (kSpecK + 1) - 1;
       const int n = run ? n_c : n_r;
       if (s >= n) continue;
       RunCoef& C = coef[g * 2 + run];
       const float* al = gts + ((g * 2 + run) * 2 + 0) * kSpecK;
       const float* be = gts + ((g * 2 + run) * 2 + 1) * kSpecK;
-      auto ik_of = [&](int t) {
-        return rsqrtf(__fadd_rn(run ? D.kkc[t][t] : D.kkr[t][t], P.eps));
-      };
+      float ik[kSpecK], iq[kSpecK];
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) {
+        ik[t] = (t < n) ? rsqrtf(__fadd_rn(run ? D.kkc[t][t] : D.kkr[t][t], P.eps)) : 0.0f;
+        iq[t] = (run && t < n) ? rsqrtf(__fadd_rn(D.qqc[t], P.eps)) : 0.0f;
+      }
       if (s < 0) {
         float r = 1.0f;
-        for (int t = 0; t < n; ++t) {
-          r = __fmul_rn(r, al[t]);
-          C.gam[t] = r;
-          C.gk[t] = __fmul_rn(r, ik_of(t));
-          C.gq[t] = run ? __fmul_rn(r, rsqrtf(__fadd_rn(D.qqc[t], P.eps))) : 0.0f;
-          C.beta[t] = be[t];
+#pragma unroll
+        for (int t = 0; t < kSpecK; ++t) {
+          if (t < n) {
+            r = __fmul_rn(r, al[t]);
+            C.gam[t] = r;
+            C.gk[t] = __fmul_rn(r, ik[t]);
+            C.gq[t] = __fmul_rn(r, iq[t]);
+            C.beta[t] = be[t];
+          }
         }
       } else {
-        const float iks = ik_of(s);
+        float iks = 0.0f;
+#pragma unroll
+        for (int t = 0; t < kSpecK; ++t) iks = (t == s) ? ik[t] : iks;
         float r = 1.0f;
-        for (int t = s; t < n; ++t) {
-          if (t > s) r = __fmul_rn(r, al[t]);
-          C.rk[t][s] = __fmul_rn(r, iks);
-          if (t > s) {
-            const float kk = run ? D.kkc[t][s] : D.kkr[t][s];
-            C.aneg[t][s] = -__fmul_rn(r, __fmul_rn(__fmul_rn(kk, iks), ik_of(t)));
-          }
-          if (run) {
-            const float iqt = rsqrtf(__fadd_rn(D.qqc[t], P.eps));
-            C.bco[t][s] = __fmul_rn(r, __fmul_rn(__fmul_rn(D.kqc[t][s], iks), iqt));
+#pragma unroll
+        for (int t = 0; t < kSpecK; ++t) {
+          if (t >= s && t < n) {
+            if (t > s) r = __fmul_rn(r, al[t]);
+            C.rk[t][s] = __fmul_rn(r, iks);
+            if (t > s) {
+              const float kk = run ? D.kkc[t][s] : D.kkr[t][s];
+              C.l[t][s] = -__fmul_rn(be[t], __fmul_rn(r, __fmul_rn(__fmul_rn(kk, iks), ik[t])));
+            }
+            if (run) C.bco[t][s] = __fmul_rn(r, __fmul_rn(__fmul_rn(D.kqc[t][s], iks), iq[t]));
           }
         }
       }
     }
+    __syncthreads();
+    // (b) thread -> (head, run, column s): column s of (I - L)^-1 by forward
+    // substitution (rows in increasing order, terms r = s .. t-1), times beta_s
+    for (int idx = tid; idx < ng * kSpecK; idx += kSpecThreads) {
+      const int g = g_lo + idx / kSpecK;
+      const int run = 1;
+      const int s = idx % kSpecK;
+      const int n = run ? n_c : n_r;
+      if (s >= n) continue;
+      RunCoef& C = coef[g * 2 + run];
+      float Lr[kSpecK][kSpecK];
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t)
+#pragma unroll
+        for (int r = 0; r < t; ++r) Lr[t][r] = (t < n && r >= s) ? C.l[t][r] : 0.0f;
+      float col[kSpecK];   // col[t] = (I - L)^-1 [t][s]
+      const float bs = C.beta[s];
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) {
+        if (t < s) {
+          col[t] = 0.0f;
+        } else if (t == s) {
+          col[t] = 1.0f;
+          C.m[t][s] = bs;
+        } else if (t < n) {
+          float acc = 0.0f;
+          bool first = true;
+#pragma unroll
+          for (int r = 0; r < t; ++r) {
+            if (r >= s) {
+              acc = first ? __fmul_rn(Lr[t][r], col[r]) : __fmaf_rn(Lr[t][r], col[r], acc);
+              first = false;
+            }
+          }
+          col[t] = acc;
+          C.m[t][s] = __fmul_rn(acc, bs);
+        }
+      }
+    }
+    __syncthreads();
+    // (c) thread -> (head, candidate row t, column s): N[t][s] = sum_r B[t][r] M[r][s]
+    for (int idx = tid; idx < ng * kSpecK * kSpecK; idx += kSpecThreads) {
+      const int g = g_lo + idx / (kSpecK * kSpecK);
+      const int t = (idx / kSpecK) % kSpecK, s = idx % kSpecK;
+      if (t >= n_c || s > t) continue;
+      RunCoef& C = coef[g * 2 + 1];
+      float acc = __fmul_rn(C.bco[t][s], C.m[s][s]);
+      for (int r = s + 1; r <= t; ++r) acc = __fmaf_rn(C.bco[t][r], C.m[r][s], acc);
+      C.nq[t][s] = acc;
+    }
   }
   __syncthreads();
+  if constexpr (MODE != SPEC_SLOTS) {
+    // the candidates' run coefficients go beside their rows in the other
+    // slot, for the next step's replay
+    if (n_c > 0) {
+      float* rc = reinterpret_cast<float*>(pg + G.rcoef_off) + (size_t)(1 - live) * G.Hv * kRunCoefFloats;
+      for (int idx = tid; idx < ng * 36; idx += kSpecThreads) {
+        const int g = g_lo + idx / 36, k = idx % 36;
+        if (!owns_head(g)) continue;
+        const float* src = reinterpret_cast<const float*>(&coef[g * 2 + 1]);
+        const int so = 4 * k;
+        const int sofs = (k < 2) ? so : (k < 4) ? 16 + (so - 8) : (k < 20) ? 160 + (so - 16) : 224 + (so - 80);
+        *reinterpret_cast<float4*>(rc + (size_t)(h0 + g) * kRunCoefFloats + so) =
+            *reinterpret_cast<const float4*>(src + sofs);
+      }
+    }
+  }
 
-  // ---- 5. items: no block-wide barrier from here on ---------------------
+  // ---- 6. items: no block-wide barrier from here on ---------------------
   // An item's state comes from the stage (copied by this thread alone). The
   // one-page modes request the next item's copy as soon as the first dot
   // products have consumed the current one; the slot layout keeps the stage
@@ -595,118 +769,147 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
     for (int it = it0; it < it1; ++it) {
       const int g = it / nCB, cb = it % nCB, h = h0 + g;
       ST* col0 = item_col0(it);
-      if (MODE == SPEC_SLOTS && it > it0) spec_stage_async<DK, ST>(stage, col0, r4, tid);
+      if (MODE == SPEC_SLOTS && it > it0) spec_stage_async<DK, ST>(stage, col0, r8, tid);
       spec_stage_wait();
       SpecS<DK> S;
       spec_unstage<DK, ST>(S, stage, tid);
       bool ahead = (MODE == SPEC_SLOTS) || (it + 1 >= it1);
       auto prefetch = [&]() {
         if (!ahead) {
-          spec_stage_async<DK, ST>(stage, item_col0(it + 1), r4, tid);
+          spec_stage_async<DK, ST>(stage, item_col0(it + 1), r8, tid);
           ahead = true;
         }
       };
-      const int vcol = g * DV + cb * BVI + colw + (b1 ? 1 : 0);   // this lane's v column
+      // per-warp scratch: dsc[r][j] the dot products of row r (k rows 0..7,
+      // candidate q rows 8..15) with the warp's column j; usc[t][j] = u
+      float* dsc = reinterpret_cast<float*>(smem + L.scr) + warp * kSpecScr;
+      float* usc = dsc + 2 * kSpecK * 16;
+      const int jw = 4 * cg + cown;                 // this lane's column in the warp
+      const bool writer = (r8 & 1) == 0;            // one of the column's two lanes
+      // the scalar phase maps lane -> (column jc of the warp, row half th)
+      const int jc = lane & 15, th = lane >> 4;
+      const int vcol = g * DV + cb * BVI + 16 * warp + jc;   // v column of jc
 
       if (n_r > 0) {
         const RunCoef& C = coef[g * 2 + 0];
-        float dk[kSpecK], v[kSpecK], u[kSpecK], uo[kSpecK];
 #pragma unroll
         for (int t = 0; t < kSpecK; t += 2) {
           if (t < n_r) {
             const float* xr[2] = {kx + t * DKP, kx + (t + 1) * DKP};
             float out[2];
-            spec_dots<DK, ST, 2>(S, xr, r4, b1, out);
-            dk[t] = out[0];
-            dk[t + 1] = out[1];
+            spec_dots<DK, ST, 2>(S, xr, r8, b2, b1, out);
+            if (writer) {
+              dsc[t * 16 + jw] = out[0];
+              dsc[(t + 1) * 16 + jw] = out[1];
+            }
             if (t == 0) prefetch();
           }
         }
+        __syncwarp();
+        // c_t = v_t - G_t dk_t for column jc; u_t = sum_s M[t][s] c_s for
+        // the rows t of half th
+        {
+          float c[kSpecK];
 #pragma unroll
-        for (int t = 0; t < kSpecK; ++t) v[t] = (t < n_r) ? to_f(vraw[(size_t)t * RW + vcol]) : 0.0f;
-        spec_u(C, n_r, v, dk, u);
+          for (int t = 0; t < kSpecK; ++t)
+            c[t] = (t < n_r) ? __fmaf_rn(-C.gk[t], dsc[t * 16 + jc],
+                                         to_f(vraw[(size_t)t * RW + vcol])) : 0.0f;
 #pragma unroll
-        for (int t = 0; t < kSpecK; ++t) uo[t] = __shfl_xor_sync(0xffffffffu, u[t], 2);
-        float u0[kSpecK], u1[kSpecK];
+          for (int tt = 0; tt < kSpecK / 2; ++tt) {
+            const int t = 2 * tt + th;
+            if (t < n_r) {
+              float acc = __fmul_rn(C.m[t][0], c[0]);
 #pragma unroll
-        for (int t = 0; t < kSpecK; ++t) {
-          u0[t] = b1 ? uo[t] : u[t];
-          u1[t] = b1 ? u[t] : uo[t];
+              for (int s = 1; s <= 2 * tt + 1; ++s)
+                if (s <= t) acc = __fmaf_rn(C.m[t][s], c[s], acc);
+              usc[t * 16 + jc] = acc;
+            }
+          }
         }
-        spec_advance<DK, ST>(S, C, n_r - 1, kx, DKP, u0, u1, r4);
-        spec_store<DK, ST>(col0, S, r4);
+        __syncwarp();
+        spec_advance<DK, ST>(S, C, n_r - 1, kx, DKP, usc + 4 * cg, r8);
+        spec_store<DK, ST>(col0, S, r8);
         // continue from exactly what was stored (a bf16 page rounds here)
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < 4; ++m)
 #pragma unroll
           for (int p = 0; p < M::P; ++p)
             S.s[m][p] = make_float2(through<ST>(S.s[m][p].x), through<ST>(S.s[m][p].y));
+        __syncwarp();   // usc is read again only after this
       }
 
       if (n_c > 0) {
         const RunCoef& C = coef[g * 2 + 1];
-        float dk[kSpecK], dq[kSpecK], v[kSpecK], u[kSpecK];
-        const float* kc = kx + n_r * DKP;
+        const float* kc = kx + CR * DKP;
 #pragma unroll
         for (int t = 0; t < kSpecK; t += 2) {
           if (t < n_c) {
             const float* xr[4] = {kc + t * DKP, kc + (t + 1) * DKP, qx + t * DKP,
                                   qx + (t + 1) * DKP};
             float out[4];
-            spec_dots<DK, ST, 4>(S, xr, r4, b1, out);
-            dk[t] = out[0];
-            dk[t + 1] = out[1];
-            dq[t] = out[2];
-            dq[t + 1] = out[3];
+            spec_dots<DK, ST, 4>(S, xr, r8, b2, b1, out);
+            if (writer) {
+              dsc[t * 16 + jw] = out[0];
+              dsc[(t + 1) * 16 + jw] = out[1];
+              dsc[(kSpecK + t) * 16 + jw] = out[2];
+              dsc[(kSpecK + t + 1) * 16 + jw] = out[3];
+            }
             if (t == 0) prefetch();
           }
         }
+        __syncwarp();
+        float c[kSpecK];
 #pragma unroll
         for (int t = 0; t < kSpecK; ++t)
-          v[t] = (t < n_c) ? to_f(vraw[(size_t)(n_r + t) * RW + vcol]) : 0.0f;
-        spec_u(C, n_c, v, dk, u);
-        // outputs: lane bit 0 picks the rows t = 2 tt + b0
-        const size_t ocol = (size_t)h * DV + (size_t)cb * BVI + colw + (b1 ? 1 : 0);
+          c[t] = (t < n_c) ? __fmaf_rn(-C.gk[t], dsc[t * 16 + jc],
+                                       to_f(vraw[(size_t)(CR + t) * RW + vcol])) : 0.0f;
+        // outputs o_t = scale (G_t S^T q^_t + sum_s N[t][s] c_s), column jc,
+        // the rows of half th
+        const size_t ocol = (size_t)h * DV + (size_t)cb * BVI + 16 * warp + jc;
 #pragma unroll
         for (int tt = 0; tt < kSpecK / 2; ++tt) {
-          const int t = 2 * tt + (b0 ? 1 : 0);
+          const int t = 2 * tt + th;
           if (t < n_c) {
-            const float dqt = b0 ? dq[2 * tt + 1] : dq[2 * tt];
-            float acc = __fmul_rn(C.gq[t], dqt);
+            float acc = __fmul_rn(C.gq[t], dsc[(kSpecK + t) * 16 + jc]);
 #pragma unroll
             for (int s = 0; s <= 2 * tt + 1; ++s)
-              if (s <= t) acc = __fmaf_rn(C.bco[t][s], u[s], acc);
+              if (s <= t) acc = __fmaf_rn(C.nq[t][s], c[s], acc);
             store_out(o, out_f32, ((size_t)q.start + t) * G.Hv * DV + ocol,
                       __fmul_rn(P.scale, acc));
           }
         }
         if constexpr (MODE == SPEC_SLOTS) {
-          // the state after every candidate goes to its slot, each rebuilt
-          // from the staged starting state
-          float uo[kSpecK], u0[kSpecK], u1[kSpecK];
+          // u of the candidates, then the state after every candidate goes
+          // to its slot, each rebuilt from the staged starting state
 #pragma unroll
-          for (int t = 0; t < kSpecK; ++t) uo[t] = __shfl_xor_sync(0xffffffffu, u[t], 2);
+          for (int tt = 0; tt < kSpecK / 2; ++tt) {
+            const int t = 2 * tt + th;
+            if (t < n_c) {
+              float acc = __fmul_rn(C.m[t][0], c[0]);
 #pragma unroll
-          for (int t = 0; t < kSpecK; ++t) {
-            u0[t] = b1 ? uo[t] : u[t];
-            u1[t] = b1 ? u[t] : uo[t];
+              for (int s = 1; s <= 2 * tt + 1; ++s)
+                if (s <= t) acc = __fmaf_rn(C.m[t][s], c[s], acc);
+              usc[t * 16 + jc] = acc;
+            }
           }
+          __syncwarp();
           const size_t off = (size_t)(col0 - Sbase);
           for (int t = 0; t < n_c; ++t) {
             SpecS<DK> T;
             spec_unstage<DK, ST>(T, stage, tid);
-            spec_advance<DK, ST>(T, C, t, kc, DKP, u0, u1, r4);
+            spec_advance<DK, ST>(T, C, t, kc, DKP, usc + 4 * cg, r8);
             ST* dst = reinterpret_cast<ST*>(pg + (size_t)t * SG.slot_bytes + SG.state_off) + off;
-            spec_store<DK, ST>(dst, T, r4);
+            spec_store<DK, ST>(dst, T, r8);
           }
         }
+        __syncwarp();   // dsc / usc are written again only after this
       }
       prefetch();   // (a run with no rows never consumed the stage)
     }
   }
   spec_stage_wait();   // no copy outlives the CTA's shared memory
 
-  // ---- 6. the last CTA of the request publishes the new flag word -------
+  // ---- 7. the last CTA of the request publishes the new flag word -------
   // No fence orders the page data first: only later launches read it. The
   // counter needs none either: every CTA read the flag before its own
   // increment of the same word, so the publish follows every read.

@@ -49,10 +49,19 @@ class PagePool:
         return v.view(torch_dtype(d.io_dtype)).view(d.conv_width - 1 + d.max_candidates, self.C)
 
     def record(self, p):
-        """[2][Kc][rec_row] view (io dtype) of page p's record."""
+        """[2][Kc][rec_row] view (io dtype) of page p's record rows."""
         d = self.dims
-        v = self._bytes(p, self.layout.record_offset, self.layout.record_bytes)
+        n = 2 * d.max_candidates * self.rec_row * torch_dtype(d.io_dtype).itemsize
+        v = self._bytes(p, self.layout.record_offset, n)
         return v.view(torch_dtype(d.io_dtype)).view(2, d.max_candidates, self.rec_row)
+
+    def record_coefficients(self, p):
+        """[2][Hv][144] fp32 view of page p's record run coefficients (per slot
+        and value head: G/|k| [8], G [8], R/|k| [8][8], M [8][8])."""
+        d = self.dims
+        n = 2 * d.max_candidates * self.rec_row * torch_dtype(d.io_dtype).itemsize
+        v = self._bytes(p, self.layout.record_offset + n, self.layout.record_bytes - n)
+        return v.view(torch.float32).view(2, d.num_v_heads, 144)
 
     def flag(self, p):
         return self._bytes(p, self.layout.flag_offset, 4).view(torch.int32)

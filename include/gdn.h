@@ -155,7 +155,11 @@ typedef struct {
  *   state   [Hv][Dv][Dk] state dtype: the GDN state (the checkpoint).
  *   record  [2][Kc][R_w] io dtype: two slots of candidate rows, each row
  *           = conv'd q|k|v (C) then a (Hv) then b (Hv), padded to R_w
- *           elements so that every row starts on a 16-byte boundary.
+ *           elements so that every row starts on a 16-byte boundary; then
+ *           [2][Hv][144] fp32: per slot and value head, the run coefficients
+ *           the verify derived for that slot's rows (G_t/|k_t| [8], G_t [8],
+ *           R[t][s]/|k_s| [8][8], M = (I - L)^-1 diag(beta) [8][8]; see
+ *           gdn_spec_verify), which the next step's replay uses as stored.
  *   flag    uint32: bit 0 live slot, bit 1 step parity, bits 2..7 number of
  *           rows in the live slot, bits 8..31 done counter (0 between calls).
  * A zero-filled page is a valid empty page (zero state, zero window, closed
