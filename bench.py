@@ -206,6 +206,14 @@ class Decode:
         self.h_in = torch.empty_like(self.d_in, device="cpu").pin_memory()
         self.h_o = torch.empty_like(self.o, device="cpu").pin_memory()
         self.h_in.copy_(self.d_in.cpu())
+        # the overlapped end-to-end leg: two device copies of the inputs and
+        # outputs, so step i+1's upload and step i-1's download run while
+        # step i's kernel runs
+        self.d_in2 = [torch.empty_like(self.d_in) for _ in range(2)]
+        self.o2 = [torch.empty_like(self.o) for _ in range(2)]
+        self.h_o2 = [torch.empty_like(self.o, device="cpu").pin_memory() for _ in range(2)]
+        self.s_in = torch.cuda.Stream(device=device)
+        self.s_out = torch.cuda.Stream(device=device)
 
     # bytes the fused decode kernel must move per launch
     def decode_bytes(self):
@@ -250,6 +258,51 @@ class Decode:
         self.d_in.copy_(self.h_in, non_blocking=True)
         self.launch(i)
         self.h_o.copy_(self.o, non_blocking=True)
+
+    def run_e2e_overlapped(self, K, i0=0):
+        """K steps through host buffers with the copies overlapped: step i's
+        inputs are uploaded (pinned host -> device buffer i%2) on one stream,
+        its kernel runs on the current stream once they have landed (and once
+        the download of step i-2 has left output buffer i%2), and its output
+        is downloaded (device -> pinned host) on a third stream. Every step's
+        copies are inside the returned time (CUDA events on the current
+        stream, which waits for the last download)."""
+        torch, gdn = self.torch, self.gdn
+        cur = torch.cuda.current_stream()
+        ev = {k: [torch.cuda.Event() for _ in range(2)]
+              for k in ("in_ready", "in_free", "out_ready", "out_free")}
+        for lst in ev.values():
+            for e in lst:
+                e.record(cur)
+        sh, R = self.sh, self.R
+        nx, na = R * sh.C, R * sh.Hv
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(cur)
+        for k in range(K):
+            b = k % 2
+            self.s_in.wait_event(ev["in_free"][b])
+            with torch.cuda.stream(self.s_in):
+                self.d_in2[b].copy_(self.h_in, non_blocking=True)
+            ev["in_ready"][b].record(self.s_in)
+            cur.wait_event(ev["in_ready"][b])
+            cur.wait_event(ev["out_free"][b])
+            d = self.d_in2[b]
+            x, a, bb = d[:nx].view(R, sh.C), d[nx:nx + na].view(R, sh.Hv), d[nx + na:].view(R, sh.Hv)
+            pool = self.pools[(i0 + k) % len(self.pools)]
+            gdn.gdn_decode(self.dims, self.batch, self.params, x, self.conv_w, a, bb, self.o2[b],
+                           pool.buf, self.status, stream=cur)
+            ev["in_free"][b].record(cur)
+            ev["out_ready"][b].record(cur)
+            self.s_out.wait_event(ev["out_ready"][b])
+            with torch.cuda.stream(self.s_out):
+                self.h_o2[b].copy_(self.o2[b], non_blocking=True)
+            ev["out_free"][b].record(self.s_out)
+        cur.wait_stream(self.s_out)
+        end.record(cur)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end) / 1e3
 
     def e2e_bytes(self):
         h2d = self.h_in.numel() * self.h_in.element_size()
@@ -311,14 +364,21 @@ def run_ours(args, world, rank, local):
     conv_ms = [e[0].elapsed_time(e[1]) for e in ev2]
     rule_ms = [e[1].elapsed_time(e[2]) for e in ev2]
 
-    # end-to-end through host buffers
+    # end-to-end through host buffers: the same steps with each step's upload
+    # and download inside the timed region, overlapped with the neighbouring
+    # steps' kernels; the serial form (upload, kernel, download on one
+    # stream) is reported beside it
     for i in range(W):
         wl.launch_e2e(i)
     torch.cuda.synchronize()
+    e2e_serial = time_steps(lambda i: wl.launch_e2e(i), K, torch)
+    wl.run_e2e_overlapped(W)
     barrier(world)
-    e2e = time_steps(lambda i: wl.launch_e2e(i), K, torch)
+    e2e = wl.run_e2e_overlapped(K)
     e2e_max = reduce_max(e2e, world)
     h2d, d2h = wl.e2e_bytes()
+    # the overlapped leg's outputs equal the device-resident step's
+    wl.check()
 
     tokens = wl.R * K * world
     dec_bytes, state_bytes = wl.decode_bytes()
@@ -361,7 +421,10 @@ def run_ours(args, world, rank, local):
                             "gdn_seq_ms": statistics.mean(rule_ms),
                             "tokens_per_s": wl.R * K2 / el2},
         "e2e": {"value": tokens / e2e_max, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max / K * 1e3},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_max / K * 1e3,
+                "copies": "per step: H2D of the packed inputs and D2H of the output, on "
+                          "their own streams, overlapped with the neighbouring steps' kernels",
+                "serial_ms_per_step": e2e_serial / K * 1e3},
         "gpu_launches": K,
         "clocks": clk.summary(),
         "wall_s": wall,
@@ -683,14 +746,62 @@ def bench_mixed(device, peaks, K=20, W=4):
         launch_two_streams(W + K + i)
     torch.cuda.synchronize()
     el2 = time_steps(lambda i: launch_two_streams(2 * W + K + i), K, torch)
+    conv_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    prefill_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    verify_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    step_ms = el / K * 1e3
+    # Algorithmic bytes of the step, per kernel (bf16 rows and outputs, fp32
+    # state): the conv reads x and writes y and the windows (fresh prefills
+    # write W-1 columns, spec requests read W-1 and write W-1+n) and the spec
+    # candidates' record rows; the prefill reads its rows and gates, writes
+    # its outputs and final states (fresh: nothing read); the verify reads and
+    # writes the spec pages' states, reads the candidate rows and the replayed
+    # record rows (the mean accepted count + 1), writes outputs, gates and
+    # run coefficients into the record.
+    C, Hv, D = sh.C, sh.Hv, sh.Dv
+    np_rows = int(lengths[ns:].sum())
+    ns_rows = int(lengths[:ns].sum())
+    rec_row = (C + 2 * Hv) * 2
+    coef_bytes = Hv * 144 * 4
+    mean_rep = float(np.mean(d["prev_accepted"])) + 1.0
+    conv_b = (2 * T * C * 2 + (R - ns) * (sh.W - 1) * C * 2
+              + ns * ((sh.W - 1) + (sh.W - 1 + n)) * C * 2 + ns_rows * rec_row)
+    state = Hv * sh.Dk * D * 4
+    pre_b = np_rows * (C + 2 * Hv) * 2 + np_rows * Hv * D * 2 + (R - ns) * state
+    ver_b = (2 * ns * state + ns_rows * (C + 2 * Hv) * 2 + ns * mean_rep * rec_row
+             + ns_rows * Hv * D * 2 + ns * (n * 2 * Hv * 2 + 2 * coef_bytes))
+    step_b = conv_b + pre_b + ver_b
+    # flops: about 7 Hv Dk Dv per row for the rule (3.7 MFLOP at these
+    # shapes), replayed rows included for the verify
+    fpr = 7 * Hv * sh.Dk * D
+    step_f = fpr * (T + ns * mean_rep)
+    hbm = float(peaks["hbm_gbs"])
+
+    def frac(b, ms):
+        return b / (ms / 1e3) / 1e9 / hbm
+
+    def ffrac(f, ms):
+        return f / (ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS
     return {"workload": f"mixed: 8 prefills of {int(lengths[ns:].min())}..{int(lengths[ns:].max())} "
                         f"tokens + {ns} spec requests x {n} rows, {T} rows, row map longest first",
-            "ms_per_step": el / K * 1e3, "tokens_per_s": T * K / el,
-            "conv_ms": statistics.mean(e[0].elapsed_time(e[1]) for e in evs),
-            "prefill_ms": statistics.mean(e[1].elapsed_time(e[2]) for e in evs),
-            "verify_ms": statistics.mean(e[2].elapsed_time(e[3]) for e in evs),
+            "ms_per_step": step_ms, "tokens_per_s": T * K / el,
+            "conv_ms": conv_ms, "prefill_ms": prefill_ms, "verify_ms": verify_ms,
             "ms_per_step_two_streams": el2 / K * 1e3, "tokens_per_s_two_streams": T * K / el2,
-            "longest_chain": int(lengths.max()), "status": int(status.item())}
+            "longest_chain": int(lengths.max()),
+            "longest_chain_prefill_ms": prefill_ms,
+            "bytes_per_step": step_b, "flops_per_step": step_f,
+            "hbm_frac": frac(step_b, step_ms), "fp32_frac": ffrac(step_f, step_ms),
+            "hbm_frac_two_streams": frac(step_b, el2 / K * 1e3),
+            "fp32_frac_two_streams": ffrac(step_f, el2 / K * 1e3),
+            "kernels": {
+                "conv": {"bytes": conv_b, "hbm_frac": frac(conv_b, conv_ms)},
+                "prefill": {"bytes": pre_b, "flops": fpr * np_rows,
+                            "hbm_frac": frac(pre_b, prefill_ms),
+                            "fp32_frac": ffrac(fpr * np_rows, prefill_ms)},
+                "verify": {"bytes": ver_b, "flops": fpr * (ns_rows + ns * mean_rep),
+                           "hbm_frac": frac(ver_b, verify_ms),
+                           "fp32_frac": ffrac(fpr * (ns_rows + ns * mean_rep), verify_ms)}},
+            "fp32_peak_tflops": FP32_PEAK_TFLOPS, "status": int(status.item())}
 
 
 def bench_long_seq(device, peaks, K=3, W=3):

@@ -7,7 +7,7 @@ never falls back to another implementation.
 
 Entry points (same names as the C ABI): ``gdn_conv``, ``gdn_seq``,
 ``gdn_decode``, ``gdn_prefill``, ``gdn_spec_verify``, ``gdn_spec_step``, ``gdn_spec_slots``,
-``gdn_chunk_prefill``,
+``gdn_chunk_prefill``, ``gdn_page_to_slots``, ``gdn_slots_to_page``,
 ``gdn_chunk_prefill_workspace_bytes``, ``gdn_page_layout``,
 ``gdn_slot_layout``, ``gdn_check_bounded_wait``, ``gdn_strerror``,
 ``gdn_abi_version``.
@@ -107,6 +107,8 @@ def load_library(path: str = LIB_PATH):
             "gdn_decode": ([D, B, PR, P, P, P, P, P, P, P, P], I),
             "gdn_prefill": ([D, B, PR, P, P, P, P, P, I, P, P], I),
             "gdn_spec_slots": ([D, B, PR, P, P, P, P, P, P, P, P, P], I),
+            "gdn_page_to_slots": ([D, I, P, P, I, I, P, P, P, P], I),
+            "gdn_slots_to_page": ([D, I, P, P, P, I, I, P, P, P, P], I),
             "gdn_chunk_prefill_workspace_bytes": ([D, B], S),
             "gdn_chunk_prefill": ([D, B, PR, P, P, P, P, P, P, S, P, P], I),
             "gdn_check_bounded_wait": ([ctypes.c_int64, P, P], I),
@@ -218,6 +220,22 @@ def gdn_spec_slots(dims, batch, params, x, conv_w, y, a, b, o, slots, status, st
                                          ctypes.byref(params), _ptr(x), _ptr(conv_w), _ptr(y),
                                          _ptr(a), _ptr(b), _ptr(o), _ptr(slots), _ptr(status),
                                          _stream(stream)), "gdn_spec_slots")
+
+
+def gdn_page_to_slots(dims, n, page, pool, num_pages, num_pools, pages, slots, status,
+                      stream=None):
+    _check(load_library().gdn_page_to_slots(ctypes.byref(dims), int(n), _ptr(page), _ptr(pool),
+                                            int(num_pages), int(num_pools), _ptr(pages),
+                                            _ptr(slots), _ptr(status), _stream(stream)),
+           "gdn_page_to_slots")
+
+
+def gdn_slots_to_page(dims, n, pool, slot, page, num_pools, num_pages, slots, pages, status,
+                      stream=None):
+    _check(load_library().gdn_slots_to_page(ctypes.byref(dims), int(n), _ptr(pool), _ptr(slot),
+                                            _ptr(page), int(num_pools), int(num_pages),
+                                            _ptr(slots), _ptr(pages), _ptr(status),
+                                            _stream(stream)), "gdn_slots_to_page")
 
 
 def gdn_chunk_prefill_workspace_bytes(dims, batch) -> int:

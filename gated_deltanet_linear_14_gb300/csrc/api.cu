@@ -277,6 +277,31 @@ gdn_status encode_rows_tmap(CUtensorMap* tm, const void* rows, int num_rows, con
   return r == CUDA_SUCCESS ? GDN_OK : GDN_ERR_UNSUPPORTED;
 }
 
+gdn_status handover_entry(int dir, const gdn_dims* dims, int32_t n, const int32_t* page,
+                          const int32_t* pool, const int32_t* slot, int32_t num_pages,
+                          int32_t num_pools, void* pages, void* slots, int32_t* status,
+                          gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
+  if (n < 0 || num_pages < 0 || num_pools < 0) return GDN_ERR_INVALID_ARG;
+  if (n > 65535) return GDN_ERR_UNSUPPORTED;
+  if (n == 0) return GDN_OK;
+  if (!page || !pool || (dir == 1 && !slot) || !pages || !slots || !status)
+    return GDN_ERR_INVALID_ARG;
+  const Geom G = make_geom(dims);
+  gdn_slot_layout_t SL;
+  slot_layout(dims, &SL);
+  const SlotGeom SG{SL.pool_bytes, SL.slot_bytes, SL.state_offset, SL.window_offset};
+  const size_t C = (size_t)G.C;
+  const size_t state_bytes = (size_t)G.Hv * G.Dv * G.Dk * dsize(dims->state_dtype);
+  const size_t window_bytes = (size_t)(G.W - 1) * C * dsize(dims->io_dtype);
+  if (launch_handover(G, SG, dir, n, page, pool, slot, num_pages, num_pools, pages, slots,
+                      state_bytes, window_bytes, status, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,6 +420,22 @@ gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gd
   if (spec(SPEC_SLOTS, G, B, P, SG, dims, y, nullptr, a, b, o, slots, status, s) != cudaSuccess)
     return GDN_ERR_LAUNCH;
   return GDN_OK;
+}
+
+gdn_status gdn_page_to_slots(const gdn_dims* dims, int32_t n, const int32_t* page,
+                             const int32_t* pool, int32_t num_pages, int32_t num_pools,
+                             const void* pages, void* slots, int32_t* status,
+                             gdn_stream_t stream) {
+  return handover_entry(0, dims, n, page, pool, nullptr, num_pages, num_pools,
+                        const_cast<void*>(pages), slots, status, stream);
+}
+
+gdn_status gdn_slots_to_page(const gdn_dims* dims, int32_t n, const int32_t* pool,
+                             const int32_t* slot, const int32_t* page, int32_t num_pools,
+                             int32_t num_pages, const void* slots, void* pages, int32_t* status,
+                             gdn_stream_t stream) {
+  return handover_entry(1, dims, n, page, pool, slot, num_pages, num_pools, pages,
+                        const_cast<void*>(slots), status, stream);
 }
 
 gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,

@@ -28,6 +28,13 @@ cudaError_t launch_decode(const Geom& G, const Batch& B, const Params& P, int io
                           const void* b, void* o, void* pages, int32_t* status,
                           cudaStream_t stream);
 
+// Page <-> slot pool hand-over (handover.cu). dir 0: page -> slot 0,
+// dir 1: slot slot[i] -> page.
+cudaError_t launch_handover(const Geom& G, const SlotGeom& SG, int dir, int n, const int32_t* page,
+                            const int32_t* pool, const int32_t* slot, int num_pages,
+                            int num_pools, void* pages, void* slots, size_t state_bytes,
+                            size_t window_bytes, int32_t* status, cudaStream_t stream);
+
 // Speculative decode in closed form (spec.cuh). mode: 0 = one-page verify
 // (rows = conv'd qkv), 1 = the same with the conv fused in (rows = raw x),
 // 2 = slot-per-candidate layout (rows = conv'd qkv, pages = slot pools).

@@ -310,6 +310,34 @@ gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch,
                           const void* b, void* o, void* slots,
                           int32_t* status, gdn_stream_t stream);
 
+/* Hand a request between the one-page layout and the slot layout. The
+ * r9700-stack v0.2.4 notes ("What it does") keep the stock per-candidate
+ * pages when prefix caching is on, so a request may move from its state page
+ * to a slot pool, or back, between steps. What moves is what the next step
+ * starts from: the state and the W-1 history columns of the conv window.
+ *
+ * gdn_page_to_slots: for i < n, copies page page[i] (of `pages`, num_pages
+ * pages) into slot 0 of slot pool pool[i] (of `slots`, num_pools pools); the
+ * next gdn_spec_slots step of the request resumes from slot 0 (n_accepted 0).
+ * The page's record must be closed (commit first, gdn_spec_verify with zero
+ * rows), else the request is skipped with GDN_DEV_RECORD_OPEN.
+ * gdn_slots_to_page: copies slot slot[i] (0 <= slot < max_candidates, e.g.
+ * the accepted candidate) of pool pool[i] into page page[i] and closes the
+ * page's record (empty record, step parity 0), so the next gdn_conv +
+ * gdn_spec_verify of the request runs with GDN_REQ_PARITY clear.
+ * page, pool, slot: device int32 [n]. Other device errors: GDN_DEV_BAD_PAGE
+ * (an index out of range), GDN_DEV_BAD_ACCEPTED (a slot out of range); the
+ * request is skipped. Requires max_candidates > 0 (else
+ * GDN_ERR_UNSUPPORTED) and n <= 65535. One launch on `stream`. */
+gdn_status gdn_page_to_slots(const gdn_dims* dims, int32_t n, const int32_t* page,
+                             const int32_t* pool, int32_t num_pages, int32_t num_pools,
+                             const void* pages, void* slots, int32_t* status,
+                             gdn_stream_t stream);
+gdn_status gdn_slots_to_page(const gdn_dims* dims, int32_t n, const int32_t* pool,
+                             const int32_t* slot, const int32_t* page, int32_t num_pools,
+                             int32_t num_pages, const void* slots, void* pages,
+                             int32_t* status, gdn_stream_t stream);
+
 /* Workspace bytes gdn_chunk_prefill needs for this batch (host only;
  * depends on num_requests and max_rows). */
 size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims,

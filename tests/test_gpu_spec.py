@@ -391,10 +391,10 @@ def test_one_page_bit_identical_to_slots_small_record(Kc):
 @pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
 def test_switch_to_slot_layout_midstream(state):
     """Prefix caching keeps the stock per-candidate pages (r9700-stack v0.2.4,
-    "What it does"): a request that ran one-page steps is committed, its
-    page's state and window are copied into slot 0 of a slot pool, and the
-    slot layout continues from there, bit-identical to a request that used
-    the slot layout from the start."""
+    "What it does"): a request that ran one-page steps is committed, handed to
+    slot 0 of a slot pool by gdn_page_to_slots, and the slot layout continues
+    from there, bit-identical to a request that used the slot layout from the
+    start."""
     d = synth.spec(R=4, steps=4)
     R, n = 4, d["n"]
     start, ln = d["row_start"][:R], d["row_len"][:R]
@@ -415,9 +415,12 @@ def test_switch_to_slot_layout_midstream(state):
     L1.ok()
     L3 = Layer(d["shapes"], d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
                num_pages=R, slots=True)
+    idx = to_dev(np.arange(R, dtype=np.int32))
+    gdn.gdn_page_to_slots(L1.dims, R, idx, idx, R, R, L1.pool.buf, L3.slots.buf, L3.status)
+    L3.ok()
     for r in range(R):
-        L3.slots.state(r, 0).copy_(L1.pool.state(r))
-        L3.slots.window(r, 0).copy_(L1.pool.window(r)[:3])
+        assert torch.equal(L3.slots.state(r, 0), L1.pool.state(r))
+        assert torch.equal(L3.slots.window(r, 0), L1.pool.window(r)[:3])
     x, a, b = step_rows(d, 2, R, n)
     y2, o2 = L2.spec_slots(L2.batch(start, ln, flags=spec_flags(2, R), n_accepted=acc), x, a, b)
     y3, o3 = L3.spec_slots(L3.batch(start, ln, flags=spec_flags(2, R), n_accepted=zero), x, a, b)
@@ -595,3 +598,43 @@ def test_fused_step_device_errors_leave_the_page_alone():
     L.spec_step(L.batch(start, ln, flags=flags, n_accepted=d["accepted"][1]), x, a, b)
     assert L.status_code() == gdn.CODES["GDN_DEV_STALE_STEP"]
     assert torch.equal(before, _page(L, 2))
+
+
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_slots_to_page_and_back_midstream(state):
+    """The other direction: a request that ran slot-layout steps is handed
+    back to a page from its accepted slot (gdn_slots_to_page) and continues
+    one-page, bit-identical to a request that stayed in the slot layout; a
+    page with an open record refuses gdn_page_to_slots."""
+    d = synth.spec(R=4, steps=5)
+    R, n = 4, d["n"]
+    start, ln = d["row_start"][:R], d["row_len"][:R]
+    _, L2, _ = make_layers(d, R, state)             # slots throughout
+    L4, _, _ = make_layers(d, R, state, slots=False)  # pages for the hand-back
+    L5 = Layer(d["shapes"], d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, state=state,
+               num_pages=R, slots=True)
+    for s in range(2):
+        x, a, b = step_rows(d, s, R, n)
+        acc = d["accepted"][s][:R] if s else np.zeros(R, np.int32)
+        L2.spec_slots(L2.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc), x, a, b)
+        L2.ok()
+    acc = d["accepted"][2][:R]
+    idx = to_dev(np.arange(R, dtype=np.int32))
+    gdn.gdn_slots_to_page(L2.dims, R, idx, to_dev(acc), idx, R, R, L2.slots.buf, L4.pool.buf,
+                          L4.status)
+    L4.ok()
+    for r in range(R):
+        assert np.array_equal(bits(L4.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
+        assert int(L4.pool.flag(r).item()) == 0
+    # step 2 both ways: slots resume from the accepted slot, the page starts fresh
+    x, a, b = step_rows(d, 2, R, n)
+    _, o2 = L2.spec_slots(L2.batch(start, ln, flags=spec_flags(2, R), n_accepted=acc), x, a, b)
+    _, o4 = one_page_step(L4, start, ln, spec_flags(0, R), np.zeros(R, np.int32), x, a, b)
+    L2.ok()
+    L4.ok()
+    assert np.array_equal(bits(o2), bits(o4))
+    # an open record is not handed over
+    before = L5.slots.buf.clone()
+    gdn.gdn_page_to_slots(L4.dims, R, idx, idx, R, R, L4.pool.buf, L5.slots.buf, L5.status)
+    assert L5.status_code() == gdn.CODES["GDN_DEV_RECORD_OPEN"]
+    assert torch.equal(before, L5.slots.buf)
