@@ -215,85 +215,97 @@ __device__ __forceinline__ float through(float x) { return to_f(from_f<T>(x)); }
 // The conv's SiLU must be reproducible bit for bit by a plain CPU program, so
 // it uses no CUDA math-library function and no division or reciprocal of the
 // compiler: only IEEE additions, multiplications and fused multiply-adds,
-// rounded to nearest even, in a fixed order.
+// rounded to nearest even, in a fixed order, and exact operations on bit
+// patterns.
 //
-// SiLU(z) = z sigmoid(z). With t = e^{-|z|} in [0, 1] and d = 1 + t in
-// [1, 2], sigmoid(z) is 1/d for z >= 0 and t/d for z < 0, so exp is only
-// taken of a non-positive argument and the reciprocal only of a number in
-// [1, 2].
+// SiLU(z) = z sigmoid(z). With a = |z| (at most 104), t = e^{-a} in [0, 1]
+// and d = 1 + t in [1, 2], sigmoid(z) is t/d for z < 0 and 1 - t/d for
+// z >= 0, so with c = max(z, 0)
+//     SiLU(z) = c - a (t/d)
+// for either sign: exp is only taken of a non-positive argument and the
+// reciprocal only of a number in [1, 2]. The chain carries -t, -d and -t/d;
+// negation is exact and rounding to nearest is symmetric, so every value has
+// the roundings of its positive form.
 //
-// exp of a <= 0: Cody and Waite's argument reduction (Cody & Waite, "Software
-// Manual for the Elementary Functions", 1980): a = n ln2 + r, n =
-// round-to-even(a log2 e), ln2 split into a 12-bit-trimmed high part and a
-// low correction; e^r from the Taylor series through r^7 (coefficients 1/k!),
-// Horner's rule with fused multiply-adds, the coefficients scaled by 2^-64
-// (exactly, so the polynomial comes out as p 2^-64 with p's own roundings);
-// then one product with 2^(n+64), which rounds once, and only where e^a is
-// subnormal. a is first raised to -104, below which e^a is under half the
-// smallest subnormal and rounds to 0.
+// e^{-a}: Cody and Waite's argument reduction (Cody & Waite, "Software Manual
+// for the Elementary Functions", 1980): -a = n ln2 + r with n the integer
+// nearest -a log2 e, found by one fused multiply-add against 1.5 2^23 (where
+// the spacing of floats is 1: the low bits of the sum's pattern are then n);
+// ln2 is split into a high part with its low 12 mantissa bits cleared, so
+// that n ln2_hi is exact, and a low correction. e^r, |r| <= ln2/2, comes from
+// the degree-6 polynomial of least maximum relative error with its first two
+// coefficients held at 1, fitted by the Remez exchange algorithm; the free
+// coefficients were rounded to float one at a time from c2 upwards, the
+// remaining ones refitted after each rounding, for a relative error of
+// 3.31e-9 (2^-28.2) with the rounded values below. Horner's rule in -r (the
+// odd coefficients negated) with fused multiply-adds, every coefficient
+// scaled by 2^-64 (exactly, so the polynomial comes out as p 2^-64 with p's
+// own roundings); then one product with -2^(n+64), which rounds once, and
+// only where e^{-a} is subnormal. At a = 104 the result is 0 (e^-104 is under
+// half the smallest subnormal). Over every float a in [0, 104] the result is
+// within 0.90 ulp of e^{-a} where that is a normal float and within 0.86 of
+// the subnormal spacing below.
 //
-// 1/d: the Newton-Raphson reciprocal iteration of Newton-Raphson division:
-// the linear seed 24/17 - (8/17) d (relative error at most 1/17 on [1, 2]),
-// then two steps r <- r + r (1 - d r), each squaring the relative error
-// (about 4, 8, then 16 bits). The quotient q = num r (num = 1 or t) is then
-// corrected once, q <- q + r (num - d q), which squares the error again
-// (about 33 bits before rounding).
-__host__ __device__ constexpr float recip_factorial(int k) {
-  double f = 1.0;
-  for (int i = 2; i <= k; ++i) f *= i;
-  return (float)(1.0 / f);
+// 1/d: the quadratic of least maximum relative error to 1/d on [1, 2],
+// 70/33 - (16/11) d + (32/99) d^2 (relative error at most 1/99,
+// equioscillating at 1, 5/4, 7/4 and 2), one Newton-Raphson step r <- r + r (1 - d r)
+// (error about 1e-4), then the quotient t r corrected once,
+// q <- q + r (t - d q) (about 1e-8 before rounding). Over every float z with
+// |z| <= 104 the SiLU is within 3.32 ulp where |z| <= 87 and the result is a
+// normal float of at least 2^-124, and within 2^-142 absolutely elsewhere.
+//
+// c = max(z, 0) is taken on the bit pattern (a signed-integer maximum with
+// 0): it is z for z > 0 and +0 for every z with the sign bit set. A NaN z
+// keeps a = NaN, so the result is NaN; z = +inf gives +inf.
+namespace silu_consts {
+constexpr float kLog2e = 0x1.715476p+0f;        // float(1 / ln 2)
+constexpr float kLn2Hi = 0x1.62ep-1f;           // ln 2, low 12 mantissa bits cleared
+constexpr float kLn2Lo = 0x1.0bfbe8p-15f;       // float(ln 2 - kLn2Hi)
+constexpr float kRound = 12582912.0f;           // 1.5 2^23
+constexpr float kC2 = 0x1.fffffcp-2f, kC3 = 0x1.55548cp-3f, kC4 = 0x1.555858p-5f,
+                kC5 = 0x1.123e26p-7f, kC6 = 0x1.6ace9ap-10f;   // c0 = c1 = 1
+constexpr float kS0 = (float)(70.0 / 33.0), kS1 = (float)(16.0 / 11.0), kS2 = (float)(32.0 / 99.0);
+}  // namespace silu_consts
+
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// min(|z|, 104), a NaN stays NaN
+__device__ __forceinline__ float silu_arg(float z) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(z)), "f"(104.0f));
+  return r;
 }
 
-// ln 2 = 0.693147180559945309417...; its float value is 0x3F317218. The high
-// part keeps that pattern with the low 12 mantissa bits cleared (0x3F317000),
-// the low part is ln 2 minus the high part, rounded to float.
-//
-// own_exp2_nonpos evaluates that exp on two values a <= 0 at once, the
-// floating-point steps in packed f32x2 form (each value sees exactly the
-// roundings of the method above, which is what a CPU program reproduces).
-// n = round-to-even(t) comes from m = t + 1.5 2^23: for |t| <= 151, m lies
-// where the spacing of floats is 1, so the addition rounds t to the nearest
-// integer, ties to even; n = m - 1.5 2^23 exactly, and the low 9 bits of m's
-// pattern are n mod 512, so adding 127 + 64 and shifting them into the
-// exponent field gives the pattern of 2^(n+64).
-__device__ __forceinline__ float2 own_exp2_nonpos(float2 a) {
-  constexpr double kLn2 = 0.693147180559945309417232121458176568;
-  const float log2e = (float)(1.0 / kLn2);
-  const float ln2_hi = __uint_as_float(0x3F317000u);
-  const float ln2_lo = (float)(kLn2 - (double)0.693115234375);
-  const float kRound = 12582912.0f;  // 1.5 2^23
-  a = make_float2(fmaxf(a.x, -104.0f), fmaxf(a.y, -104.0f));
-  const float2 t = __fmul2_rn(a, make_float2(log2e, log2e));
-  const float2 m = __fadd2_rn(t, make_float2(kRound, kRound));
-  const float2 n = __fadd2_rn(m, make_float2(-kRound, -kRound));
-  float2 r = __ffma2_rn(n, make_float2(-ln2_hi, -ln2_hi), a);
-  r = __ffma2_rn(n, make_float2(-ln2_lo, -ln2_lo), r);
-  const float c7 = recip_factorial(7) * 0x1p-64f;
-  float2 p = make_float2(c7, c7);
-#pragma unroll
-  for (int k = 6; k >= 0; --k) {
-    const float ck = recip_factorial(k) * 0x1p-64f;
-    p = __ffma2_rn(p, r, make_float2(ck, ck));
-  }
-  const float2 s = make_float2(__uint_as_float((__float_as_uint(m.x) + 191u) << 23),
-                               __uint_as_float((__float_as_uint(m.y) + 191u) << 23));
-  return __fmul2_rn(p, s);
-}
-
-// SiLU on two values (the method above).
+// SiLU on two values (the method above), the floating-point steps in packed
+// f32x2 form; each value sees exactly the roundings of the scalar steps.
 __device__ __forceinline__ float2 own_silu2(float2 z) {
-  const float2 one = make_float2(1.0f, 1.0f);
-  const float2 t = own_exp2_nonpos(make_float2(-fabsf(z.x), -fabsf(z.y)));
-  const float2 d = __fadd2_rn(one, t);
-  const float2 nd = make_float2(-d.x, -d.y);
-  const float s0 = (float)(24.0 / 17.0), s1 = (float)(8.0 / 17.0);
-  float2 r = __ffma2_rn(make_float2(-s1, -s1), d, make_float2(s0, s0));
-#pragma unroll
-  for (int i = 0; i < 2; ++i) r = __ffma2_rn(r, __ffma2_rn(nd, r, one), r);
-  const float2 num = make_float2(z.x >= 0.0f ? 1.0f : t.x, z.y >= 0.0f ? 1.0f : t.y);
-  float2 q = __fmul2_rn(num, r);
-  q = __ffma2_rn(r, __ffma2_rn(nd, q, num), q);
-  return __fmul2_rn(z, q);
+  using namespace silu_consts;
+  constexpr float s = 0x1p-64f;
+  const float2 a = make_float2(silu_arg(z.x), silu_arg(z.y));
+  const float2 m = __ffma2_rn(a, splat2(-kLog2e), splat2(kRound));
+  const float2 n = __fadd2_rn(m, splat2(-kRound));
+  float2 r = __ffma2_rn(n, splat2(kLn2Hi), a);   // a + n ln2 = -r
+  r = __ffma2_rn(n, splat2(kLn2Lo), r);
+  float2 p = splat2(kC6 * s);
+  p = __ffma2_rn(p, r, splat2(-kC5 * s));
+  p = __ffma2_rn(p, r, splat2(kC4 * s));
+  p = __ffma2_rn(p, r, splat2(-kC3 * s));
+  p = __ffma2_rn(p, r, splat2(kC2 * s));
+  p = __ffma2_rn(p, r, splat2(-1.0f * s));
+  p = __ffma2_rn(p, r, splat2(1.0f * s));
+  // -2^(n+64): the low 9 bits of m's pattern are n mod 512; 447 = 256 + 191
+  // puts 64 + 127 into the exponent field and sets the sign bit
+  const float2 negs = make_float2(__uint_as_float((__float_as_uint(m.x) << 23) + (447u << 23)),
+                                  __uint_as_float((__float_as_uint(m.y) << 23) + (447u << 23)));
+  const float2 nt = __fmul2_rn(p, negs);           // -t
+  const float2 nd = __fadd2_rn(nt, splat2(-1.0f));  // -d
+  float2 rc = __ffma2_rn(__ffma2_rn(splat2(kS2), nd, splat2(kS1)), nd, splat2(kS0));
+  rc = __ffma2_rn(rc, __ffma2_rn(nd, rc, splat2(1.0f)), rc);
+  float2 nq = __fmul2_rn(nt, rc);                  // -t/d
+  nq = __ffma2_rn(rc, __ffma2_rn(nd, nq, nt), nq);
+  const float2 c = make_float2(__int_as_float(max(__float_as_int(z.x), 0)),
+                               __int_as_float(max(__float_as_int(z.y), 0)));
+  return __ffma2_rn(a, nq, c);
 }
 
 // ----------------------------------------------------------------- gates

@@ -27,19 +27,30 @@
 
 namespace gdn {
 
-constexpr int kConvThreads = 128;
-// The exact SiLU (own exp and reciprocal per element) makes the conv bound
-// by its floating-point pipe rather than by HBM, so residency matters more
-// than wide vectors or deep load batches: 8-byte vectors, 4 rows in flight
-// and 8 CTAs (32 warps) per SM ran a 32k-row batch in 0.50 ms, against
-// 0.57 ms with 8 rows in flight and 0.68 ms with 16-byte vectors at 3 CTAs
-// per SM (with the earlier, division-based SiLU).
+// The exact SiLU (own exp and reciprocal per element) keeps the conv's
+// floating-point pipe busier than its HBM traffic, so the kernel is built to
+// keep that pipe fed: channel pairs in packed f32x2 form, 8-byte vectors, 4
+// CTAs of 256 threads per SM (32 warps), and the input rows staged into
+// shared memory by each thread's own cp.async two batches ahead, so the
+// arithmetic of a batch never waits for its loads.
+constexpr int kConvThreads = 256;
 constexpr int kConvVecBytes = 8;
-constexpr int kConvRows = 32;  // rows per tile (>= W-1)
-constexpr int kConvBatch = 4;  // rows whose loads are in flight together
+constexpr int kConvRows = 32;   // rows per tile (>= W-1)
+constexpr int kConvBatch = 4;   // rows per ring stage
+constexpr int kConvStages = 3;  // ring stages: the batch in use and two in flight
+
+__device__ __forceinline__ void conv_cp8(void* smem, const void* gmem) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(d), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void conv_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// wait until at most kConvStages - 1 groups of this thread are pending
+__device__ __forceinline__ void conv_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kConvStages - 1) : "memory");
+}
 
 template <class IO, class YT, int W, bool SLOTS>
-__global__ void __launch_bounds__(kConvThreads, 8)
+__global__ void __launch_bounds__(kConvThreads, 4)
 conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
             const IO* __restrict__ w, YT* __restrict__ y, void* pages, int32_t* status) {
   pdl_begin();
@@ -100,6 +111,27 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
   const int c0 = (blockIdx.x * kConvThreads + threadIdx.x) * V;
   if (c0 >= G.C) return;
 
+  // Each thread copies its own 8-byte vector of every row into its own
+  // column of the ring and reads back only that, so its cp.async waits are
+  // the only ordering needed (no block-wide barrier). Every copy is issued
+  // here, after the last early return, and waited for before the end.
+  __shared__ uint2 ring[kConvStages][kConvBatch][kConvThreads];
+  const int t_end = min(q.len, t0 + kConvRows);
+  const int nb = (t_end - t0 + kConvBatch - 1) / kConvBatch;
+  const IO* xr = x + (size_t)q.start * G.C + c0;  // row t at xr + t C
+  auto issue = [&](int b) {
+    if (b < nb) {
+#pragma unroll
+      for (int i = 0; i < kConvBatch; ++i) {
+        const int t = t0 + b * kConvBatch + i;
+        if (t < t_end) conv_cp8(&ring[b % kConvStages][i][threadIdx.x], xr + (size_t)t * G.C);
+      }
+    }
+    conv_commit();
+  };
+#pragma unroll
+  for (int b = 0; b < kConvStages - 1; ++b) issue(b);
+
   // taps and bias
   float wt[W][V];
   {
@@ -121,7 +153,7 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
   for (int j = 0; j < H; ++j) {
     const int pos = t0 - H + j;
     if (pos >= 0) {
-      load_f<IO, V>(x + (size_t)(q.start + pos) * G.C + c0, h[j]);
+      load_f<IO, V>(xr + (size_t)pos * G.C, h[j]);
     } else if (hist_src) {
       load_f<IO, V>(hist_src + (size_t)(H + pos) * G.C + c0, h[j]);
     } else {
@@ -130,61 +162,12 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
     }
   }
 
-  // rows in groups of kConvBatch: all loads of a group are issued before any
-  // of its arithmetic, so each thread keeps kConvBatch x 16 bytes in flight
-  const int t_end = min(q.len, t0 + kConvRows);
-  for (int tb = t0; tb < t_end; tb += kConvBatch) {
-    uint2 raw[kConvBatch];
-#pragma unroll
-    for (int i = 0; i < kConvBatch; ++i)
-      if (tb + i < t_end)
-        raw[i] = *reinterpret_cast<const uint2*>(x + (size_t)(q.start + tb + i) * G.C + c0);
-#pragma unroll
-    for (int i = 0; i < kConvBatch; ++i) {
-      const int t = tb + i;
-      if (t >= t_end) break;
-      float xv[V];
-      {
-        const IO* e = reinterpret_cast<const IO*>(&raw[i]);
-#pragma unroll
-        for (int v = 0; v < V; ++v) xv[v] = to_f(e[v]);
-      }
-      // channel pairs in packed f32x2 form: each channel sees the same
-      // fused multiply-adds, in the same order, as a scalar loop would
-      float yv[V];
-#pragma unroll
-      for (int v = 0; v < V; v += 2) {
-        float2 acc = make_float2(bias[v], bias[v + 1]);
-#pragma unroll
-        for (int j = 0; j < H; ++j)
-          acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]), make_float2(h[j][v], h[j][v + 1]), acc);
-        acc = __ffma2_rn(make_float2(wt[H][v], wt[H][v + 1]), make_float2(xv[v], xv[v + 1]), acc);
-        const float2 y2 = own_silu2(acc);
-        yv[v] = y2.x;
-        yv[v + 1] = y2.y;
-      }
-      store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
-#pragma unroll
-      for (int j = 0; j < H - 1; ++j)
-#pragma unroll
-        for (int v = 0; v < V; ++v) h[j][v] = h[j + 1][v];
-#pragma unroll
-      for (int v = 0; v < V; ++v) h[H - 1][v] = xv[v];
-      if constexpr (!SLOTS) {
-        if (rec_out) store_f<IO, V>(rec_out + (size_t)t * G.rec_row + c0, yv);
-      } else {
-        // window after candidate t goes to slot t
-        IO* wdst = reinterpret_cast<IO*>(pool + (size_t)t * SG.slot_bytes + SG.window_off);
-#pragma unroll
-        for (int j = 0; j < H; ++j) store_f<IO, V>(wdst + (size_t)j * G.C + c0, h[j]);
-      }
-    }
-  }
-
-  if constexpr (!SLOTS) {
-    if (blockIdx.y != 0) return;
-    // The window channels [c0, c0+V) are read and written only by this
-    // thread, so the initial history can be read again here.
+  // The new window. The window channels [c0, c0+V) are read and written
+  // only by this thread of row tile 0, which has already taken its history
+  // into registers; the history is read again here where the new window
+  // keeps some of it. Writing it before the rows keeps its pointers out of
+  // the main loop.
+  if (!SLOTS && blockIdx.y == 0) {
     if (q.spec) {
       // columns 0..H-1 keep the history this step started from; the raw
       // candidates follow, so the next step can roll by its accepted count
@@ -219,6 +202,65 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
       }
     }
   }
+
+  // one row: taps, SiLU, stores, then the window slides by one. rec is a
+  // constant at each call, so the full-batch path below has no branch
+  // between its rows and their arithmetic interleaves.
+  auto row = [&](const uint2 raw, int t, bool rec) {
+    float xv[V];
+    {
+      const IO* e = reinterpret_cast<const IO*>(&raw);
+#pragma unroll
+      for (int v = 0; v < V; ++v) xv[v] = to_f(e[v]);
+    }
+    // channel pairs in packed f32x2 form: each channel sees the same fused
+    // multiply-adds, in the same order, as a scalar loop would
+    float yv[V];
+#pragma unroll
+    for (int v = 0; v < V; v += 2) {
+      float2 acc = make_float2(bias[v], bias[v + 1]);
+#pragma unroll
+      for (int j = 0; j < H; ++j)
+        acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]), make_float2(h[j][v], h[j][v + 1]), acc);
+      acc = __ffma2_rn(make_float2(wt[H][v], wt[H][v + 1]), make_float2(xv[v], xv[v + 1]), acc);
+      const float2 y2 = own_silu2(acc);
+      yv[v] = y2.x;
+      yv[v + 1] = y2.y;
+    }
+    store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
+#pragma unroll
+    for (int j = 0; j < H - 1; ++j)
+#pragma unroll
+      for (int v = 0; v < V; ++v) h[j][v] = h[j + 1][v];
+#pragma unroll
+    for (int v = 0; v < V; ++v) h[H - 1][v] = xv[v];
+    if constexpr (!SLOTS) {
+      if (rec) store_f<IO, V>(rec_out + (size_t)t * G.rec_row + c0, yv);
+    } else {
+      // window after candidate t goes to slot t
+      IO* wdst = reinterpret_cast<IO*>(pool + (size_t)t * SG.slot_bytes + SG.window_off);
+#pragma unroll
+      for (int j = 0; j < H; ++j) store_f<IO, V>(wdst + (size_t)j * G.C + c0, h[j]);
+    }
+  };
+
+  for (int b = 0; b < nb; ++b) {
+    issue(b + kConvStages - 1);
+    conv_wait();  // batch b has landed
+    const int tb = t0 + b * kConvBatch;
+    const int s = b % kConvStages;
+    if (tb + kConvBatch <= t_end && rec_out == nullptr) {
+      // a full batch of plain rows
+#pragma unroll
+      for (int i = 0; i < kConvBatch; ++i) row(ring[s][i][threadIdx.x], tb + i, false);
+    } else {
+      // the ragged end of a tile, or candidate rows that also go to the record
+#pragma unroll
+      for (int i = 0; i < kConvBatch; ++i)
+        if (tb + i < t_end) row(ring[s][i][threadIdx.x], tb + i, rec_out != nullptr);
+    }
+  }
+
 }
 
 template <class IO, class YT, bool SLOTS>

@@ -187,31 +187,37 @@ void parallel_for(long n, int threads, F f) {
 
 // ------------------------------------------------------- fp32 conv mirror
 //
-// SiLU(x) = x sigmoid(x), evaluated as the GPU conv does, step for step.
-// With t = e^{-|x|} in [0, 1] and d = 1 + t in [1, 2], sigmoid(x) is 1/d for
-// x >= 0 and t/d for x < 0: exp is only taken of a non-positive argument and
-// the reciprocal only of a number in [1, 2].
+// SiLU(z) = z sigmoid(z), evaluated as the GPU conv does, step for step.
+// With a = |z| (raised to at most 104), t = e^{-a} in [0, 1] and
+// d = 1 + t in [1, 2], sigmoid(z) = t/d for z < 0 and 1 - t/d for z >= 0, so
+// with c = max(z, 0):
+//     SiLU(z) = c - a (t/d)
+// for both signs: exp is only taken of a non-positive argument and the
+// reciprocal only of a number in [1, 2]. The chain below carries -t, -d and
+// -t/d (negation is exact, so each value has the roundings of its positive
+// form).
 //
-// exp of a <= 0: Cody & Waite argument reduction (W. J. Cody and W. Waite,
-// "Software Manual for the Elementary Functions", 1980): a = n ln2 + r with
-// n = round(a / ln2) and ln2 split into a short high part and a low
-// correction so n*ln2_hi is exact; e^r from its Taylor series, truncated
-// after the r^7 term and evaluated by Horner's rule with fused multiply-adds,
-// its coefficients scaled by 2^-64 (exactly: the result is p 2^-64 with p's
-// own roundings); then one product with 2^(n+64), which rounds once, and
-// only where e^a is subnormal. a is first raised to -104, below which e^a is
-// under half the smallest subnormal and rounds to 0.
+// e^{-a}: Cody & Waite argument reduction (W. J. Cody and W. Waite,
+// "Software Manual for the Elementary Functions", 1980): -a = n ln2 + r with
+// n the nearest integer to -a log2(e) (one fused multiply-add against
+// 1.5 2^23, where the spacing of floats is 1), ln2 split into a short high
+// part and a low correction so n*ln2_hi is exact; e^r from the degree-6
+// polynomial of least maximum relative error on |r| <= ln2/2 with its first
+// two coefficients held at 1 (Remez exchange, coefficients rounded to float
+// one at a time from the highest-order free one, refitting the rest after
+// each rounding; relative error 3.31e-9 = 2^-28.2 with the rounded
+// coefficients), by Horner's rule with fused multiply-adds, the coefficients
+// scaled by 2^-64 (exactly); then one product with -2^(n+64), which rounds
+// once, and only where e^{-a} is subnormal. At a = 104 the result is 0.
 //
-// 1/d: Newton-Raphson reciprocal iteration (the textbook Newton-Raphson
-// division method): the linear seed 24/17 - (8/17) d, within relative error
-// 1/17 of 1/d on [1, 2], then two steps r <- r + r (1 - d r), each of which
-// squares the relative error (about 4, 8, then 16 bits). The quotient
-// q = num * r (num = 1 or t) is corrected once, q <- q + r (num - d q), which
-// squares it again (about 33 bits before rounding).
+// 1/d: the quadratic of least maximum relative error to 1/d on [1, 2]
+// (70/33 - (16/11) d + (32/99) d^2, error at most 1/99), one Newton-Raphson
+// step r <- r + r (1 - d r) (error about 1e-4), then the quotient q = t r
+// corrected once, q <- q + r (t - d q) (about 1e-8 before rounding).
 struct OwnExpConsts {
   float log2e, ln2_hi, ln2_lo;
-  float c[8];  // 1/k!, k = 0..7
-  float seed0, seed1;  // 24/17, 8/17
+  float c[7];     // e^r ~ sum c_k r^k, |r| <= ln2/2
+  float seed[3];  // 70/33, 16/11, 32/99
   OwnExpConsts() {
     const double ln2 = std::log(2.0);
     log2e = (float)(1.0 / ln2);
@@ -224,13 +230,12 @@ struct OwnExpConsts {
     std::memcpy(&hi, &bits, 4);
     ln2_hi = hi;
     ln2_lo = (float)(ln2 - (double)hi);
-    double f = 1.0;
-    for (int k = 0; k < 8; ++k) {
-      if (k > 0) f *= k;
-      c[k] = (float)(1.0 / f);
-    }
-    seed0 = (float)(24.0 / 17.0);
-    seed1 = (float)(8.0 / 17.0);
+    const float fit[7] = {1.0f, 1.0f, 0x1.fffffcp-2f, 0x1.55548cp-3f, 0x1.555858p-5f,
+                          0x1.123e26p-7f, 0x1.6ace9ap-10f};
+    for (int k = 0; k < 7; ++k) c[k] = fit[k];
+    seed[0] = (float)(70.0 / 33.0);
+    seed[1] = (float)(16.0 / 11.0);
+    seed[2] = (float)(32.0 / 99.0);
   }
 };
 const OwnExpConsts kExp;
@@ -242,32 +247,45 @@ float pow2_exact(int n) {  // 2^n for -126 <= n <= 127, built from the bits
   return f;
 }
 
-// e^a for a <= 0 (a NaN is treated as -104, like the GPU's fmaxf).
-float own_exp_nonpos_f32(float a) {
-  a = std::fmax(a, -104.0f);
-  const float t = a * kExp.log2e;        // one rounding, no contraction
-  const float n = std::nearbyint(t);     // round half to even (default mode)
-  float r = std::fma(-n, kExp.ln2_hi, a);
-  r = std::fma(-n, kExp.ln2_lo, r);
+// -e^{-a} for 0 <= a <= 104 (the caller clamps).
+float own_negexp_f32(float a) {
+  const float kRound = 12582912.0f;                    // 1.5 2^23
+  const float m = std::fma(a, -kExp.log2e, kRound);   // n + 1.5 2^23, n = round(-a log2 e)
+  const float n = m - kRound;                          // exact
+  float r = std::fma(n, kExp.ln2_hi, a);               // a + n ln2 = -r
+  r = std::fma(n, kExp.ln2_lo, r);
+  // Horner in -r with the odd coefficients negated: the same roundings as
+  // Horner in r
   const float s = pow2_exact(-64);
-  float p = kExp.c[7] * s;
-  for (int k = 6; k >= 0; --k) p = std::fma(p, r, kExp.c[k] * s);
-  return p * pow2_exact((int)n + 64);
+  float p = (kExp.c[6] * s);
+  for (int k = 5; k >= 0; --k) p = std::fma(p, r, ((k & 1) ? -kExp.c[k] : kExp.c[k]) * s);
+  return p * -pow2_exact((int)n + 64);
 }
 
-float silu_own_f32(float x) {
-  const float t = own_exp_nonpos_f32(-std::fabs(x));
-  const float d = 1.0f + t;
-  float r = std::fma(-kExp.seed1, d, kExp.seed0);
-  for (int i = 0; i < 2; ++i) {
-    const float e = std::fma(-d, r, 1.0f);
-    r = std::fma(r, e, r);
-  }
-  const float num = (x >= 0.0f) ? 1.0f : t;
-  float q = num * r;
-  const float e = std::fma(-d, q, num);
-  q = std::fma(r, e, q);
-  return x * q;
+// a = min(|z|, 104); a NaN stays NaN.
+float silu_arg(float z) { return std::isnan(z) ? z : std::fmin(std::fabs(z), 104.0f); }
+
+float silu_own_f32(float z) {
+  const float a = silu_arg(z);
+  const float negt = std::isnan(a) ? a : own_negexp_f32(a);
+  const float N = negt - 1.0f;                         // -d
+  // 70/33 - (16/11) d + (32/99) d^2 in -d
+  float r = std::fma(std::fma(kExp.seed[2], N, kExp.seed[1]), N, kExp.seed[0]);
+  r = std::fma(r, std::fma(N, r, 1.0f), r);            // one Newton-Raphson step
+  float nq = negt * r;                                 // -t/d
+  nq = std::fma(r, std::fma(N, nq, negt), nq);         // corrected once
+  int32_t zb;
+  std::memcpy(&zb, &z, 4);
+  const int32_t cb = zb > 0 ? zb : 0;                  // max(z, 0) on the bit pattern
+  float c;
+  std::memcpy(&c, &cb, 4);
+  return std::fma(a, nq, c);
+}
+
+// e^x for x <= 0 through the same steps (x NaN is treated as -104).
+float own_exp_nonpos_f32(float x) {
+  const float a = std::fmin(-x, 104.0f);
+  return -own_negexp_f32(std::isnan(a) ? 104.0f : a);
 }
 
 }  // namespace
