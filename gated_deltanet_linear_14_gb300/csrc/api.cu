@@ -500,15 +500,15 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_p
 
 size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims, const gdn_batch* batch) {
   if (check_dims(dims) != GDN_OK || check_batch(batch, true) != GDN_OK) return 0;
-  return 0;
+  if (dims->io_dtype != GDN_BF16 || dims->head_k_dim != 128 || dims->head_v_dim != 128) return 0;
+  const size_t chunks = ((size_t)batch->max_rows + 63) / 64;
+  return (size_t)batch->num_requests * (size_t)dims->num_v_heads * chunks * gdn::kChunkItemBytes;
 }
 
 gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
                              const void* qkv, const void* a, const void* b, void* o, void* pages,
                              void* workspace, size_t workspace_bytes, int32_t* status,
                              gdn_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   gdn_status e = check_dims(dims);
   if (e != GDN_OK) return e;
   if ((e = check_batch(batch, true)) != GDN_OK) return e;
@@ -529,6 +529,17 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch, const
   const Geom G = make_geom(dims);
   const Batch B = make_batch(batch);
   const Params P = make_params(params, dims);
+  const size_t need = gdn_chunk_prefill_workspace_bytes(dims, batch);
+  if (workspace && need > 0) {
+    if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (((uintptr_t)workspace & 15) != 0) return GDN_ERR_INVALID_ARG;
+    const int ws_chunks = (batch->max_rows + 63) / 64;
+    if (launch_chunk2(&tmap, G, B, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32,
+                      a, b, o, pages, workspace, ws_chunks, status,
+                      (cudaStream_t)stream) != cudaSuccess)
+      return GDN_ERR_LAUNCH;
+    return GDN_OK;
+  }
   if (launch_chunk(&tmap, G, B, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a, b,
                    o, pages, status, (cudaStream_t)stream) != cudaSuccess)
     return GDN_ERR_LAUNCH;

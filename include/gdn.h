@@ -338,8 +338,10 @@ gdn_status gdn_slots_to_page(const gdn_dims* dims, int32_t n, const int32_t* poo
                              int32_t num_pages, const void* slots, void* pages,
                              int32_t* status, gdn_stream_t stream);
 
-/* Workspace bytes gdn_chunk_prefill needs for this batch (host only;
- * depends on num_requests and max_rows). */
+/* Workspace bytes gdn_chunk_prefill needs for its two-pass form on this
+ * batch (host only): num_requests x num_v_heads x ceil(max_rows / 64) items
+ * of 82944 bytes (81 KiB). 0 when the chunked form does not support the
+ * shape (io dtype other than bf16, Dk or Dv other than 128). */
 size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims,
                                          const gdn_batch* batch);
 
@@ -353,12 +355,22 @@ size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims,
  *   O = scale (diag(e^gamma) Q^ S + (Q^ K^T o e^{gamma_t-gamma_s} o causal) Vn),
  *   S <- e^{gamma_L} S + (diag(e^{gamma_L-gamma}) K^)^T Vn.
  * Equal to gdn_seq in exact arithmetic; within 1e-4 relative in fp32.
- * Arguments as gdn_seq, plus a device workspace of at least
- * gdn_chunk_prefill_workspace_bytes() bytes (0 today: the pointer may be
- * NULL). SPEC requests are skipped. Requires io dtype bf16 and
- * Dk = Dv = 128 (else GDN_ERR_UNSUPPORTED) and qkv 16-byte aligned (the rows
- * are read by TMA). One CTA per (request, value head) walks the request's
- * chunks; its tensor memory holds the fp32 state throughout.               */
+ * Arguments as gdn_seq, plus a device workspace:
+ *   workspace        NULL, or device memory of at least
+ *                    gdn_chunk_prefill_workspace_bytes() bytes, 16-byte
+ *                    aligned (else GDN_ERR_WORKSPACE / GDN_ERR_INVALID_ARG);
+ *                    owned by the caller, overwritten, and in use until the
+ *                    launches on `stream` complete.
+ * With a workspace the call makes two launches. A pre-pass with one CTA per
+ * (request, value head, chunk) does the steps that do not read the state
+ * (the Gram products, A and its inverse T, U, Wm and the masked product P)
+ * and stores Wm, U, P and the chunk's decay factors in the workspace; then
+ * one CTA per (request, value head) walks the request's chunks with the
+ * fp32 state in its tensor memory and does the rest (Wm S, Q^ S, P Vn and
+ * the state update). With workspace NULL one launch does all of it on the
+ * per-request chain. The two forms agree bit for bit. SPEC requests are
+ * skipped. Requires io dtype bf16 and Dk = Dv = 128 (else
+ * GDN_ERR_UNSUPPORTED) and qkv 16-byte aligned (the rows are read by TMA). */
 gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
                              const gdn_params* params, const void* qkv,
                              const void* a, const void* b, void* o,
@@ -374,8 +386,9 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
 
 /* Prefill dispatch: the plain requests of the batch with at least
  * chunk_min_rows rows (<= 0 selects GDN_PREFILL_CHUNK_MIN_ROWS) go through
- * gdn_chunk_prefill, the others through gdn_seq; two launches on `stream`,
- * each leaving the other's requests alone. The r9700-stack v0.2.3 notes
+ * gdn_chunk_prefill (its one-launch form, which needs no workspace), the
+ * others through gdn_seq; two launches on `stream`, each leaving the other's
+ * requests alone. The r9700-stack v0.2.3 notes
  * (section 1) describe the same split by prefill length (R9K_GDN_PREFILL_MAX,
  * break-even measured per model and card); here the threshold is a call
  * argument. When the chunked form does not support the shape (io dtype other

@@ -242,3 +242,58 @@ def test_prefill_dispatch_matches_each_path():
     assert_close(f64(op), o_ref, TOL, what="o", c=CHUNK_ELEM_C)
     S = np.stack([f64(Lp.pool.state_math(r)) for r in range(R)])
     assert_close(S, S_ref, TOL, inner=2, what="S", c=CHUNK_ELEM_C)
+
+
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_two_pass_form_bit_identical_to_one_launch_form(state):
+    """gdn_chunk_prefill with a workspace (chunk-parallel pre-pass, then the
+    state chain) and without one (everything on the chain) produce the same
+    outputs and final states bit for bit, on ragged requests with and
+    without an initial state."""
+    sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
+    rng = np.random.default_rng(211)
+    lengths = [300, 64, 1, 130, 0, 191, 65]
+    R = len(lengths)
+    start, ln, T = synth.pack(lengths, [4, 2, 6, 0, 5, 1, 3])
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    S0 = synth.state(rng, R, sh, std=0.1)
+    fresh = np.array([False, True, False, False, True, True, False])
+    if state == gdn.GDN_BF16:
+        S0 = oracle.round_bf16(S0).astype(np.float32)
+    qkv, a, b = to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"])
+    outs = []
+    for use_ws in (False, True):
+        L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], state=state, num_pages=R)
+        L.seed(range(R), S0=S0)
+        B = L.batch(start, ln, flags=np.where(fresh, gdn.GDN_REQ_FRESH, 0))
+        o = torch.zeros(B.num_rows, sh.Hv, sh.Dv, dtype=torch.float32, device="cuda")
+        ws_bytes = gdn.gdn_chunk_prefill_workspace_bytes(L.dims, B)
+        assert ws_bytes == R * sh.Hv * ((max(lengths) + 63) // 64) * 82944
+        ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device="cuda") if use_ws else None
+        gdn.gdn_chunk_prefill(L.dims, B, L.params, qkv, a, b, o, L.pool.buf, ws,
+                              ws_bytes if use_ws else 0, L.status)
+        L.ok()
+        outs.append((o.clone(), torch.stack([L.pool.state(r).clone() for r in range(R)])))
+    assert torch.equal(outs[0][0].view(torch.int32), outs[1][0].view(torch.int32))
+    s0, s1 = outs[0][1], outs[1][1]
+    assert torch.equal(s0.view(torch.int16) if s0.dtype == torch.bfloat16 else s0.view(torch.int32),
+                       s1.view(torch.int16) if s1.dtype == torch.bfloat16 else s1.view(torch.int32))
+
+
+def test_two_pass_form_rejects_a_short_workspace():
+    sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
+    rng = np.random.default_rng(5)
+    start, ln, T = synth.pack([100, 20])
+    d = {"shapes": sh, "io": synth.BF16}
+    d.update(synth.params(rng, sh, synth.BF16))
+    rows = synth.rows(rng, T, sh, synth.BF16)
+    L = Layer(sh, synth.BF16, d["A_log"], d["dt_bias"], d["conv_w"], num_pages=2)
+    B = L.batch(start, ln, flags=gdn.GDN_REQ_FRESH)
+    o = torch.zeros(T, sh.Hv, sh.Dv, dtype=torch.float32, device="cuda")
+    need = gdn.gdn_chunk_prefill_workspace_bytes(L.dims, B)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_chunk_prefill(L.dims, B, L.params, to_dev(rows["x"]), to_dev(rows["a"]),
+                              to_dev(rows["b"]), o, L.pool.buf, ws, need - 16, L.status)
