@@ -7,7 +7,7 @@ never falls back to another implementation.
 
 Entry points (same names as the C ABI): ``gdn_conv``, ``gdn_seq``,
 ``gdn_decode``, ``gdn_prefill``, ``gdn_spec_verify``, ``gdn_spec_step``, ``gdn_spec_slots``,
-``gdn_chunk_prefill``, ``gdn_page_to_slots``, ``gdn_slots_to_page``,
+``gdn_chunk_prefill``, ``gdn_chunk_prefill_noalloc``, ``gdn_page_to_slots``, ``gdn_slots_to_page``,
 ``gdn_chunk_prefill_workspace_bytes``, ``gdn_page_layout``,
 ``gdn_slot_layout``, ``gdn_check_bounded_wait``, ``gdn_strerror``,
 ``gdn_abi_version``.
@@ -111,6 +111,7 @@ def load_library(path: str = LIB_PATH):
             "gdn_slots_to_page": ([D, I, P, P, P, I, I, P, P, P, P], I),
             "gdn_chunk_prefill_workspace_bytes": ([D, B], S),
             "gdn_chunk_prefill": ([D, B, PR, P, P, P, P, P, P, S, P, P], I),
+            "gdn_chunk_prefill_noalloc": ([D, B, PR, P, P, P, P, P, P, P], I),
             "gdn_check_bounded_wait": ([ctypes.c_int64, P, P], I),
             "gdn_strerror": ([I], ctypes.c_char_p),
             "gdn_abi_version": ([], I),
@@ -250,6 +251,14 @@ def gdn_chunk_prefill(dims, batch, params, qkv, a, b, o, pages, workspace, works
                                             _ptr(o), _ptr(pages), _ptr(workspace),
                                             int(workspace_bytes), _ptr(status), _stream(stream)),
            "gdn_chunk_prefill")
+
+
+def gdn_chunk_prefill_noalloc(dims, batch, params, qkv, a, b, o, pages, status, stream=None):
+    _check(load_library().gdn_chunk_prefill_noalloc(ctypes.byref(dims), ctypes.byref(batch),
+                                                    ctypes.byref(params), _ptr(qkv), _ptr(a),
+                                                    _ptr(b), _ptr(o), _ptr(pages), _ptr(status),
+                                                    _stream(stream)),
+           "gdn_chunk_prefill_noalloc")
 
 
 def gdn_check_bounded_wait(limit_ns, status, stream=None):

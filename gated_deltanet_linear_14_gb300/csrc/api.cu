@@ -304,6 +304,37 @@ gdn_status handover_entry(int dir, const gdn_dims* dims, int32_t n, const int32_
 
 }  // namespace
 
+// Scratch of gdn_chunk_prefill_noalloc: one array per device, part of the
+// library's device image (every device that loads this module holds it until
+// the process exits). Its size bounds the batches that entry point takes.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_chunk_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// The array's device address, looked up once per device (with that device
+// current) and kept; nullptr and the runtime's error if the lookup fails.
+cudaError_t chunk_scratch_address(void** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_chunk_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t gdn_abi_version(void) { return (1 << 16) | 1; }
@@ -542,6 +573,42 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch, const
   }
   if (launch_chunk(&tmap, G, B, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a, b,
                    o, pages, status, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH;
+  return GDN_OK;
+}
+
+gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_batch* batch,
+                                     const gdn_params* params, const void* qkv, const void* a,
+                                     const void* b, void* o, void* pages, int32_t* status,
+                                     gdn_stream_t stream) {
+  gdn_status e = check_dims(dims);
+  if (e != GDN_OK) return e;
+  if ((e = check_batch(batch, true)) != GDN_OK) return e;
+  if ((e = check_params(params, true)) != GDN_OK) return e;
+  if (dims->io_dtype != GDN_BF16 || dims->head_k_dim != 128 || dims->head_v_dim != 128)
+    return GDN_ERR_UNSUPPORTED;
+  if (batch->num_requests == 0) return GDN_OK;
+  if (!status || !pages) return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_chunk_prefill_workspace_bytes(dims, batch);
+  if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
+  CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  if (batch->num_rows > 0) {
+    if (!qkv || !a || !b || !o) return GDN_ERR_INVALID_ARG;
+    if (((uintptr_t)qkv & 15) != 0) return GDN_ERR_UNSUPPORTED;
+    const gdn_status te = encode_rows_tmap(&tmap, qkv, batch->num_rows, dims);
+    if (te != GDN_OK) return te;
+  }
+  void* scratch = nullptr;
+  if (chunk_scratch_address(&scratch) != cudaSuccess) return GDN_ERR_LAUNCH;
+  // every item the chain reads is written by the pre-pass of the same call,
+  // so nothing in the scratch has to start at zero
+  const Geom G = make_geom(dims);
+  const Batch B = make_batch(batch);
+  const Params P = make_params(params, dims);
+  const int ws_chunks = (batch->max_rows + 63) / 64;
+  if (launch_chunk2(&tmap, G, B, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a,
+                    b, o, pages, scratch, ws_chunks, status, (cudaStream_t)stream) != cudaSuccess)
     return GDN_ERR_LAUNCH;
   return GDN_OK;
 }

@@ -378,6 +378,29 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
                              size_t workspace_bytes, int32_t* status,
                              gdn_stream_t stream);
 
+/* gdn_chunk_prefill's two-pass form with no caller workspace and no
+ * allocation, for callers that cannot call cudaMalloc. The paper has no
+ * counterpart: this is a deployment variant of gdn_chunk_prefill.
+ * The workspace is a 64 MiB (67,108,864-byte) array in the library's device
+ * image, one per device, held from the first use on that device until the
+ * process exits. The first call on each device looks its address up
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before capturing a stream into a CUDA graph. Batches whose
+ * gdn_chunk_prefill_workspace_bytes() exceed 64 MiB are rejected with
+ * GDN_ERR_WORKSPACE (about 800 items of (request, value head, 64-row
+ * chunk)). Every call shares the array and leaves its contents behind;
+ * nothing in it needs to start at zero (the pre-pass of a call writes every
+ * item that call reads). Calls whose launches overlap on the GPU (on
+ * different streams, or from different threads) race on the array: order
+ * them on one stream. Arguments, results and errors otherwise as
+ * gdn_chunk_prefill with a workspace; GDN_ERR_LAUNCH also when the address
+ * lookup fails. Calls no allocating routine.                                */
+gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_batch* batch,
+                                     const gdn_params* params, const void* qkv,
+                                     const void* a, const void* b, void* o,
+                                     void* pages, int32_t* status,
+                                     gdn_stream_t stream);
+
 /* Default row count from which gdn_prefill uses the chunked form. Measured on
  * GB300 (16/32 heads, Dk = Dv = 128): with 8 requests per step the chunked
  * form is faster from 32 rows (2.0x at 64, 2.7x at 1024); with a single
