@@ -45,11 +45,21 @@ constexpr uint32_t PP_X = 98304;     // solve scratch (4 KB)
 constexpr uint32_t PP_VEC = 102400;  // 9 x 64 floats of per-token vectors
 constexpr uint32_t kPrepSmem = PP_VEC + 9 * 256 + 1024;
 
-// U^T rows in the workspace: row j's half h (32 floats, 128 bytes) keeps its
-// 16-byte piece q at piece q ^ (j & 7), so that a warp writing or reading one
-// piece of 32 rows spreads over all banks.
+// U^T in the workspace, piece-major: the 16-byte piece q (4 floats) of row
+// j's half h sits at ((h * 8 + q) * 128 + j) * 16, so the 32 rows of a warp
+// read or write one piece as 512 contiguous bytes.
 __device__ __forceinline__ uint32_t ut_piece(int j, int half, int q) {
-  return (uint32_t)(j * 256 + half * 128 + ((q ^ (j & 7)) << 4));
+  return (uint32_t)((((half * 8 + q) << 7) + j) << 4);
+}
+
+// A 16-byte load through the read-only path, issued where it is written (the
+// chain issues its U^T loads at the top of a chunk and uses them after MMA4/5).
+__device__ __forceinline__ float4 ldg_nc_early(const void* p) {
+  float4 v;
+  asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
+  return v;
 }
 
 __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
@@ -446,32 +456,49 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     return !any_fail;
   };
 
+  // U^T of chunk c for this thread's row and half. Issued only after the
+  // chunk's last tensor-memory load before MMA4/5 completes: a wait for
+  // tensor-memory loads also waits for global loads in flight.
+  auto load_u = [&](int c, float* u) {
+    const char* ut = items + (size_t)c * kChunkItemBytes + CW_UT;
+#pragma unroll
+    for (int pq = 0; pq < 8; ++pq) {
+      const float4 v = ldg_nc_early(ut + ut_piece(row, wg, pq));
+      u[4 * pq] = v.x; u[4 * pq + 1] = v.y; u[4 * pq + 2] = v.z; u[4 * pq + 3] = v.w;
+    }
+  };
+
   // outputs of chunk c: O[t][j] = scale (co_t (S^T Q^T)[j][t] + (Vn^T P^T)[j][t]),
-  // gathered as a [64][128] tile (the Vn^T region, which MMA6 of chunk c has
-  // read) and written out as whole 16-byte row pieces
-  auto outputs = [&](int c) {
+  // by the second warpgroup alone (its four warps reach all 128 TMEM lanes),
+  // so that they run while the first warpgroup's issuing thread queues the
+  // next MMAs. Gathered as a [64][128] tile (the Vn^T region, which MMA6 of
+  // chunk c has read) and written out as whole 16-byte row pieces. u_next,
+  // when given, receives U^T of chunk c+1 after the last tensor-memory load.
+  auto outputs = [&](int c, float* u_next) {
     const int n_c = min(kCL, q.len - c * kCL);
     const size_t R0 = (size_t)q.start + (size_t)c * kCL;
     const float* co = reinterpret_cast<const float*>(sm + SQ_VEC + (c & 1) * 768) + 64;
-    {
+    float* of = reinterpret_cast<float*>(sm + SQ_VN);
+    bf16* ob = reinterpret_cast<bf16*>(sm + SQ_VN);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
       float oq[32], op[32];
-      tmem_ld32(trow + TM_OQ + (c & 1) * 64 + wg * 32, oq);
-      tmem_ld32(trow + TM_OP + (c & 1) * 64 + wg * 32, op);
-      float* of = reinterpret_cast<float*>(sm + SQ_VN);
-      bf16* ob = reinterpret_cast<bf16*>(sm + SQ_VN);
+      tmem_ld32(trow + TM_OQ + (c & 1) * 64 + half * 32, oq);
+      tmem_ld32(trow + TM_OP + (c & 1) * 64 + half * 32, op);
+      if (half == 1 && u_next) load_u(c + 1, u_next);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int t = wg * 32 + i;
+        const int t = half * 32 + i;
         const float v = __fmul_rn(P.scale, __fmaf_rn(co[t], oq[i], op[i]));
         if (out_f32) of[t * kCD + row] = v;
         else ob[t * kCD + row] = __float2bfloat16_rn(v);
       }
     }
-    __syncthreads();
+    asm volatile("bar.sync 1, 128;" ::: "memory");
     const int lg = out_f32 ? 5 : 4;
     const int per_row = 1 << lg;
     const uint4* src = reinterpret_cast<const uint4*>(sm + SQ_VN);
-    for (int idx = tid; idx < (n_c << lg); idx += kChunkThreads) {
+    for (int idx = tid - 128; idx < (n_c << lg); idx += 128) {
       const int t = idx >> lg, piece = idx & (per_row - 1);
       const size_t row_off = ((R0 + t) * G.Hv + h) * G.Dv;
       uint4* dst = out_f32 ? reinterpret_cast<uint4*>(reinterpret_cast<float*>(o) + row_off)
@@ -484,16 +511,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     const int n_c = min(kCL, q.len - c * kCL);
     const float* vec = reinterpret_cast<const float*>(sm + SQ_VEC + (c & 1) * 768);
     if (!wait_bar(bar_a, c & 1)) { fail = true; break; }
-    // U^T of this thread's row and half, consumed after MMA4/5
-    float u[32];
-    {
-      const char* ut = items + (size_t)c * kChunkItemBytes + CW_UT;
-#pragma unroll
-      for (int pq = 0; pq < 8; ++pq) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(ut + ut_piece(row, wg, pq)));
-        u[4 * pq] = v.x; u[4 * pq + 1] = v.y; u[4 * pq + 2] = v.z; u[4 * pq + 3] = v.w;
-      }
-    }
+    float u[32];   // U^T of this thread's row and half, loaded under MMA4/5
     // S^T hi/lo operand tiles, and e^{gamma_L} S^T back into TMEM for MMA7
     {
       const float eL = vec[128];
@@ -515,6 +533,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     __syncthreads();
     // MMA4: (W S)^T = S^T W^T (3 hi/lo passes) ; MMA5: (Q S)^T = S^T Q^T
     if (tid == 0) {
+      load_u(c, u);
       tc_fence_after();
       const uint32_t id4 = idesc_bf16(128, 64, 0, 1);
       const int sel_s[3] = {0, 0, 1}, sel_w[3] = {0, 1, 0};
@@ -538,7 +557,8 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
       mma_commit(bar_mma);
     }
     // the previous chunk's outputs while they run
-    if (c > 0) outputs(c - 1);
+    if (wg == 1 && c > 0) outputs(c - 1, u);
+    else if (wg == 1 || tid != 0) load_u(c, u);
     if (!wait_bar(bar_mma, mma_count++ & 1)) { fail = true; break; }
     if (tid == 0 && c + 1 < nchunks) issue_a(c + 1);
 
@@ -591,7 +611,8 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     if (!wait_bar(bar_mma, mma_count++ & 1)) { fail = true; break; }
     if (tid == 0 && c + 1 < nchunks) issue_b(c + 1);
   }
-  if (!fail && nchunks > 0) outputs(nchunks - 1);
+  if (!fail && nchunks > 0 && wg == 1) outputs(nchunks - 1, nullptr);
+  __syncthreads();
 
   if (!fail) {
 #pragma unroll

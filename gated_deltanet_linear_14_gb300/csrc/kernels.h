@@ -28,7 +28,8 @@ cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const 
 // kChunkItemBytes; ws_chunks >= ceil(max_rows / 64). Item layout (bytes):
 //   CW_WT   W^T hi | lo, [128][64] bf16 each, 128B-swizzled operand tiles
 //   CW_P    P hi | lo, [64][64] bf16 each, the same layout
-//   CW_UT   U^T fp32 [128][64], row j at j*256, 16-byte pieces permuted
+//   CW_UT   U^T fp32 [128][64]: 4-float piece q of row j's half h at
+//           ((h * 8 + q) * 128 + j) * 16
 //   CW_VEC  e^{gamma_L-gamma}/|k| [64] | e^gamma/|q| [64] | e^{gamma_L} (768 B)
 constexpr uint32_t CW_WT = 0, CW_P = 32768, CW_UT = 49152, CW_VEC = 81920;
 constexpr size_t kChunkItemBytes = 82944;
