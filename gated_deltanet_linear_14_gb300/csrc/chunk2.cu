@@ -12,15 +12,17 @@
 //     CTAs per SM. It runs those state-independent steps exactly as the
 //     one-kernel form does and writes, per item, the operands the chain will
 //     need into the workspace: W^T as bf16 hi/lo tiles in the 128B-swizzled
-//     operand layout, P likewise, U^T in fp32, and the per-token factors
-//     e^{gamma_L - gamma}/|k|, e^gamma/|q| and e^{gamma_L}.
+//     operand layout, Q^T (exact in bf16) beside W^T hi, P as hi/lo tiles,
+//     U^T in fp32, and the per-token factors e^{gamma_L - gamma}/|k|,
+//     e^gamma/|q| and e^{gamma_L}.
 //   pass 2, chunk_seq_kernel: one CTA per (request, value head) walks the
 //     chunks with the fp32 state in tensor memory. Per chunk: split S^T into
-//     hi/lo operand tiles (and decay it in TMEM), MMA4 S^T W^T and MMA5 S^T
-//     Q^T, Vn = U - W S and V', MMA6 Vn^T P^T and MMA7 S^T += V'^T K. The
-//     operands of chunk c+1 are fetched while chunk c runs (W^T, Q and the
-//     factors once MMA4/5 have read theirs, P and K once MMA6/7 have), and
-//     the outputs of chunk c are formed while MMA4/5 of chunk c+1 run.
+//     hi/lo operand tiles (and decay it in TMEM), MMA4/5 S^T [W^T | Q^T] (one
+//     N = 128 product for both), Vn = U - W S and V', MMA6 Vn^T P^T and MMA7
+//     S^T += V'^T K. The operands of chunk c+1 are fetched while chunk c runs
+//     (W^T, Q^T and the factors once MMA4/5 have read theirs, P and K once
+//     MMA6/7 have), and the outputs of chunk c are formed while MMA4/5 of
+//     chunk c+1 run.
 //
 // Every value is computed by the same operations in the same order as in the
 // one-kernel form, so the two forms agree bit for bit.
@@ -33,14 +35,16 @@ namespace gdn {
 
 // ------------------------------------------------------------------ pass 1
 
-// Shared memory of the pre-pass (bytes from a 1024-aligned base).
+// Shared memory of the pre-pass (bytes from a 1024-aligned base). Every
+// output is staged in its workspace layout and written by bulk copies.
 constexpr uint32_t PP_QK = 0;        // TMA: per atom a (a*16384) Q rows 0..63, K rows 64..127;
-                                     //   T_U hi | lo in the Q halves once MMA1 has read them;
-                                     //   W^T hi | lo staging (32 KB) at the end
-constexpr uint32_t PP_V = 32768;     // TMA: V atom a at PP_V + a*8192
+                                     //   Q^T rows 0..63 | 64..127 in the Q halves once MMA1
+                                     //   and the norms have read Q; W^T lo in the K halves
+                                     //   once MMA2 has read K
+constexpr uint32_t PP_V = 32768;     // TMA: V atom a at PP_V + a*8192; then W^T hi
 constexpr uint32_t PP_P = 49152;     // P hi | lo [64][64]
-constexpr uint32_t PP_A = 65536;     // A fp32 [64][64] -> T_W hi | lo; U^T staging (32 KB, with PP_T)
-constexpr uint32_t PP_T = 81920;     // T fp32 [64][64]
+constexpr uint32_t PP_A = 65536;     // A fp32 [64][64] -> T_W hi | lo -> U^T (with PP_T)
+constexpr uint32_t PP_T = 81920;     // T fp32 [64][64] -> T_U hi | lo (in place)
 constexpr uint32_t PP_X = 98304;     // solve scratch (4 KB)
 constexpr uint32_t PP_VEC = 102400;  // 9 x 64 floats of per-token vectors
 constexpr uint32_t kPrepSmem = PP_VEC + 9 * 256 + 1024;
@@ -67,9 +71,11 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                "r"(src), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void bulk_store_commit_wait() {
+// commit the bulk stores issued so far and wait until they have read shared
+// memory (the writes complete before the grid does)
+__device__ __forceinline__ void bulk_store_commit_wait_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Wait for the previous grid without letting the next one start early: the
@@ -210,9 +216,34 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
       }
     s_iq[tid] = rsqrtf(__fadd_rn(__fadd_rn(__fadd_rn(qq[0], qq[1]), __fadd_rn(qq[2], qq[3])), P.eps));
   }
+  // Q^T [128 i][64 t] as an MN-major operand tile (exact in bf16) for the
+  // chain's merged W S / Q S product: this thread's row i, half wg of t,
+  // gathered from the K-major Q tile while MMA1 runs, then written over the
+  // Q halves (rows 0..63 in atom 0's, 64..127 in atom 1's)
+  uint32_t qt[16];
+  {
+    const int ii = row & 63;
+    const uint8_t* qa = sm + PP_QK + (row >> 6) * 16384;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int t0 = 32 * wg + 2 * e;
+      const uint32_t lo = *reinterpret_cast<const uint16_t*>(
+          qa + t0 * 128 + ((((ii >> 3) ^ (t0 & 7)) << 4) | ((ii & 7) << 1)));
+      const uint32_t hi = *reinterpret_cast<const uint16_t*>(
+          qa + (t0 + 1) * 128 + ((((ii >> 3) ^ ((t0 + 1) & 7)) << 4) | ((ii & 7) << 1)));
+      qt[e] = lo | (hi << 16);
+    }
+  }
   ok = mbar_wait(bar_mma, 0);
   if (__syncthreads_or(!ok)) goto fail;
   tc_fence_after();
+  {
+    uint8_t* qdst = sm + PP_QK + (row >> 6) * 16384;
+#pragma unroll
+    for (int cq = 0; cq < 4; ++cq)
+      *reinterpret_cast<uint4*>(qdst + sw128_chunk(row & 63, 4 * wg + cq)) =
+          make_uint4(qt[4 * cq], qt[4 * cq + 1], qt[4 * cq + 2], qt[4 * cq + 3]);
+  }
 
   {
     float d1[32];
@@ -266,7 +297,8 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
   __syncthreads();
   solve_unit_lower64(Am, Tm, Xs, tid);
 
-  // T_W (into the A region) and T_U (into the Q halves), hi/lo bf16 tiles
+  // T_W (into the A region) and T_U (over T itself), hi/lo bf16 tiles: every
+  // thread takes its part of T into registers before any tile is written
   {
     const int t = tid & 63, which = (tid >> 6) & 1, half = tid >> 7;
     float w[32];
@@ -278,9 +310,9 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
     const float* colscale = which ? s_beta : s_cw;
 #pragma unroll
     for (int i = 0; i < 32; ++i) w[i] = __fmul_rn(w[i], colscale[32 * half + i]);
-    uint8_t* hi = which ? sm + PP_QK : sm + PP_A;
-    uint8_t* lo = which ? sm + PP_QK + 16384 : sm + PP_A + 8192;
-    store_half_hilo(hi, lo, t, half, w);
+    __syncthreads();
+    uint8_t* hi = which ? sm + PP_T : sm + PP_A;
+    store_half_hilo(hi, hi + 8192, t, half, w);
   }
   fence_async_smem();
   __syncthreads();
@@ -299,18 +331,20 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         mma_bf16(tmem + TM_U, sdesc(sb + PP_V + ks * 2048, 8192, 1024),
-                 sdesc(sb + PP_QK + pass * 16384 + ks * 32, 16, 1024), id, (pass | ks) != 0);
+                 sdesc(sb + PP_T + pass * 8192 + ks * 32, 16, 1024), id, (pass | ks) != 0);
     mma_commit(bar_mma);
   }
   ok = mbar_wait(bar_mma, 1);
   if (__syncthreads_or(!ok)) goto fail;
   tc_fence_after();
 
-  // W^T hi/lo tiles over the Q/K tiles; U^T (fp32, pieces permuted) over A and T
+  // staging in the workspace layout: W^T hi over V, W^T lo over the K halves
+  // (rows 0..63 in atom 0's, 64..127 in atom 1's: the same swizzle, as a row
+  // and its row - 64 share their low bits), U^T over A and T
   {
     float w[32];
     tmem_ld32(trow + TM_W + wg * 32, w);
-    store_half_hilo(sm + PP_QK, sm + PP_QK + 16384, row, wg, w);
+    store_half_hilo(sm + PP_V, sm + PP_QK + 8192 + (row >> 6) * 8192, row, wg, w);
     tmem_ld32(trow + TM_U + wg * 32, w);
 #pragma unroll
     for (int pq = 0; pq < 8; ++pq)
@@ -321,11 +355,15 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
   tc_fence_before();
   __syncthreads();
   if (tid == 0) {
-    bulk_store(item + CW_WT, sb + PP_QK, 32768);
+    bulk_store(item + CW_WT, sb + PP_V, 16384);                   // W^T hi
+    bulk_store(item + CW_WT + 16384, sb + PP_QK, 8192);           // Q^T rows 0..63
+    bulk_store(item + CW_WT + 24576, sb + PP_QK + 16384, 8192);   // Q^T rows 64..127
+    bulk_store(item + CW_WT + 32768, sb + PP_QK + 8192, 8192);    // W^T lo rows 0..63
+    bulk_store(item + CW_WT + 40960, sb + PP_QK + 24576, 8192);   // W^T lo rows 64..127
     bulk_store(item + CW_P, sb + PP_P, 16384);
     bulk_store(item + CW_UT, sb + PP_A, 32768);
     bulk_store(item + CW_VEC, smem_u32(s_cv), 768);
-    bulk_store_commit_wait();
+    bulk_store_commit_wait_read();
   }
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
@@ -342,8 +380,8 @@ fail:
 
 // Shared memory of the chain (bytes from a 1024-aligned base).
 constexpr uint32_t SQ_S = 0;          // S^T hi: atom a at a*16384 ([128][64]); lo at +32768
-constexpr uint32_t SQ_QK = 65536;     // TMA: per atom a (a*16384) Q rows 0..63, K rows 64..127
-constexpr uint32_t SQ_WT = 98304;     // W^T hi | lo (from the workspace)
+constexpr uint32_t SQ_K = 65536;      // TMA: K atom a at SQ_K + a*8192 ([64 t][64 i])
+constexpr uint32_t SQ_WT = 81920;     // W^T hi | Q^T | W^T lo (from the workspace)
 constexpr uint32_t SQ_P = 131072;     // P hi | lo (from the workspace)
 constexpr uint32_t SQ_VN = 147456;    // Vn^T hi | lo ([128][64] each); then the output tile
 constexpr uint32_t SQ_VP = 180224;    // V'^T hi | lo
@@ -399,7 +437,8 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
   const uint32_t tmem = tmem_slot;
   const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t sb = smem_u32(sm);
-  constexpr uint32_t TM_S = 0, TM_WS = 128, TM_OQ = 192, TM_OP = 320;  // OQ, OP: two slots each
+  // S^T; per chunk parity a [W S | Q S]^T slot of 128 columns and a (P Vn)^T slot of 64
+  constexpr uint32_t TM_S = 0, TM_D4 = 128, TM_OP = 384;
 
   // the initial state S^T (row j, columns of this warpgroup's half) into TMEM
   {
@@ -419,15 +458,12 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
   }
 
   const int nchunks = (q.len + kCL - 1) / kCL;
-  const int xq = kh * kCD, xk = G.Hk * kCD + kh * kCD;
+  const int xk = G.Hk * kCD + kh * kCD;
   // operands read by MMA4/5 (and the chunk's factors)
   auto issue_a = [&](int c) {
-    const int y = q.start + c * kCL;
     const char* it = items + (size_t)c * kChunkItemBytes;
-    mbar_expect_tx(bar_a, 2 * 8192 + 32768 + 768);
-#pragma unroll
-    for (int a = 0; a < 2; ++a) tma_load_2d(sb + SQ_QK + a * 16384, &tm_qkv, xq + 64 * a, y, bar_a);
-    bulk_load(sb + SQ_WT, it + CW_WT, 32768, bar_a);
+    mbar_expect_tx(bar_a, 49152 + 768);
+    bulk_load(sb + SQ_WT, it + CW_WT, 49152, bar_a);
     bulk_load(sb + SQ_VEC + (c & 1) * 768, it + CW_VEC, 768, bar_a);
   };
   // operands read by MMA6/7
@@ -437,7 +473,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     mbar_expect_tx(bar_b, 2 * 8192 + 16384);
 #pragma unroll
     for (int a = 0; a < 2; ++a)
-      tma_load_2d(sb + SQ_QK + a * 16384 + 8192, &tm_qkv, xk + 64 * a, y, bar_b);
+      tma_load_2d(sb + SQ_K + a * 8192, &tm_qkv, xk + 64 * a, y, bar_b);
     bulk_load(sb + SQ_P, it + CW_P, 16384, bar_b);
   };
   tc_fence_before();
@@ -483,7 +519,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       float oq[32], op[32];
-      tmem_ld32(trow + TM_OQ + (c & 1) * 64 + half * 32, oq);
+      tmem_ld32(trow + TM_D4 + (c & 1) * 128 + 64 + half * 32, oq);
       tmem_ld32(trow + TM_OP + (c & 1) * 64 + half * 32, op);
       if (half == 1 && u_next) load_u(c + 1, u_next);
 #pragma unroll
@@ -531,29 +567,26 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    // MMA4: (W S)^T = S^T W^T (3 hi/lo passes) ; MMA5: (Q S)^T = S^T Q^T
+    // MMA4/5 merged: [(W S)^T | (Q S)^T] = S^T [W^T | Q^T]; the W columns take
+    // three hi/lo passes (S_hi W_hi, S_hi W_lo, S_lo W_hi), the Q columns two
+    // (S_hi Q, S_lo Q), each in the one-kernel form's order
     if (tid == 0) {
       load_u(c, u);
       tc_fence_after();
-      const uint32_t id4 = idesc_bf16(128, 64, 0, 1);
-      const int sel_s[3] = {0, 0, 1}, sel_w[3] = {0, 1, 0};
+      const uint32_t d4 = tmem + TM_D4 + (c & 1) * 128;
+      const uint32_t id128 = idesc_bf16(128, 128, 0, 1), id64 = idesc_bf16(128, 64, 0, 1);
+      auto a_s = [&](int lo, int ks) {
+        return sdesc(sb + SQ_S + lo * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+      };
 #pragma unroll
-      for (int pass = 0; pass < 3; ++pass)
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(d4, a_s(0, ks), sdesc(sb + SQ_WT + ks * 2048, 16384, 1024), id128, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tmem + TM_WS,
-                   sdesc(sb + SQ_S + sel_s[pass] * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                   sdesc(sb + SQ_WT + sel_w[pass] * 16384 + ks * 2048, 16384, 1024), id4,
-                   (pass | ks) != 0);
-      const uint32_t id5 = idesc_bf16(128, 64, 0, 0);
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(d4, a_s(0, ks), sdesc(sb + SQ_WT + 32768 + ks * 2048, 16384, 1024), id64, 1u);
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_bf16(tmem + TM_OQ + (c & 1) * 64,
-                   sdesc(sb + SQ_S + pass * 32768 + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-                   sdesc(sb + SQ_QK + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id5,
-                   (pass | ks) != 0);
+      for (int ks = 0; ks < 8; ++ks)
+        mma_bf16(d4, a_s(1, ks), sdesc(sb + SQ_WT + ks * 2048, 16384, 1024), id128, 1u);
       mma_commit(bar_mma);
     }
     // the previous chunk's outputs while they run
@@ -565,7 +598,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
     {
       float ws_[32];
-      tmem_ld32(trow + TM_WS + wg * 32, ws_);
+      tmem_ld32(trow + TM_D4 + (c & 1) * 128 + wg * 32, ws_);
 #pragma unroll
       for (int s = 0; s < 32; ++s) u[s] = __fsub_rn(u[s], ws_[s]);
       store_half_hilo(sm + SQ_VN, sm + SQ_VN + 16384, row, wg, u);
@@ -580,7 +613,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
       // K rows past the request's end belong to other requests: zero them
       for (int idx = tid; idx < (kCL - n_c) * 16; idx += kChunkThreads) {
         const int r = n_c + (idx >> 4), a = (idx >> 3) & 1, ch = idx & 7;
-        *reinterpret_cast<uint4*>(sm + SQ_QK + a * 16384 + 8192 + r * 128 + ch * 16) =
+        *reinterpret_cast<uint4*>(sm + SQ_K + a * 8192 + r * 128 + ch * 16) =
             make_uint4(0, 0, 0, 0);
       }
       fence_async_smem();
@@ -605,7 +638,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           mma_bf16(tmem + TM_S, sdesc(sb + SQ_VP + pass * 16384 + ks * 32, 16, 1024),
-                   sdesc(sb + SQ_QK + 8192 + ks * 2048, 16384, 1024), id7, 1u);
+                   sdesc(sb + SQ_K + ks * 2048, 8192, 1024), id7, 1u);
       mma_commit(bar_mma);
     }
     if (!wait_bar(bar_mma, mma_count++ & 1)) { fail = true; break; }

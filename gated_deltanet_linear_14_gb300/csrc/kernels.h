@@ -26,13 +26,14 @@ cudaError_t launch_chunk(const void* tmap, const Geom& G, const Batch& B, const 
 // writes one workspace item each, then the chain per (request, value head)
 // reads them. Item (r, h, c) sits at ((r * Hv + h) * ws_chunks + c) *
 // kChunkItemBytes; ws_chunks >= ceil(max_rows / 64). Item layout (bytes):
-//   CW_WT   W^T hi | lo, [128][64] bf16 each, 128B-swizzled operand tiles
+//   CW_WT   W^T hi | Q^T | W^T lo: [128][64] bf16 each, 128B-swizzled
+//           operand tiles (Q^T is exact in bf16), one 48 KiB block
 //   CW_P    P hi | lo, [64][64] bf16 each, the same layout
 //   CW_UT   U^T fp32 [128][64]: 4-float piece q of row j's half h at
 //           ((h * 8 + q) * 128 + j) * 16
 //   CW_VEC  e^{gamma_L-gamma}/|k| [64] | e^gamma/|q| [64] | e^{gamma_L} (768 B)
-constexpr uint32_t CW_WT = 0, CW_P = 32768, CW_UT = 49152, CW_VEC = 81920;
-constexpr size_t kChunkItemBytes = 82944;
+constexpr uint32_t CW_WT = 0, CW_P = 49152, CW_UT = 65536, CW_VEC = 98304;
+constexpr size_t kChunkItemBytes = 99328;
 cudaError_t launch_chunk2(const void* tmap, const Geom& G, const Batch& B, const Params& P,
                           int state_bf16, int out_f32, const void* a, const void* b, void* o,
                           void* pages, void* ws, int ws_chunks, int32_t* status,

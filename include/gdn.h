@@ -340,7 +340,7 @@ gdn_status gdn_slots_to_page(const gdn_dims* dims, int32_t n, const int32_t* poo
 
 /* Workspace bytes gdn_chunk_prefill needs for its two-pass form on this
  * batch (host only): num_requests x num_v_heads x ceil(max_rows / 64) items
- * of 82944 bytes (81 KiB). 0 when the chunked form does not support the
+ * of 99328 bytes (97 KiB). 0 when the chunked form does not support the
  * shape (io dtype other than bf16, Dk or Dv other than 128). */
 size_t gdn_chunk_prefill_workspace_bytes(const gdn_dims* dims,
                                          const gdn_batch* batch);
@@ -387,7 +387,7 @@ gdn_status gdn_chunk_prefill(const gdn_dims* dims, const gdn_batch* batch,
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before capturing a stream into a CUDA graph. Batches whose
  * gdn_chunk_prefill_workspace_bytes() exceed 64 MiB are rejected with
- * GDN_ERR_WORKSPACE (about 800 items of (request, value head, 64-row
+ * GDN_ERR_WORKSPACE (about 670 items of (request, value head, 64-row
  * chunk)). Every call shares the array and leaves its contents behind;
  * nothing in it needs to start at zero (the pre-pass of a call writes every
  * item that call reads). Calls whose launches overlap on the GPU (on

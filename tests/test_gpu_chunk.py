@@ -270,7 +270,7 @@ def test_two_pass_form_bit_identical_to_one_launch_form(state):
         B = L.batch(start, ln, flags=np.where(fresh, gdn.GDN_REQ_FRESH, 0))
         o = torch.zeros(B.num_rows, sh.Hv, sh.Dv, dtype=torch.float32, device="cuda")
         ws_bytes = gdn.gdn_chunk_prefill_workspace_bytes(L.dims, B)
-        assert ws_bytes == R * sh.Hv * ((max(lengths) + 63) // 64) * 82944
+        assert ws_bytes == R * sh.Hv * ((max(lengths) + 63) // 64) * 99328
         ws = torch.full((ws_bytes,), 0xA5, dtype=torch.uint8, device="cuda") if use_ws else None
         gdn.gdn_chunk_prefill(L.dims, B, L.params, qkv, a, b, o, L.pool.buf, ws,
                               ws_bytes if use_ws else 0, L.status)

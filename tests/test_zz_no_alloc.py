@@ -66,7 +66,7 @@ def test_noalloc_rejects_a_batch_beyond_its_scratch():
     sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
     L = Layer(sh, synth.BF16, np.zeros(sh.Hv), np.zeros(sh.Hv),
               np.zeros((sh.C, sh.W), np.float32), num_pages=1)
-    # 4 value heads x 256 chunks of 64 rows = 1024 items of 81 KiB > 64 MiB
+    # 4 value heads x 256 chunks of 64 rows = 1024 items of 97 KiB > 64 MiB
     T = 256 * 64
     B = L.batch([0], [T], flags=gdn.GDN_REQ_FRESH)
     assert gdn.gdn_chunk_prefill_workspace_bytes(L.dims, B) > 64 << 20
