@@ -939,8 +939,10 @@ def bench_long_chunk(device, peaks, K=5, W=3, small=False):
     chunks = R * (T // R // 64)
     flops = chunks * sh.Hv * CHUNK_FLOPS
     tf = flops / (el / K) / 1e12
-    return {"workload": "long prefill: 4 x 8192 tokens, chunk 64, tensor-core WY form (rule only; "
-                        "rows are conv'd bf16 N(0,1))",
+    size = "1 x 4096 tokens, 4/8 heads" if small else "4 x 8192 tokens"
+    return {"workload": f"long prefill: {size}, chunk 64, tensor-core WY form, two passes "
+                        "(pre-pass + state chain; rule only; rows are conv'd bf16 N(0,1))",
+            "workspace_bytes": int(ws_bytes),
             "ms_per_launch": el / K * 1e3, "tokens_per_s": T * K / el,
             "algorithmic_tflops": tf, "tensor_peak_tflops": float(peaks["bf16_tflops"]),
             "frac_of_tensor_peak": tf / float(peaks["bf16_tflops"]),
