@@ -337,7 +337,7 @@ cudaError_t chunk_scratch_address(void** out) {
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return (1 << 16) | 1; }
+int32_t gdn_abi_version(void) { return (1 << 16) | 2; }
 
 gdn_status gdn_page_layout(const gdn_dims* dims, gdn_page_layout_t* out) {
   gdn_status e = check_dims(dims);
