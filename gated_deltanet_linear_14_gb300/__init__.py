@@ -105,7 +105,7 @@ def load_library(path: str = LIB_PATH):
             "gdn_spec_verify": ([D, B, PR, P, P, P, P, P, P, P], I),
             "gdn_spec_step": ([D, B, PR, P, P, P, P, P, P, P, P], I),
             "gdn_decode": ([D, B, PR, P, P, P, P, P, P, P, P], I),
-            "gdn_prefill": ([D, B, PR, P, P, P, P, P, I, P, P], I),
+            "gdn_prefill": ([D, B, PR, P, P, P, P, P, I, P, S, P, P], I),
             "gdn_spec_slots": ([D, B, PR, P, P, P, P, P, P, P, P, P], I),
             "gdn_page_to_slots": ([D, I, P, P, I, I, P, P, P, P], I),
             "gdn_slots_to_page": ([D, I, P, P, P, I, I, P, P, P, P], I),
@@ -195,10 +195,12 @@ def gdn_decode(dims, batch, params, x, conv_w, a, b, o, pages, status, stream=No
                                      _ptr(status), _stream(stream)), "gdn_decode")
 
 
-def gdn_prefill(dims, batch, params, qkv, a, b, o, pages, status, chunk_min_rows=0, stream=None):
+def gdn_prefill(dims, batch, params, qkv, a, b, o, pages, status, chunk_min_rows=0, stream=None,
+                workspace=None, workspace_bytes=0):
     _check(load_library().gdn_prefill(ctypes.byref(dims), ctypes.byref(batch), ctypes.byref(params),
                                       _ptr(qkv), _ptr(a), _ptr(b), _ptr(o), _ptr(pages),
-                                      int(chunk_min_rows), _ptr(status), _stream(stream)),
+                                      int(chunk_min_rows), _ptr(workspace), int(workspace_bytes),
+                                      _ptr(status), _stream(stream)),
            "gdn_prefill")
 
 

@@ -337,7 +337,7 @@ cudaError_t chunk_scratch_address(void** out) {
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return (1 << 16) | 2; }
+int32_t gdn_abi_version(void) { return (2 << 16) | 0; }
 
 gdn_status gdn_page_layout(const gdn_dims* dims, gdn_page_layout_t* out) {
   gdn_status e = check_dims(dims);
@@ -494,7 +494,8 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch, const gdn_pa
 
 gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_params* params,
                        const void* qkv, const void* a, const void* b, void* o, void* pages,
-                       int32_t chunk_min_rows, int32_t* status, gdn_stream_t stream) {
+                       int32_t chunk_min_rows, void* workspace, size_t workspace_bytes,
+                       int32_t* status, gdn_stream_t stream) {
   gdn_status e = check_dims(dims);
   if (e != GDN_OK) return e;
   if ((e = check_batch(batch, true)) != GDN_OK) return e;
@@ -513,9 +514,13 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_p
   // that a failure to encode it still leaves nothing launched or written
   CUtensorMap tmap;
   std::memset(&tmap, 0, sizeof(tmap));
+  size_t need = 0;
   if (any_long) {
     const gdn_status te = encode_rows_tmap(&tmap, qkv, batch->num_rows, dims);
     if (te != GDN_OK) return te;
+    need = gdn_chunk_prefill_workspace_bytes(dims, batch);
+    if (workspace && workspace_bytes < need) return GDN_ERR_WORKSPACE;
+    if (workspace && ((uintptr_t)workspace & 15) != 0) return GDN_ERR_INVALID_ARG;
   }
   Batch Bs = make_batch(batch);
   if (any_long) Bs.max_len = threshold - 1;
@@ -523,6 +528,13 @@ gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch, const gdn_p
   if (!any_long) return GDN_OK;
   Batch Bc = make_batch(batch);
   Bc.min_len = threshold;
+  if (workspace && need > 0) {
+    const int ws_chunks = (batch->max_rows + 63) / 64;
+    if (launch_chunk2(&tmap, G, Bc, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32,
+                      a, b, o, pages, workspace, ws_chunks, status, s) != cudaSuccess)
+      return GDN_ERR_LAUNCH;
+    return GDN_OK;
+  }
   if (launch_chunk(&tmap, G, Bc, P, dims->state_dtype == GDN_BF16, dims->out_dtype == GDN_F32, a,
                    b, o, pages, status, s) != cudaSuccess)
     return GDN_ERR_LAUNCH;

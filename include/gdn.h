@@ -409,9 +409,11 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_batch* batc
 
 /* Prefill dispatch: the plain requests of the batch with at least
  * chunk_min_rows rows (<= 0 selects GDN_PREFILL_CHUNK_MIN_ROWS) go through
- * gdn_chunk_prefill (its one-launch form, which needs no workspace), the
- * others through gdn_seq; two launches on `stream`, each leaving the other's
- * requests alone. The r9700-stack v0.2.3 notes
+ * gdn_chunk_prefill, the others through gdn_seq, each launch leaving the
+ * other's requests alone. workspace / workspace_bytes as for
+ * gdn_chunk_prefill on the same batch: with a workspace the chunked
+ * requests take the two-pass form (three launches on `stream` in all),
+ * with NULL the one-launch form (two launches). The r9700-stack v0.2.3 notes
  * (section 1) describe the same split by prefill length (R9K_GDN_PREFILL_MAX,
  * break-even measured per model and card); here the threshold is a call
  * argument. When the chunked form does not support the shape (io dtype other
@@ -420,7 +422,8 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_dims* dims, const gdn_batch* batc
 gdn_status gdn_prefill(const gdn_dims* dims, const gdn_batch* batch,
                        const gdn_params* params, const void* qkv, const void* a,
                        const void* b, void* o, void* pages,
-                       int32_t chunk_min_rows, int32_t* status,
+                       int32_t chunk_min_rows, void* workspace,
+                       size_t workspace_bytes, int32_t* status,
                        gdn_stream_t stream);
 
 /* Failure-detection check of the bounded on-chip waits. Every wait a

@@ -187,10 +187,14 @@ class Layer:
         gdn.gdn_seq(self.dims, batch, self.params, qkv, a, b, o, self.pool.buf, self.status)
         return o
 
-    def prefill(self, batch, qkv, a, b, chunk_min_rows=0):
+    def prefill(self, batch, qkv, a, b, chunk_min_rows=0, workspace=False):
         o = self.out(batch.num_rows)
+        ws, ws_bytes = None, 0
+        if workspace:
+            ws_bytes = gdn.gdn_chunk_prefill_workspace_bytes(self.dims, batch)
+            ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
         gdn.gdn_prefill(self.dims, batch, self.params, qkv, a, b, o, self.pool.buf, self.status,
-                        chunk_min_rows)
+                        chunk_min_rows, workspace=ws, workspace_bytes=ws_bytes)
         return o
 
     def verify(self, batch, qkv, a, b):

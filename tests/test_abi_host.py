@@ -44,7 +44,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert gdn.gdn_abi_version() >> 16 == 1
+    assert gdn.gdn_abi_version() >> 16 == 2
 
 
 def full_dims(Kc=8, state=gdn.GDN_F32, io=gdn.GDN_BF16):

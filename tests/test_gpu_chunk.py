@@ -197,10 +197,12 @@ def test_chunk_long_prefill_full_size_sampled_heads():
         assert_close(S, S_ref[0], TOL, inner=2, what=f"S request {r} heads {h0},{h0 + 1}", c=CHUNK_ELEM_C)
 
 
-def test_prefill_dispatch_matches_each_path():
+@pytest.mark.parametrize("use_ws", [False, True])
+def test_prefill_dispatch_matches_each_path(use_ws):
     """gdn_prefill sends requests with >= threshold rows through the chunked
-    form and the rest token by token: each request equals, bit for bit, the
-    kernel it was sent to, and all are within 1e-4 of the oracle."""
+    form (one launch without a workspace, two passes with one) and the rest
+    token by token: each request equals, bit for bit, the kernel it was sent
+    to, and all are within 1e-4 of the oracle."""
     sh = synth.Shapes(Hk=2, Hv=4, Dk=128, Dv=128)
     rng = np.random.default_rng(55)
     lengths = [20, 63, 64, 200, 1, 0, 130]
@@ -224,7 +226,10 @@ def test_prefill_dispatch_matches_each_path():
     Lp = layer()
     Bp = Lp.batch(start, ln, flags=flags)
     op = Lp.out(T)
-    gdn.gdn_prefill(Lp.dims, Bp, Lp.params, qkv, a, b, op, Lp.pool.buf, Lp.status, thr)
+    ws_bytes = gdn.gdn_chunk_prefill_workspace_bytes(Lp.dims, Bp) if use_ws else 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if use_ws else None
+    gdn.gdn_prefill(Lp.dims, Bp, Lp.params, qkv, a, b, op, Lp.pool.buf, Lp.status, thr,
+                    workspace=ws, workspace_bytes=ws_bytes)
     Lp.ok()
     Ls = layer()
     os_ = Ls.seq(Ls.batch(start, ln, flags=flags), qkv, a, b)

@@ -199,10 +199,11 @@ def test_commit_then_plain_decode_continues():
         assert_close(f64(L.pool.state_math(r)), S_ref[0], TOL, inner=2, what=f"S request {r}")
 
 
-@pytest.mark.parametrize("prefill_entry", ["seq", "prefill"])
+@pytest.mark.parametrize("prefill_entry", ["seq", "prefill", "prefill_ws"])
 def test_mixed_prefill_and_spec_step_through_row_map(prefill_entry):
-    """gdn_seq, or gdn_prefill (prefills of 128+ rows take the chunked form),
-    for the plain rows of a step that also verifies spec requests."""
+    """gdn_seq, or gdn_prefill (prefills of 64+ rows take the chunked form: one
+    launch, or with a workspace two passes), for the plain rows of a step that
+    also verifies spec requests, through a row map with a processing order."""
     for shuffled in (False, True):
         d = synth.mixed(shuffled=shuffled)
         sh, n, ns, npf = d["shapes"], d["n"], d["n_spec"], d["n_prefill"]
@@ -225,7 +226,8 @@ def test_mixed_prefill_and_spec_step_through_row_map(prefill_entry):
         B = L.batch(d["row_start"], lengths, flags=flags, n_accepted=acc, order=order)
         x, a, b = to_dev(d["x"]), to_dev(d["a"]), to_dev(d["b"])
         y = L.conv(B, x)
-        o = L.seq(B, y, a, b) if prefill_entry == "seq" else L.prefill(B, y, a, b)
+        o = L.seq(B, y, a, b) if prefill_entry == "seq" else \
+            L.prefill(B, y, a, b, workspace=(prefill_entry == "prefill_ws"))
         o2 = L.verify(B, y, a, b)
         L.ok()
         row_is_spec = np.zeros(d["T"], bool)
@@ -242,7 +244,7 @@ def test_mixed_prefill_and_spec_step_through_row_map(prefill_entry):
                                           d["b"].value[sl], d["A_log"], d["dt_bias"], [0],
                                           [lengths[r]], sh.Hk, sh.Hv, sh.Dk, sh.Dv)
             # gdn_prefill sends prompts of 64+ rows through the chunked form
-            c = CHUNK_ELEM_C if prefill_entry == "prefill" else 1.0
+            c = CHUNK_ELEM_C if prefill_entry != "seq" else 1.0
             assert_close(f64(o[sl]), o_ref, TOL, what=f"o prefill {r}", c=c)
             assert_close(f64(L.pool.state_math(r)), S_ref[0], TOL, inner=2,
                          what=f"S prefill {r}", c=c)
