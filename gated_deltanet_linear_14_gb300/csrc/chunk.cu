@@ -138,7 +138,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
 
   const int nchunks = (q.len + kCL - 1) / kCL;
   const int xq = kh * kCD, xk = G.Hk * kCD + kh * kCD, xv = 2 * G.Hk * kCD + h * G.Dv;
+  // phases issued (by thread 0) and completed, for the drain after a failed wait
+  uint32_t tma_iss = 0, tma_done = 0, m_iss = 0, m_done = 0;
   auto issue_tma = [&](int c) {
+    ++tma_iss;
     const int y = q.start + c * kCL;
     mbar_expect_tx(bar_tma, 6 * 8192);
 #pragma unroll
@@ -204,6 +207,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     ++mma_count;
     const bool any_fail = __syncthreads_or(!ok);
     tc_fence_after();
+    if (!any_fail) ++m_done;
     return !any_fail;
   };
 
@@ -216,6 +220,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     {
       const bool ok = mbar_wait(bar_tma, c & 1);
       if (__syncthreads_or(!ok)) { fail = true; break; }
+      ++tma_done;
     }
     if (n_c < kCL) {
       // rows past the request's end belong to other requests: zero them
@@ -240,6 +245,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
         mma_bf16(tmem + TM_D1, sdesc(base, 16, 1024), sdesc(base + 8192, 16, 1024), id, ks > 0);
       }
       mma_commit(bar_mma);
+      ++m_iss;
     }
     // q norms while it runs (this chunk's gates are in place already)
     if (tid < kCL) {
@@ -347,6 +353,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
           mma_bf16(tmem + TM_U, sdesc(sb + OFF_V + ks * 2048, 8192, 1024),
                    sdesc(sb + OFF_R1 + 16384 + pass * 8192 + ks * 32, 16, 1024), id, (pass | ks) != 0);
       mma_commit(bar_mma);
+      ++m_iss;
     }
     // S^T hi/lo operand tiles, and e^{gamma_L} S^T back into TMEM for MMA7
     {
@@ -400,6 +407,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
                    sdesc(sb + OFF_QK + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), id5,
                    (pass | ks) != 0);
       mma_commit(bar_mma);
+      ++m_iss;
     }
     // the next chunk's gates while they run: past this point the chunk reads
     // none of s_beta, s_gam, s_l2 (its later phases use s_cv and s_co)
@@ -449,6 +457,7 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
           mma_bf16(tmem + TM_S, sdesc(sb + OFF_R2 + pass * 16384 + ks * 32, 16, 1024),
                    sdesc(sb + OFF_QK + 8192 + ks * 2048, 16384, 1024), id7, 1u);
       mma_commit(bar_mma);
+      ++m_iss;
     }
     if (!wait_mma()) { fail = true; break; }
     if (tid == 0 && c + 1 < nchunks) issue_tma(c + 1);
@@ -499,6 +508,10 @@ chunk_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Params
     if (q.fresh && h == 0 && tid == 0) *flagp = 0u;  // empty record
   } else if (tid == 0) {
     report(status, GDN_DEV_TIMEOUT);
+    // let the copies and MMAs still in flight finish (each wait bounded)
+    // before the shared and tensor memory are given up
+    for (uint32_t k = tma_done; k < tma_iss; ++k) mbar_wait(bar_tma, k & 1);
+    for (uint32_t k = m_done; k < m_iss; ++k) mbar_wait(bar_mma, k & 1);
   }
   tc_fence_before();
   __syncthreads();

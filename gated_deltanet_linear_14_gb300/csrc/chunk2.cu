@@ -173,8 +173,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
     }
   }
 
+  // phases issued and completed, for the drain after a failed wait
+  uint32_t tma_done = 0, mma_iss = 0, mma_done = 0;
   bool ok = mbar_wait(bar_tma, 0);
   if (__syncthreads_or(!ok)) goto fail;
+  tma_done = 1;
   if (n_c < kCL) {
     // rows past the request's end belong to other requests: zero them
     const int nrow = kCL - n_c;
@@ -198,6 +201,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
       mma_bf16(tmem + TM_D1, sdesc(base, 16, 1024), sdesc(base + 8192, 16, 1024), id, ks > 0);
     }
     mma_commit(bar_mma);
+    ++mma_iss;
   }
   if (tid < kCL) {
     float qq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -236,6 +240,7 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
   }
   ok = mbar_wait(bar_mma, 0);
   if (__syncthreads_or(!ok)) goto fail;
+  mma_done = 1;
   tc_fence_after();
   {
     uint8_t* qdst = sm + PP_QK + (row >> 6) * 16384;
@@ -333,9 +338,11 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
         mma_bf16(tmem + TM_U, sdesc(sb + PP_V + ks * 2048, 8192, 1024),
                  sdesc(sb + PP_T + pass * 8192 + ks * 32, 16, 1024), id, (pass | ks) != 0);
     mma_commit(bar_mma);
+    ++mma_iss;
   }
   ok = mbar_wait(bar_mma, 1);
   if (__syncthreads_or(!ok)) goto fail;
+  mma_done = 2;
   tc_fence_after();
 
   // staging in the workspace layout: W^T hi over V, W^T lo over the K halves
@@ -370,7 +377,13 @@ chunk_prep_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, P
   return;
 
 fail:
-  if (tid == 0) report(status, GDN_DEV_TIMEOUT);
+  if (tid == 0) {
+    report(status, GDN_DEV_TIMEOUT);
+    // let the copies and MMAs still in flight finish (each wait bounded)
+    // before the shared and tensor memory are given up
+    if (tma_done == 0) mbar_wait(bar_tma, 0);
+    for (uint32_t k = mma_done; k < mma_iss; ++k) mbar_wait(bar_mma, k & 1);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 256);
@@ -459,8 +472,11 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
 
   const int nchunks = (q.len + kCL - 1) / kCL;
   const int xk = G.Hk * kCD + kh * kCD;
+  // phases issued (by thread 0) and completed, for the drain after a failed wait
+  uint32_t a_iss = 0, a_done = 0, b_iss = 0, b_done = 0, m_iss = 0, m_done = 0;
   // operands read by MMA4/5 (and the chunk's factors)
   auto issue_a = [&](int c) {
+    ++a_iss;
     const char* it = items + (size_t)c * kChunkItemBytes;
     mbar_expect_tx(bar_a, 49152 + 768);
     bulk_load(sb + SQ_WT, it + CW_WT, 49152, bar_a);
@@ -468,6 +484,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
   };
   // operands read by MMA6/7
   auto issue_b = [&](int c) {
+    ++b_iss;
     const int y = q.start + c * kCL;
     const char* it = items + (size_t)c * kChunkItemBytes;
     mbar_expect_tx(bar_b, 2 * 8192 + 16384);
@@ -547,6 +564,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     const int n_c = min(kCL, q.len - c * kCL);
     const float* vec = reinterpret_cast<const float*>(sm + SQ_VEC + (c & 1) * 768);
     if (!wait_bar(bar_a, c & 1)) { fail = true; break; }
+    ++a_done;
     float u[32];   // U^T of this thread's row and half, loaded under MMA4/5
     // S^T hi/lo operand tiles, and e^{gamma_L} S^T back into TMEM for MMA7
     {
@@ -588,11 +606,13 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
       for (int ks = 0; ks < 8; ++ks)
         mma_bf16(d4, a_s(1, ks), sdesc(sb + SQ_WT + ks * 2048, 16384, 1024), id128, 1u);
       mma_commit(bar_mma);
+      ++m_iss;
     }
     // the previous chunk's outputs while they run
     if (wg == 1 && c > 0) outputs(c - 1, u);
     else if (wg == 1 || tid != 0) load_u(c, u);
     if (!wait_bar(bar_mma, mma_count++ & 1)) { fail = true; break; }
+    ++m_done;
     if (tid == 0 && c + 1 < nchunks) issue_a(c + 1);
 
     // Vn^T = U^T - (W S)^T ; V'^T = Vn^T diag(e^{gamma_L - gamma} / |k|)
@@ -609,6 +629,7 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     fence_async_smem();
     tc_fence_before();
     if (!wait_bar(bar_b, c & 1)) { fail = true; break; }
+    ++b_done;
     if (n_c < kCL) {
       // K rows past the request's end belong to other requests: zero them
       for (int idx = tid; idx < (kCL - n_c) * 16; idx += kChunkThreads) {
@@ -640,8 +661,10 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
           mma_bf16(tmem + TM_S, sdesc(sb + SQ_VP + pass * 16384 + ks * 32, 16, 1024),
                    sdesc(sb + SQ_K + ks * 2048, 8192, 1024), id7, 1u);
       mma_commit(bar_mma);
+      ++m_iss;
     }
     if (!wait_bar(bar_mma, mma_count++ & 1)) { fail = true; break; }
+    ++m_done;
     if (tid == 0 && c + 1 < nchunks) issue_b(c + 1);
   }
   if (!fail && nchunks > 0 && wg == 1) outputs(nchunks - 1, nullptr);
@@ -658,6 +681,11 @@ chunk_seq_kernel(const __grid_constant__ CUtensorMap tm_qkv, Geom G, Batch B, Pa
     if (q.fresh && h == 0 && tid == 0) *flagp = 0u;  // empty record
   } else if (tid == 0) {
     report(status, GDN_DEV_TIMEOUT);
+    // let the copies and MMAs still in flight finish (each wait bounded)
+    // before the shared and tensor memory are given up
+    for (uint32_t k = a_done; k < a_iss; ++k) mbar_wait(bar_a, k & 1);
+    for (uint32_t k = b_done; k < b_iss; ++k) mbar_wait(bar_b, k & 1);
+    for (uint32_t k = m_done; k < m_iss; ++k) mbar_wait(bar_mma, k & 1);
   }
   tc_fence_before();
   __syncthreads();
