@@ -592,8 +592,12 @@ def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
     for par in (0, 1):
         flags = np.full(R, gdn.GDN_REQ_SPEC | (gdn.GDN_REQ_PARITY if par else 0))
         for k in range(8):
+            # the row map's processing order puts the longest replays first
+            # (the engine knows each request's accepted count), so the last
+            # wave of CTAs holds the shortest
             batches[(par, k)] = _dev_batch(gdn, torch, device, d["row_start"], d["row_len"],
-                                           np.arange(R), flags, acc=accs[k])
+                                           np.arange(R), flags, acc=accs[k],
+                                           order=np.argsort(-accs[k], kind="stable"))
     steps_done = [0] * pools
 
     def launch(i, ev=None):
