@@ -347,10 +347,13 @@ __device__ __forceinline__ void cp_async_wait_all_but_one() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
-// 3 CTAs per SM (161 registers): measured faster than 2 (the item loop is
-// bound by latency, not by a pipe) and than 4 (which spills).
+// The verify runs 3 CTAs per SM (161 registers): measured faster than 2 (the
+// item loop is bound by latency, not by a pipe) and than 4 (which spills).
+// The slot layout keeps every candidate's state in registers on its way out
+// and spilled 280 bytes at 3 per SM; at 2 per SM (240 registers) it does not
+// spill and runs 244 us per 64-request step, against 294 us.
 template <class IO, class ST, int DK, int MODE>
-__global__ void __launch_bounds__(kSpecThreads, 3)
+__global__ void __launch_bounds__(kSpecThreads, MODE == SPEC_SLOTS ? 2 : 3)
 spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_in,
             const IO* __restrict__ conv_w, const IO* __restrict__ a_in,
             const IO* __restrict__ b_in, void* o, int out_f32, void* pages, int32_t* status,
