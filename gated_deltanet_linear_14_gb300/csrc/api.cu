@@ -66,9 +66,12 @@ void layout(const gdn_dims* d, gdn_page_layout_t* L, int* rec_row_elems) {
   L->window_bytes = (size_t)(d->conv_width - 1 + d->max_candidates) * C * io;
   L->record_offset = align_up(L->window_offset + L->window_bytes, kAlign);
   // both slots' rows, then both slots' run coefficients (fp32, one block of
-  // kRunCoefBytes per value head and slot)
+  // kRunCoefBytes per value head and slot), then the live slot's u (fp32, per
+  // value head, candidate and value column; a step reads it before it
+  // writes its candidates' u there)
   L->record_bytes = 2 * (size_t)d->max_candidates * rec_row * io +
-                    (d->max_candidates > 0 ? 2 * (size_t)d->num_v_heads * kRunCoefBytes : 0);
+                    (d->max_candidates > 0 ? 2 * (size_t)d->num_v_heads * kRunCoefBytes : 0) +
+                    (size_t)d->num_v_heads * d->max_candidates * d->head_v_dim * 4;
   L->flag_offset = align_up(L->record_offset + L->record_bytes, kAlign);
   L->page_bytes = align_up(L->flag_offset + sizeof(uint32_t), kAlign);
   if (rec_row_elems) *rec_row_elems = (int)rec_row;
@@ -103,6 +106,7 @@ Geom make_geom(const gdn_dims* d) {
   G.state_off = L.state_offset;
   G.record_off = L.record_offset;
   G.rcoef_off = L.record_offset + 2 * (size_t)d->max_candidates * rec_row * dsize(d->io_dtype);
+  G.ru_off = G.rcoef_off + (d->max_candidates > 0 ? 2 * (size_t)d->num_v_heads * kRunCoefBytes : 0);
   G.flag_off = L.flag_offset;
   return G;
 }
@@ -182,11 +186,12 @@ int device_sms() {
   return sms[dev];
 }
 
-// CTAs per (request, q/k head) for the closed-form spec kernel: one unless
-// the batch would leave SMs idle; then the group's items are split in halves
-// (as long as they divide evenly) until there are three CTAs per SM.
+// CTAs per (request, q/k head) for the slot-layout kernel: one unless the
+// batch would leave SMs idle; then the group's items are split in halves (as
+// long as they divide evenly) until there are three CTAs per SM. (The
+// one-page step's item kernel always runs one CTA per item.)
 int spec_splits(const gdn_dims* d, int R, int mode) {
-  if (mode == SPEC_FUSED) return 1;
+  if (mode != SPEC_SLOTS) return 1;
   const int Gh = d->num_v_heads / d->num_k_heads;
   const int bvi = d->head_v_dim < kSpecBV ? d->head_v_dim : kSpecBV;
   const int items = Gh * (d->head_v_dim / bvi);
@@ -201,9 +206,8 @@ int spec_splits(const gdn_dims* d, int R, int mode) {
 // supported: a very wide group of value heads).
 bool spec_fits(const gdn_dims* d) {
   const int Gh = d->num_v_heads / d->num_k_heads;
-  const SpecSmem L = spec_smem(d->head_k_dim, d->head_v_dim, Gh, (int)dsize(d->io_dtype),
-                               (int)dsize(d->state_dtype));
-  return (int)L.total <= kSpecSmemMax;
+  return (int)spec_smem_most(d->head_k_dim, Gh, (int)dsize(d->io_dtype),
+                             (int)dsize(d->state_dtype)) <= kSpecSmemMax;
 }
 
 cudaError_t spec(int mode, const Geom& G, const Batch& B, const Params& P, const SlotGeom& SG,
@@ -337,7 +341,7 @@ cudaError_t chunk_scratch_address(void** out) {
 
 extern "C" {
 
-int32_t gdn_abi_version(void) { return (2 << 16) | 0; }
+int32_t gdn_abi_version(void) { return (2 << 16) | 1; }
 
 gdn_status gdn_page_layout(const gdn_dims* dims, gdn_page_layout_t* out) {
   gdn_status e = check_dims(dims);

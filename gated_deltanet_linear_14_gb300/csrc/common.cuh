@@ -20,13 +20,15 @@ struct Geom {
   int rec_row;        // record row stride in elements (16-byte padded)
   size_t page_bytes, window_off, state_off, record_off, flag_off;
   size_t rcoef_off;   // the record's run-coefficient blocks ([2][Hv], kRunCoefBytes each)
+  size_t ru_off;      // the record's u per value column ([Hv][Kc][Dv] fp32)
 };
 
-// Run coefficients of one value head for the rows of one record slot, kept
-// so that the next step's replay need not derive them again: G_t / |k_t|,
-// G_t, R[t][s] / |k_s| and M = (I - L)^-1 diag(beta), fp32, 8 + 8 + 64 + 64
-// values (see spec.cuh).
-constexpr size_t kRunCoefFloats = 8 + 8 + 64 + 64;
+// Run coefficients of one value head for the rows of one record slot: G_t /
+// |k_t|, G_t / |q_t|, G_t, R[t][s] / |k_s|, M = (I - L)^-1 diag(beta) and
+// N = B M, fp32, 8 + 8 + 8 + 64 + 64 + 64 values (see spec.cuh). The item
+// kernel reads the candidates' from here; the next step's replay reads G and
+// R/|k| of the same rows.
+constexpr size_t kRunCoefFloats = 8 + 8 + 8 + 64 + 64 + 64;
 constexpr size_t kRunCoefBytes = kRunCoefFloats * 4;
 
 struct Batch {
@@ -110,6 +112,27 @@ struct SpecState {
   int live, parity, width, accepted;  // accepted = -1 when nothing to replay
   int err;
 };
+
+// As spec_state, with the request's accepted count already loaded (-1 when
+// the batch has none).
+__device__ __forceinline__ SpecState spec_state_acc(const Geom& G, const Req& q, uint32_t flag,
+                                                    int accepted) {
+  SpecState s;
+  s.live = flag_live(flag);
+  s.parity = flag_parity(flag);
+  s.width = flag_width(flag);
+  s.accepted = -1;
+  s.err = 0;
+  const int want = (q.flags & GDN_REQ_PARITY) ? 1 : 0;
+  if (s.width > G.Kc) s.err = GDN_DEV_BAD_FLAG;
+  else if (s.parity != want) s.err = GDN_DEV_STALE_STEP;
+  else if (q.len > G.Kc) s.err = GDN_DEV_TOO_MANY_CANDIDATES;
+  else if (s.width > 0) {
+    if (accepted < 0 || accepted >= s.width) s.err = GDN_DEV_BAD_ACCEPTED;
+    else s.accepted = accepted;
+  }
+  return s;
+}
 
 __device__ __forceinline__ SpecState spec_state(const Geom& G, const Batch& B, const Req& q,
                                                 uint32_t flag) {
@@ -310,19 +333,29 @@ __device__ __forceinline__ float2 own_silu2(float2 z) {
 
 // ----------------------------------------------------------------- gates
 
-// g (log decay) and beta from the raw inputs, fp32, CUDA math library.
-__device__ __forceinline__ void gates(const Params& P, int h, float a_in, float b_in,
-                                      float& alpha, float& beta) {
-  if (P.gate_mode == 1) {
+// g (log decay) and beta from the raw inputs, fp32, CUDA math library, with
+// the head's A_log and dt_bias already at hand.
+__device__ __forceinline__ void gates_v(int gate_mode, float A_log_h, float dt_bias_h, float a_in,
+                                        float b_in, float& alpha, float& beta) {
+  if (gate_mode == 1) {
     alpha = expf(a_in);
     beta = b_in;
     return;
   }
-  const float x = __fadd_rn(a_in, P.dt_bias[h]);
+  const float x = __fadd_rn(a_in, dt_bias_h);
   const float sp = (x > 20.0f) ? x : log1pf(expf(x));
-  const float g = -__fmul_rn(expf(P.A_log[h]), sp);
+  const float g = -__fmul_rn(expf(A_log_h), sp);
   alpha = expf(g);
   beta = __frcp_rn(__fadd_rn(1.0f, expf(-b_in)));
+}
+
+__device__ __forceinline__ void gates(const Params& P, int h, float a_in, float b_in,
+                                      float& alpha, float& beta) {
+  if (P.gate_mode == 1) {
+    gates_v(1, 0.0f, 0.0f, a_in, b_in, alpha, beta);
+    return;
+  }
+  gates_v(0, P.A_log[h], P.dt_bias[h], a_in, b_in, alpha, beta);
 }
 
 // g (the log decay) and beta, for the chunked form (which works with prefix

@@ -21,40 +21,52 @@
 // with c_t = v_t - G_t S^T k^_t and L[t][s] = -beta_t R[t][s] (k^_s.k^_t),
 // u = (I - L)^-1 diag(beta) c =: M c, and the outputs are
 // o = scale (G S^T q^ + N c) with N = B M, B[t][s] = R[t][s] (k^_s.q^_t).
-// M and N depend only on the rows (not on S or the value column), so a CTA
-// forms them once per value head; every column then needs only independent
-// short dot products with its c. A run so costs one read of S for all its
-// dot products and (only where a state is kept) one rank-n update. M's
-// leading block is the inverse of L's leading block, so a run of the first
-// a + 1 rows sees exactly the coefficients the longer run had; the record
-// keeps the candidates' G/|k|, G, R/|k| and M beside their rows, and the
-// next step's replay uses them as they are. The verify runs two such runs:
-// the replayed rows (state only: the checkpoint is S_a) and the candidates
-// (outputs only). The slot layout runs the candidates and stores every S_t.
-// Both compute each quantity with the same code and in the same order from
-// the same inputs (a replayed row and the candidate row it was are the same
-// bits, its dot products come from the same stored state), so the one-page
+// M and N depend only on the rows (not on S or the value column), so they
+// are formed once per value head; every column then needs only independent
+// short dot products with its c. M's leading block is the inverse of L's
+// leading block, so a run of the first a + 1 rows sees exactly the
+// coefficients and the u the longer run had.
+//
+// The one-page step so keeps, in the record slot beside the candidates'
+// rows, their coefficients (G/|k|, G/|q|, G, R/|k|, M, N) and their u per
+// value column (fp32). The next step's replay of the first a + 1 of them is
+// then only the rank-(a+1) update S_a = G_a S + sum_s (R[a][s]/|k_s|) k_s u_s^T
+// of the stored state: the u it needs are the ones the candidate run formed
+// from that same stored state. The slot layout runs the candidates and
+// stores every S_t. All three entry points compute each quantity with the
+// same code and in the same order from the same inputs, so the one-page
 // checkpoint equals the slot that was kept for it, bit for bit, and so do
 // all outputs.
 //
-// Work decomposition. One CTA per (request, q/k head kh, split): the Hv/Hk
-// value heads that read q/k head kh, in items of 64 value columns; a
-// request's items may be split over several CTAs when the batch alone would
-// not fill the GPU (not with the conv fused in: every CTA of a group reads
-// the q/k window columns that the group's writer rolls, so the fused step
-// runs one CTA per group). A CTA stages the group's rows, forms the
-// candidates' Gram products and gates once, and derives their run
-// coefficients per head in shared memory. Items then run with no block-wide
-// barrier: 4 warps x 16 columns; inside a warp, 4 groups of 4 columns x 8
-// lanes, a lane holding 4 columns x Dk/8 entries of S in registers (chunks
-// of 16 bytes at Dk index VEC (8 i + r8)). Each 16-byte shared load of a q/k
-// row by an 8-lane quarter of the warp reads 128 distinct bytes and feeds 4
-// columns. The per-column scalar work (c, u = M c, the outputs) goes through
-// a small per-warp scratch: the dot products land there, then each lane
-// takes one column and half of the rows, which keeps the per-column arrays
-// out of registers (161 of them, 3 CTAs per SM). The next item's state is
-// copied into shared memory by the thread that will read it (cp.async)
-// while the current one is computed.
+// Kernels.
+// - spec_coef_kernel, one CTA per (request, q/k head kh): stages the
+//   candidates' q and k rows of kh (the fused step convolves the group's
+//   q, k and v channels first and writes them into the record), forms their
+//   Gram products and gates once, derives the run coefficients of every
+//   value head of the group, and stores them in the record slot the
+//   candidates go to.
+// - spec_item_kernel, one CTA per (request, value head, block of 64 value
+//   columns): copies its part of the state while it reads the flag word and
+//   the replay's inputs, then (after the coefficient kernel, which it follows
+//   as a programmatic dependent launch) the candidates' rows and
+//   coefficients; replays and stores the checkpoint; runs the candidates and
+//   stores their outputs and u. The last CTA of a request publishes the new
+//   flag word. Small CTAs of one item each keep the SMs evenly loaded to the
+//   end of the launch.
+// - spec_slots_kernel, one CTA per (request, q/k head, split): the slot
+//   layout. It forms the coefficients with the coefficient kernel's code,
+//   then per item runs the candidates from the source slot and rebuilds and
+//   stores the state after each one.
+//
+// Inside an item: 4 warps x 16 columns; inside a warp, 4 groups of 4
+// columns x 8 lanes, a lane holding 4 columns x Dk/8 entries of S in
+// registers (chunks of 16 bytes at Dk index VEC (8 i + r8)). Each 16-byte
+// shared load of a q/k row by an 8-lane quarter of the warp reads 128
+// distinct bytes and feeds 4 columns. The per-column scalar work (c, u = M c,
+// the outputs) goes through a small per-warp scratch: the dot products land
+// there, then each lane takes one column and half of the rows, which keeps
+// the per-column arrays out of registers. A state item is copied into shared
+// memory by the thread that will read it (cp.async).
 #pragma once
 
 #include "common.cuh"
@@ -110,53 +122,78 @@ struct RunCoef {
   float nq[kSpecK][kSpecK];    // N = B M                               (s <= t)
 };
 
-// The record keeps, per value head, the fields the next step's replay needs
-// (gk, gam, rk, m: kRunCoefFloats values) in this order.
+// The record keeps, per value head, gk gq gam (24 floats) and rk m nq (192
+// floats): kRunCoefFloats values, in 16-byte pieces. Piece k of the record
+// block sits at float spec_coef_piece(k) of a RunCoef: gk 0-1, gq 2-3,
+// gam 4-5, rk 6-21, m 22-37, nq 38-53.
 static_assert(offsetof(RunCoef, gk) == 0 && offsetof(RunCoef, gam) == 64 &&
-                  offsetof(RunCoef, rk) == 640 && offsetof(RunCoef, m) == 896,
+                  offsetof(RunCoef, beta) == 96 && offsetof(RunCoef, rk) == 640 &&
+                  offsetof(RunCoef, nq) == 1152 && sizeof(RunCoef) == 1408,
               "record coefficient copy offsets");
-static_assert(kRunCoefFloats == 8 + 8 + 64 + 64, "record coefficient block");
+static_assert(kRunCoefFloats == 24 + 192, "record coefficient block");
+constexpr int kCoefPieces = (int)kRunCoefFloats / 4;
+__host__ __device__ constexpr int spec_coef_piece(int k) { return k < 6 ? 4 * k : 160 + 4 * (k - 6); }
 
-// Raw dot products of a CTA's rows (k_s.k_t with s <= t, k_s.q_t, q_t.q_t).
+// Raw dot products of the candidate rows (k_s.k_t and k_s.q_t with s <= t,
+// q_t.q_t).
 struct RunDots {
-  float kkr[kSpecK][kSpecK];   // replayed rows: [t][s]
-  float kkc[kSpecK][kSpecK];   // candidates: [t][s]
-  float kqc[kSpecK][kSpecK];   // candidates: k_s.q_t at [t][s]
+  float kkc[kSpecK][kSpecK];   // [t][s]
+  float kqc[kSpecK][kSpecK];   // k_s.q_t at [t][s]
   float qqc[kSpecK];
-};
-
-// Dynamic shared memory of the spec kernel (byte offsets, 16-byte aligned).
-struct SpecSmem {
-  uint32_t raw;     // [2 Kc][RW] io dtype: rows q | k | v of the group
-  uint32_t ab;      // [2 Kc][2 Gh] float: a then b per head of the group
-  uint32_t kx;      // [2 Kc][DKP] float: k rows (replayed, then candidates)
-  uint32_t qx;      // [Kc][DKP] float: candidate q rows
-  uint32_t dots;    // RunDots
-  uint32_t gates;   // [Gh][2 runs][2][Kc] float: alpha, beta
-  uint32_t coef;    // RunCoef [Gh][2 runs]
-  uint32_t stage;   // [NC][threads] 16-byte chunks: one item's state per thread
-  uint32_t scr;     // per warp: [2 Kc][16] dot products, [Kc][16] u of its columns
-  uint32_t total;
-  int RW, DKP;
 };
 
 __host__ __device__ inline uint32_t spec_al16(uint32_t x) { return (x + 15u) & ~15u; }
 
-__host__ __device__ inline SpecSmem spec_smem(int DK, int DV, int Gh, int io_bytes,
-                                               int st_bytes) {
+// Dynamic shared memory of the three kernels (byte offsets, 16-byte aligned;
+// a region a kernel does not use has size 0).
+struct SpecSmem {
+  uint32_t raw;     // coef / slots: [Kc][RW] io dtype, the candidates' rows
+  uint32_t ab;      // coef / slots: [Kc][2 Gh] float: a then b per head
+  uint32_t hc;      // coef / slots: [Gh][2] float: A_log, dt_bias per head
+  uint32_t kx;      // [NK][DKP] float: k rows (items: replayed 0..7, candidates 8..15)
+  uint32_t qx;      // [Kc][DKP] float: candidate q rows
+  uint32_t dots;    // coef / slots: RunDots
+  uint32_t gates;   // coef / slots: [Gh][2][Kc] float: alpha, beta
+  uint32_t coef;    // RunCoef: coef / slots [Gh]; items [3] (record slots 0 and 1, candidates)
+  uint32_t rawk;    // items: [3 Kc][DK] io dtype (record slots 0 and 1, candidates)
+  uint32_t rawq;    // items: [Kc][DK] io dtype
+  uint32_t rawv;    // items: [Kc][VW] io dtype, the candidates' v of the CTA's columns
+  uint32_t ur;      // items: [Kc][VW] float, the record's u of the CTA's columns
+  uint32_t stage;   // items / slots: [NC][threads] 16-byte chunks of one item's state
+  uint32_t scr;     // items / slots: per warp [2 Kc][16] dot products, [Kc][16] u
+  uint32_t total;
+  int RW, DKP, VW;
+};
+
+// kind: SPEC_VERIFY = the item kernel (VW value columns per CTA),
+// SPEC_FUSED = the coefficient kernel, SPEC_SLOTS = the slot kernel.
+__host__ __device__ inline SpecSmem spec_smem(int kind, int DK, int DV, int Gh, int io_bytes,
+                                               int st_bytes, int VW) {
   SpecSmem L;
-  L.RW = (2 * DK + Gh * DV + 7) / 8 * 8;
   L.DKP = DK + 4;
+  L.RW = (kind == SPEC_SLOTS) ? (2 * DK + Gh * DV + 7) / 8 * 8 : 2 * DK;
+  L.VW = VW;
+  const bool items = (kind == SPEC_VERIFY), coef = (kind == SPEC_FUSED);
+  const uint32_t K = kSpecK;
   uint32_t off = 0;
-  L.raw = off;   off = spec_al16(off + (uint32_t)(2 * kSpecK * L.RW * io_bytes));
-  L.ab = off;    off = spec_al16(off + (uint32_t)(2 * kSpecK * 2 * Gh * 4));
-  L.kx = off;    off = spec_al16(off + (uint32_t)(2 * kSpecK * L.DKP * 4));
-  L.qx = off;    off = spec_al16(off + (uint32_t)(kSpecK * L.DKP * 4));
-  L.dots = off;  off = spec_al16(off + (uint32_t)sizeof(RunDots));
-  L.gates = off; off = spec_al16(off + (uint32_t)(Gh * 2 * 2 * kSpecK * 4));
-  L.coef = off;  off = spec_al16(off + (uint32_t)(Gh * 2 * sizeof(RunCoef)));
-  L.stage = off; off = spec_al16(off + (uint32_t)(DK / 2 * st_bytes * kSpecThreads));
-  L.scr = off;   off = spec_al16(off + (uint32_t)((kSpecThreads / 32) * kSpecScr * 4));
+  auto take = [&](uint32_t& at, uint32_t bytes) {
+    at = off;
+    off = spec_al16(off + bytes);
+  };
+  take(L.raw, items ? 0u : K * L.RW * io_bytes);
+  take(L.ab, items ? 0u : K * 2 * Gh * 4);
+  take(L.hc, items ? 0u : Gh * 2 * 4);
+  take(L.kx, (items ? 2 * K : K) * L.DKP * 4);
+  take(L.qx, K * L.DKP * 4);
+  take(L.dots, items ? 0u : (uint32_t)sizeof(RunDots));
+  take(L.gates, items ? 0u : Gh * 2 * K * 4);
+  take(L.coef, (items ? 3u : (uint32_t)Gh) * (uint32_t)sizeof(RunCoef));
+  take(L.rawk, items ? 3 * K * DK * io_bytes : 0u);
+  take(L.rawq, items ? K * DK * io_bytes : 0u);
+  take(L.rawv, items ? K * VW * io_bytes : 0u);
+  take(L.ur, items ? K * VW * 4 : 0u);
+  take(L.stage, coef ? 0u : (uint32_t)(DK / 2 * st_bytes * kSpecThreads));
+  take(L.scr, coef ? 0u : (uint32_t)((kSpecThreads / 32) * kSpecScr * 4));
   L.total = off;
   return L;
 }
@@ -265,12 +302,12 @@ __device__ __forceinline__ void spec_dots(const SpecS<DK>& S, const float* const
 
 // S <- the state after row a of a run that started from S:
 //   G_a S + sum_{s<=a} k_s (R[a][s] / |k_s|) u_s^T,
-// k rows (raw, fp32, stored by spec_xpos) at kx + s * kstride; us[s * 16 +
-// m] holds u_s of the lane's column m (its warp's scratch).
+// k rows (raw, fp32, stored by spec_xpos) at kx + s * kstride; us[s * ustride
+// + m] holds u_s of the lane's column m.
 template <int DK, class ST>
 __device__ __forceinline__ void spec_advance(SpecS<DK>& S, const RunCoef& C, int a,
                                              const float* kx, int kstride, const float* us,
-                                             int r8) {
+                                             int ustride, int r8) {
   using M = SpecMap<DK, ST>;
   const float gm = C.gam[a];
   const float2 g2 = make_float2(gm, gm);
@@ -282,7 +319,7 @@ __device__ __forceinline__ void spec_advance(SpecS<DK>& S, const RunCoef& C, int
   for (int s = 0; s < kSpecK; ++s) {
     if (s <= a) {
       const float c = C.rk[a][s];
-      const float4 u4 = *reinterpret_cast<const float4*>(us + s * 16);
+      const float4 u4 = *reinterpret_cast<const float4*>(us + s * ustride);
       const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
       float2 w2[4];
 #pragma unroll
@@ -324,6 +361,22 @@ __device__ __forceinline__ float spec_rowdot(const float* a, const float* b) {
   return __fadd_rn(__fadd_rn(acc.x, acc.y), __fadd_rn(acc.z, acc.w));
 }
 
+// fp32 copies of n rows (io dtype, DK apart from src, q/k entries at column
+// 0) in the order the lanes read them, dst rows DKP apart. Block-wide loop
+// over NT threads.
+template <int DK, class ST, class IO, int NT>
+__device__ __forceinline__ void spec_rows_f32(float* dst, int DKP, const IO* src, int sstride,
+                                              int n) {
+  constexpr int Q4 = DK / 4;
+  for (int idx = threadIdx.x; idx < n * Q4; idx += NT) {
+    const int t = idx / Q4, d = (idx % Q4) * 4;
+    float f[4];
+    load_f<IO, 4>(src + (size_t)t * sstride + d, f);
+    *reinterpret_cast<float4*>(dst + t * DKP + spec_xpos<DK, ST>(d)) =
+        make_float4(f[0], f[1], f[2], f[3]);
+  }
+}
+
 // (s, t) with s <= t of triangular task index k (row t holds t + 1 tasks).
 __device__ __forceinline__ void spec_tri(int k, int& s, int& t) {
   t = 0;
@@ -334,7 +387,6 @@ __device__ __forceinline__ void spec_tri(int k, int& s, int& t) {
   s = k;
 }
 
-
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
@@ -342,162 +394,312 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 // All of this thread's copy groups but the most recent one have landed.
 __device__ __forceinline__ void cp_async_wait_all_but_one() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
-// The verify runs 3 CTAs per SM (161 registers): measured faster than 2 (the
-// item loop is bound by latency, not by a pipe) and than 4 (which spills).
-// The slot layout keeps every candidate's state in registers on its way out
-// and spilled 280 bytes at 3 per SM; at 2 per SM (240 registers) it does not
-// spill and runs 244 us per 64-request step, against 294 us.
-template <class IO, class ST, int DK, int MODE>
-__global__ void __launch_bounds__(kSpecThreads, MODE == SPEC_SLOTS ? 2 : 3)
-spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_in,
-            const IO* __restrict__ conv_w, const IO* __restrict__ a_in,
-            const IO* __restrict__ b_in, void* o, int out_f32, void* pages, int32_t* status,
-            int splits) {
-  using M = SpecMap<DK, ST>;
+// The candidates' Gram products, gates and run coefficients for the value
+// heads g_lo .. g_lo+ng-1 of a group. Block-wide over NT threads: every
+// thread calls it, with the rows, gate inputs and head constants in shared
+// memory and visible to all.
+//   kx, qx [n_c][DKP] float: the k and q rows, stored by spec_xpos (the Gram
+//          products sum in that order)
+//   abs_  [n_c][2 Gh] float: a of head g at g, b at Gh + g
+//   hc    [Gh][2] float: A_log, dt_bias of head g
+//   coef  [Gh] RunCoef: coef[g] receives head g's candidate coefficients
+// Loops over rows run to kSpecK with guards, so every array index is a
+// compile-time constant.
+template <int DK, int NT>
+__device__ void spec_candidate_coefs(const Params& P, int Gh, int g_lo, int ng, int n_c,
+                                     const float* kx, const float* qx, int DKP,
+                                     const float* abs_, const float* hc, RunDots& D, float* gts,
+                                     RunCoef* coef) {
+  const int tid = threadIdx.x;
+  // Gram products and norms; gates of the heads, thread -> (head, row); the
+  // coefficient blocks start from zero (the entries past the run stay zero
+  // wherever they are stored)
+  {
+    const int Bc = n_c * (n_c + 1) / 2;
+    for (int k0 = tid; k0 < 2 * Bc + n_c; k0 += NT) {
+      int k = k0;
+      if (k < Bc) {
+        int s, t;
+        spec_tri(k, s, t);
+        D.kkc[t][s] = spec_rowdot<DK>(kx + s * DKP, kx + t * DKP);
+      } else if ((k -= Bc) < Bc) {
+        int s, t;
+        spec_tri(k, s, t);
+        D.kqc[t][s] = spec_rowdot<DK>(kx + s * DKP, qx + t * DKP);
+      } else {
+        k -= Bc;
+        D.qqc[k] = spec_rowdot<DK>(qx + k * DKP, qx + k * DKP);
+      }
+    }
+    for (int idx = tid; idx < ng * n_c; idx += NT) {
+      const int g = g_lo + idx / n_c, t = idx % n_c;
+      float alpha, beta;
+      gates_v(P.gate_mode, hc[2 * g], hc[2 * g + 1], abs_[t * 2 * Gh + g],
+              abs_[t * 2 * Gh + Gh + g], alpha, beta);
+      gts[(g * 2 + 0) * kSpecK + t] = alpha;
+      gts[(g * 2 + 1) * kSpecK + t] = beta;
+    }
+    constexpr int C4 = (int)(sizeof(RunCoef) / 16);
+    for (int idx = tid; idx < ng * C4; idx += NT) {
+      const int g = g_lo + idx / C4, k4 = idx % C4;
+      reinterpret_cast<float4*>(&coef[g])[k4] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  __syncthreads();
+  // (a) thread -> (head, column s = -1..7): decay products R[.][s], G, and
+  // the columns of L, B and R/|k|
+  for (int idx = tid; idx < ng * (kSpecK + 1); idx += NT) {
+    const int g = g_lo + idx / (kSpecK + 1);
+    const int s = idx % (kSpecK + 1) - 1;
+    const int n = n_c;
+    if (s >= n) continue;
+    RunCoef& C = coef[g];
+    const float* al = gts + (g * 2 + 0) * kSpecK;
+    const float* be = gts + (g * 2 + 1) * kSpecK;
+    float ik[kSpecK], iq[kSpecK];
+#pragma unroll
+    for (int t = 0; t < kSpecK; ++t) {
+      ik[t] = (t < n) ? rsqrtf(__fadd_rn(D.kkc[t][t], P.eps)) : 0.0f;
+      iq[t] = (t < n) ? rsqrtf(__fadd_rn(D.qqc[t], P.eps)) : 0.0f;
+    }
+    if (s < 0) {
+      float r = 1.0f;
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) {
+        if (t < n) {
+          r = __fmul_rn(r, al[t]);
+          C.gam[t] = r;
+          C.gk[t] = __fmul_rn(r, ik[t]);
+          C.gq[t] = __fmul_rn(r, iq[t]);
+          C.beta[t] = be[t];
+        }
+      }
+    } else {
+      float iks = 0.0f;
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) iks = (t == s) ? ik[t] : iks;
+      float r = 1.0f;
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) {
+        if (t >= s && t < n) {
+          if (t > s) r = __fmul_rn(r, al[t]);
+          C.rk[t][s] = __fmul_rn(r, iks);
+          if (t > s) {
+            const float kk = D.kkc[t][s];
+            C.l[t][s] = -__fmul_rn(be[t], __fmul_rn(r, __fmul_rn(__fmul_rn(kk, iks), ik[t])));
+          }
+          C.bco[t][s] = __fmul_rn(r, __fmul_rn(__fmul_rn(D.kqc[t][s], iks), iq[t]));
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // (b) thread -> (head, column s): column s of (I - L)^-1 by forward
+  // substitution (rows in increasing order, terms r = s .. t-1), times beta_s
+  for (int idx = tid; idx < ng * kSpecK; idx += NT) {
+    const int g = g_lo + idx / kSpecK;
+    const int s = idx % kSpecK;
+    const int n = n_c;
+    if (s >= n) continue;
+    RunCoef& C = coef[g];
+    float Lr[kSpecK][kSpecK];
+#pragma unroll
+    for (int t = 0; t < kSpecK; ++t)
+#pragma unroll
+      for (int r = 0; r < t; ++r) Lr[t][r] = (t < n && r >= s) ? C.l[t][r] : 0.0f;
+    float col[kSpecK];   // col[t] = (I - L)^-1 [t][s]
+    const float bs = C.beta[s];
+#pragma unroll
+    for (int t = 0; t < kSpecK; ++t) {
+      if (t < s) {
+        col[t] = 0.0f;
+      } else if (t == s) {
+        col[t] = 1.0f;
+        C.m[t][s] = bs;
+      } else if (t < n) {
+        float acc = 0.0f;
+        bool first = true;
+#pragma unroll
+        for (int r = 0; r < t; ++r) {
+          if (r >= s) {
+            acc = first ? __fmul_rn(Lr[t][r], col[r]) : __fmaf_rn(Lr[t][r], col[r], acc);
+            first = false;
+          }
+        }
+        col[t] = acc;
+        C.m[t][s] = __fmul_rn(acc, bs);
+      }
+    }
+  }
+  __syncthreads();
+  // (c) thread -> (head, row t, column s): N[t][s] = sum_r B[t][r] M[r][s]
+  for (int idx = tid; idx < ng * kSpecK * kSpecK; idx += NT) {
+    const int g = g_lo + idx / (kSpecK * kSpecK);
+    const int t = (idx / kSpecK) % kSpecK, s = idx % kSpecK;
+    if (t >= n_c || s > t) continue;
+    RunCoef& C = coef[g];
+    float acc = __fmul_rn(C.bco[t][s], C.m[s][s]);
+    for (int r = s + 1; r <= t; ++r) acc = __fmaf_rn(C.bco[t][r], C.m[r][s], acc);
+    C.nq[t][s] = acc;
+  }
+  __syncthreads();
+}
+
+// The candidates' dot products with the item's state (k rows at kc, q rows
+// at qx, DKP apart) into the warp's scratch (dsc[t][j]: k rows at t, q rows
+// at kSpecK + t); after the first pair, after_first() runs (S is then in
+// registers, so the next item's copy may start).
+template <int DK, class ST, class F>
+__device__ __forceinline__ void spec_candidate_dots(const SpecS<DK>& S, const float* kc,
+                                                    const float* qx, int DKP, int n_c, int r8,
+                                                    bool b2, bool b1, float* dsc, int jw,
+                                                    bool writer, F&& after_first) {
+#pragma unroll
+  for (int t = 0; t < kSpecK; t += 2) {
+    if (t < n_c) {
+      const float* xr[4] = {kc + t * DKP, kc + (t + 1) * DKP, qx + t * DKP, qx + (t + 1) * DKP};
+      float out[4];
+      spec_dots<DK, ST, 4>(S, xr, r8, b2, b1, out);
+      if (writer) {
+        dsc[t * 16 + jw] = out[0];
+        dsc[(t + 1) * 16 + jw] = out[1];
+        dsc[(kSpecK + t) * 16 + jw] = out[2];
+        dsc[(kSpecK + t + 1) * 16 + jw] = out[3];
+      }
+      if (t == 0) after_first();
+    }
+  }
+}
+
+// The candidates' per-column work of one item once their dot products are in
+// the warp's scratch: c_t = v_t - G_t/|k_t| (S^T k_t), the outputs
+// o_t = scale (G_t/|q_t| (S^T q_t) + sum_s N[t][s] c_s), then
+// u_t = sum_s M[t][s] c_s, for column jc of the warp and the rows
+// t = 2 tt + th. v_t of the column at vsrc[t * vstride]; o_t at
+// o0 + t * ostride; u_t is handed to put_u(t, u).
+template <class IO, class PutU>
+__device__ __forceinline__ void spec_candidate_columns(const RunCoef& C, const float* dsc, int jc,
+                                                       int th, int n_c, const IO* vsrc,
+                                                       int vstride, float scale, void* o,
+                                                       int out_f32, size_t o0, size_t ostride,
+                                                       PutU&& put_u) {
+  float c[kSpecK];
+#pragma unroll
+  for (int t = 0; t < kSpecK; ++t)
+    c[t] = (t < n_c) ? __fmaf_rn(-C.gk[t], dsc[t * 16 + jc], to_f(vsrc[(size_t)t * vstride]))
+                     : 0.0f;
+#pragma unroll
+  for (int tt = 0; tt < kSpecK / 2; ++tt) {
+    const int t = 2 * tt + th;
+    if (t < n_c) {
+      float acc = __fmul_rn(C.gq[t], dsc[(kSpecK + t) * 16 + jc]);
+#pragma unroll
+      for (int s = 0; s <= 2 * tt + 1; ++s)
+        if (s <= t) acc = __fmaf_rn(C.nq[t][s], c[s], acc);
+      store_out(o, out_f32, o0 + (size_t)t * ostride, __fmul_rn(scale, acc));
+    }
+  }
+#pragma unroll
+  for (int tt = 0; tt < kSpecK / 2; ++tt) {
+    const int t = 2 * tt + th;
+    if (t < n_c) {
+      float acc = __fmul_rn(C.m[t][0], c[0]);
+#pragma unroll
+      for (int s = 1; s <= 2 * tt + 1; ++s)
+        if (s <= t) acc = __fmaf_rn(C.m[t][s], c[s], acc);
+      put_u(t, acc);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One-page step, part 1: the candidates' run coefficients per value head.
+template <class IO, class ST, int DK, bool FUSED>
+__global__ void __launch_bounds__(kSpecThreads)
+spec_coef_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in,
+                 const IO* __restrict__ conv_w, const IO* __restrict__ a_in,
+                 const IO* __restrict__ b_in, void* pages, int32_t* status) {
+  constexpr int NT = kSpecThreads;
   constexpr int DV = DK;
-  constexpr int CR = kSpecK;                       // first row of the candidates
-  constexpr int VE = 16 / (int)sizeof(IO);         // io elements per 16-byte piece
+  constexpr int VE = 16 / (int)sizeof(IO);
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_begin();
 
   const int Gh = G.Hv / G.Hk;
-  const int kh = blockIdx.x / splits, split = blockIdx.x % splits;
-  const int BVI = DV < kSpecBV ? DV : kSpecBV;     // columns per item
-  const int nCB = DV / BVI;
-  const int n_items = Gh * nCB;
-  const int per = (n_items + splits - 1) / splits;
-  const int it0 = split * per, it1 = min(n_items, it0 + per);
-  const int h0 = kh * Gh;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r8 = lane & 7, cg = lane >> 3;
-  const bool b2 = (r8 & 4) != 0, b1 = (r8 & 2) != 0, b0 = (r8 & 1) != 0;
-  const int colw = 16 * warp + 4 * cg;             // the lane's first column in an item
-  const int cown = 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0); // the column its dot products end in
-  const bool active = colw < BVI;
+  const int kh = blockIdx.x, h0 = kh * Gh;
+  const int tid = threadIdx.x;
   const bool reporter = (blockIdx.x == 0 && tid == 0);
-
   const Req q = load_req(B, blockIdx.y);
   if (q.err) {
     if (reporter) report(status, q.err);
     return;
   }
-  if (MODE != SPEC_SLOTS && !q.spec) return;
+  if (!q.spec) return;
 
-  const SpecSmem L = spec_smem(DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST));
+  const SpecSmem L = spec_smem(SPEC_FUSED, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), 0);
   IO* raw = reinterpret_cast<IO*>(smem + L.raw);
   float* abs_ = reinterpret_cast<float*>(smem + L.ab);
-  float* kx = reinterpret_cast<float*>(smem + L.kx);
-  float* qx = reinterpret_cast<float*>(smem + L.qx);
-  RunDots& D = *reinterpret_cast<RunDots*>(smem + L.dots);
-  float* gts = reinterpret_cast<float*>(smem + L.gates);
-  RunCoef* coef = reinterpret_cast<RunCoef*>(smem + L.coef);
-  uint8_t* stage = smem + L.stage;
-  const int RW = L.RW, DKP = L.DKP;
-  const int g_lo = it0 / nCB, g_hi = (it1 > it0) ? (it1 - 1) / nCB + 1 : g_lo;  // own heads
-  const int ng = g_hi - g_lo;
+  float* hc = reinterpret_cast<float*>(smem + L.hc);
+  const int RW = L.RW;
   const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK, v_off = 2 * G.Hk * DK + h0 * DV;
-  const int n_c = q.len;
-  // channel of row element c (q | k | v of the group's heads) in a packed row
+  const int n_c = (q.len <= G.Kc) ? q.len : 0;   // (more is an error, found below)
+  // channel of group element c (q | k | v of the group's heads)
   auto chan = [&](int c) {
     return (c < DK) ? q_off + c : (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
   };
-  const int row_els = 2 * DK + Gh * DV;
-  const int pieces = row_els / VE;
 
-  // ---- 1. this step's candidate rows start copying (they do not depend on
-  // the page), then the page is checked ---------------------------------
-  if constexpr (MODE != SPEC_FUSED) {
-    if (q.len <= G.Kc) {
-      for (int idx = tid; idx < n_c * pieces; idx += kSpecThreads) {
-        const int t = idx / pieces, c = (idx % pieces) * VE;
-        cp_async16(raw + (size_t)(CR + t) * RW + c, rows_in + (size_t)(q.start + t) * G.C + chan(c));
-      }
+  // ---- the candidates' q and k rows start copying; the flag word, the gate
+  // inputs and the heads' constants are loaded together (none depends on
+  // another), then the page is checked
+  if constexpr (!FUSED) {
+    constexpr int pieces = 2 * DK / VE;
+    for (int idx = tid; idx < n_c * pieces; idx += NT) {
+      const int t = idx / pieces, c = (idx % pieces) * VE;
+      cp_async16(raw + (size_t)t * RW + c, rows_in + (size_t)(q.start + t) * G.C + chan(c));
     }
   }
   cp_async_commit();
-
   char* pg = page_ptr(G, pages, q.page);
-  ST* Sbase;
-  int n_r = 0, live = 0, parity = 0;
-  uint32_t* flagp = nullptr;
-  int err = 0;
-  if constexpr (MODE == SPEC_SLOTS) {
-    const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
-    if (src < 0 || src >= G.Kc) err = GDN_DEV_BAD_ACCEPTED;
-    else if (q.len > G.Kc) err = GDN_DEV_TOO_MANY_CANDIDATES;
-    pg = reinterpret_cast<char*>(pages) + (size_t)q.page * SG.pool_bytes;
-    Sbase = reinterpret_cast<ST*>(pg + (size_t)(err ? 0 : src) * SG.slot_bytes + SG.state_off);
-  } else {
-    Sbase = reinterpret_cast<ST*>(pg + G.state_off);
-    flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
-    const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
-    SpecState ss = spec_state(G, B, q, flag);
-    if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
-    err = ss.err;
-    n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
-    live = ss.live;
-    parity = ss.parity;
+  uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+  const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
+  for (int idx = tid; idx < n_c * Gh; idx += NT) {
+    const int t = idx / Gh, g = idx % Gh;
+    const size_t rn = ((size_t)q.start + t) * G.Hv + h0 + g;
+    abs_[t * 2 * Gh + g] = to_f(a_in[rn]);
+    abs_[t * 2 * Gh + Gh + g] = to_f(b_in[rn]);
   }
-  if (err) {
-    if (reporter) report(status, err);
-    asm volatile("cp.async.wait_all;" ::: "memory");   // nothing lands after the CTA is gone
+  for (int g = tid; g < Gh; g += NT) {
+    hc[2 * g] = P.A_log[h0 + g];
+    hc[2 * g + 1] = P.dt_bias[h0 + g];
+  }
+  SpecState ss = spec_state(G, B, q, flag);
+  if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
+  if (ss.err) {
+    if (reporter) report(status, ss.err);
+    cp_async_wait_all();   // nothing lands after the CTA is gone
     return;
   }
-  const int n_all = n_r + n_c;
-  IO* rec = reinterpret_cast<IO*>(pg + G.record_off);   // one-page modes only
-  // head g's record gates and conv channels are written by the CTA holding
-  // its first item; the q/k channels by split 0
-  auto owns_head = [&](int g) { return (g * nCB) / per == split; };
-  auto item_col0 = [&](int it) -> ST* {
-    const int h = h0 + it / nCB, cb = it % nCB;
-    return Sbase + ((size_t)h * DV + (size_t)cb * BVI + colw) * DK;
-  };
+  const int n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
+  IO* rec_out = reinterpret_cast<IO*>(pg + G.record_off) + (size_t)(1 - ss.live) * G.Kc * G.rec_row;
 
-  // ---- 2. replayed rows (k and v from the live record slot), the fused
-  // conv, gate inputs; the first item's state starts copying last ---------
-  for (int idx = tid; idx < n_r * pieces; idx += kSpecThreads) {
-    const int t = idx / pieces, c = (idx % pieces) * VE;
-    if (c < DK) continue;                            // a replayed row's q is not used
-    cp_async16(raw + (size_t)t * RW + c, rec + ((size_t)live * G.Kc + t) * G.rec_row + chan(c));
-  }
-  // the replay's run coefficients: those the previous step derived for the
-  // same rows as its candidates (the leading block is the same whatever the
-  // run's length), kept in the record slot beside them
-  if (n_r > 0) {
-    const float* rc = reinterpret_cast<const float*>(pg + G.rcoef_off) + (size_t)live * G.Hv * kRunCoefFloats;
-    for (int idx = tid; idx < ng * 36; idx += kSpecThreads) {
-      const int g = g_lo + idx / 36, k = idx % 36;
-      const float* src = rc + (size_t)(h0 + g) * kRunCoefFloats;
-      float* dst = reinterpret_cast<float*>(&coef[g * 2 + 0]);
-      // pieces 0-1: gk, 2-3: gam, 4-19: rk, 20-35: m (4 floats each)
-      const int so = 4 * k;
-      const int dofs = (k < 2) ? so : (k < 4) ? 16 + (so - 8) : (k < 20) ? 160 + (so - 16) : 224 + (so - 80);
-      cp_async16(dst + dofs, src + so);
-    }
-  }
-  cp_async_commit();
-  if (active && it0 < it1) spec_stage_async<DK, ST>(stage, item_col0(it0), r8, tid);
-  else cp_async_commit();   // keep "all but the newest group" meaning the rows
-
-  if constexpr (MODE == SPEC_FUSED) {
+  if constexpr (FUSED) {
     // the conv of the group's channels for this step's candidates, exactly
     // as gdn_conv computes it for a spec request: history = window columns
     // n_r .. n_r+W-2 (the record's accepted rows rolled out), taps oldest
-    // first, own SiLU, rounded to the io dtype. Every load of a channel
-    // vector is issued before its arithmetic.
-    const int nvec = row_els / 4;
+    // first, own SiLU, rounded to the io dtype; the rows go to the record.
+    // Every load of a channel vector is issued before its arithmetic.
+    const int nvec = (2 * DK + Gh * DV) / 4;
     IO* win = reinterpret_cast<IO*>(pg + G.window_off);
-    IO* rec_out = rec + (size_t)(1 - live) * G.Kc * G.rec_row;
-    for (int vi = tid; vi < nvec; vi += kSpecThreads) {
+    for (int vi = tid; vi < nvec; vi += NT) {
       const int c4 = 4 * vi;
-      const int gg = (c4 < 2 * DK) ? -1 : (c4 - 2 * DK) / DV;
-      if (gg >= 0 && (gg < g_lo || gg >= g_hi)) continue;   // another split's head
-      const bool owner = (gg < 0) ? (split == 0) : owns_head(gg);
       const int ch = chan(c4);
       float wt[4][4], hcol[3][4], h0c[3][4], xr[kSpecK][4];
       {
@@ -535,11 +737,9 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
             yv[v] = y2.x;
             yv[v + 1] = y2.y;
           }
-          store_f<IO, 4>(raw + (size_t)(CR + t) * RW + c4, yv);
-          if (owner) {
-            store_f<IO, 4>(rec_out + (size_t)t * G.rec_row + ch, yv);
-            store_f<IO, 4>(win + (size_t)(3 + t) * G.C + ch, xr[t]);
-          }
+          if (c4 < 2 * DK) store_f<IO, 4>(raw + (size_t)t * RW + c4, yv);
+          store_f<IO, 4>(rec_out + (size_t)t * G.rec_row + ch, yv);
+          store_f<IO, 4>(win + (size_t)(3 + t) * G.C + ch, xr[t]);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
             hcol[0][v] = hcol[1][v];
@@ -548,389 +748,426 @@ spec_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_
           }
         }
       }
-      if (owner) {
-        // window columns 0..2: the history this step started from
+      // window columns 0..2: the history this step started from
 #pragma unroll
-        for (int j = 0; j < 3; ++j) store_f<IO, 4>(win + (size_t)j * G.C + ch, h0c[j]);
-      }
+      for (int j = 0; j < 3; ++j) store_f<IO, 4>(win + (size_t)j * G.C + ch, h0c[j]);
     }
   }
-  // gate inputs per row and own head: record rows, then this step's rows
-  for (int idx = tid; idx < n_all * ng; idx += kSpecThreads) {
-    const int t = idx / ng, g = g_lo + idx % ng, h = h0 + g;
-    const int row = (t < n_r) ? t : CR + (t - n_r);
-    float av, bv;
-    if (t < n_r) {
-      const IO* rr = rec + ((size_t)live * G.Kc + t) * G.rec_row;
-      av = to_f(rr[G.C + h]);
-      bv = to_f(rr[G.C + G.Hv + h]);
-    } else {
-      const size_t rn = (size_t)q.start + (t - n_r);
-      av = to_f(a_in[rn * G.Hv + h]);
-      bv = to_f(b_in[rn * G.Hv + h]);
-      if (MODE != SPEC_SLOTS && owns_head(g)) {
-        // the candidates' gates go next to their conv'd rows in the other slot
-        IO* rr = rec + ((size_t)(1 - live) * G.Kc + (t - n_r)) * G.rec_row;
-        rr[G.C + h] = a_in[rn * G.Hv + h];
-        rr[G.C + G.Hv + h] = b_in[rn * G.Hv + h];
-      }
-    }
-    abs_[row * 2 * Gh + g] = av;
-    abs_[row * 2 * Gh + Gh + g] = bv;
+  // the candidates' gate inputs go next to their conv'd rows in the record slot
+  for (int idx = tid; idx < n_c * Gh; idx += NT) {
+    const int t = idx / Gh, g = idx % Gh, h = h0 + g;
+    const size_t rn = ((size_t)q.start + t) * G.Hv + h;
+    IO* rr = rec_out + (size_t)t * G.rec_row;
+    rr[G.C + h] = a_in[rn];
+    rr[G.C + G.Hv + h] = b_in[rn];
   }
-  cp_async_wait_all_but_one();   // the rows (not the state) have landed
+  cp_async_wait_all();
   __syncthreads();
+  if (n_c == 0) return;
 
-  // ---- 3. fp32 copies of the k rows (all) and q rows (candidates), each
-  // in the order the lanes read it (spec_xpos); the Gram products below sum
-  // over that order too ---------------------------------------------------
+  float* kx = reinterpret_cast<float*>(smem + L.kx);
+  float* qx = reinterpret_cast<float*>(smem + L.qx);
+  spec_rows_f32<DK, ST, IO, NT>(kx, L.DKP, raw + DK, RW, n_c);
+  spec_rows_f32<DK, ST, IO, NT>(qx, L.DKP, raw, RW, n_c);
+  __syncthreads();
+  RunCoef* coef = reinterpret_cast<RunCoef*>(smem + L.coef);
+  spec_candidate_coefs<DK, NT>(P, Gh, 0, Gh, n_c, kx, qx, L.DKP, abs_, hc,
+                               *reinterpret_cast<RunDots*>(smem + L.dots),
+                               reinterpret_cast<float*>(smem + L.gates), coef);
+  // the record's coefficient blocks of the slot the candidates go to
+  float* rc = reinterpret_cast<float*>(pg + G.rcoef_off) + (size_t)(1 - ss.live) * G.Hv * kRunCoefFloats;
+  for (int idx = tid; idx < Gh * kCoefPieces; idx += NT) {
+    const int g = idx / kCoefPieces, k = idx % kCoefPieces;
+    *reinterpret_cast<float4*>(rc + (size_t)(h0 + g) * kRunCoefFloats + 4 * k) =
+        *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(&coef[g]) +
+                                         spec_coef_piece(k));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One-page step, part 2: replay, checkpoint and the candidates, per item.
+// rows_in: the candidates' conv'd rows (gdn_spec_verify), or null to read
+// them from the record slot they went to (the fused step). nsplit CTAs per
+// value head, each with Dv / (BVI nsplit) items of BVI columns.
+//
+// 3 CTAs per SM (at most 168 registers): the items are bound by latency,
+// not by a pipe, and a fourth CTA would spill.
+template <class IO, class ST, int DK>
+__global__ void __launch_bounds__(kSpecThreads, 3)
+spec_item_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in, void* o, int out_f32,
+                 void* pages, int32_t* status, int nsplit) {
+  using M = SpecMap<DK, ST>;
+  constexpr int DV = DK;
+  constexpr int VE = 16 / (int)sizeof(IO);
+  extern __shared__ __align__(16) uint8_t smem[];
+
+  const int Gh = G.Hv / G.Hk;
+  const int h = blockIdx.x / nsplit, sp = blockIdx.x % nsplit, kh = h / Gh;
+  const int BVI = DV < kSpecBV ? DV : kSpecBV;     // columns per item
+  const int per = DV / BVI / nsplit;               // items per CTA
+  const int cb0 = sp * per;                        // first column block
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r8 = lane & 7, cg = lane >> 3;
+  const bool b2 = (r8 & 4) != 0, b1 = (r8 & 2) != 0;
+  const int colw = 16 * warp + 4 * cg;             // the lane's first column in an item
+  const int cown = 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0); // the column its dot products end in
+  const bool active = colw < BVI;
+  const bool reporter = (blockIdx.x == 0 && tid == 0);
+
+  // Until the wait on the coefficient kernel, this kernel uses only what the
+  // launches before that kernel wrote (it lets this one start only once they
+  // have completed): the request, the state, the flag word, the live record
+  // slot, the record's u and the caller's rows. (It also copies the other
+  // record slot, which the coefficient kernel may be writing, and ignores it.)
+  const Req q = load_req(B, blockIdx.y);
+  if (q.err) {
+    if (reporter) report(status, q.err);
+    return;
+  }
+  if (!q.spec) return;
+
+  const SpecSmem L = spec_smem(SPEC_VERIFY, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), per * BVI);
+  IO* rawk = reinterpret_cast<IO*>(smem + L.rawk);
+  IO* rawq = reinterpret_cast<IO*>(smem + L.rawq);
+  IO* rawv = reinterpret_cast<IO*>(smem + L.rawv);
+  float* ur = reinterpret_cast<float*>(smem + L.ur);
+  float* kx = reinterpret_cast<float*>(smem + L.kx);
+  float* qx = reinterpret_cast<float*>(smem + L.qx);
+  RunCoef* coef = reinterpret_cast<RunCoef*>(smem + L.coef);   // slots 0, 1; candidates
+  uint8_t* stage = smem + L.stage;
+  const int DKP = L.DKP, VW = L.VW;
+  const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK;
+  const int v_off = 2 * G.Hk * DK + h * DV + cb0 * BVI;     // the CTA's first v column
+  const int n_c = q.len;
+
+  char* pg = page_ptr(G, pages, q.page);
+  ST* Sbase = reinterpret_cast<ST*>(pg + G.state_off);
+  auto item_col0 = [&](int cb) -> ST* {
+    return Sbase + ((size_t)h * DV + (size_t)cb * BVI + colw) * DK;
+  };
+
+  // ---- 1. everything the setup reads from memory, at once: the first
+  // item's state, the flag word and the accepted count, both record slots' k
+  // rows and G, R/|k| blocks (which one is live comes with the flag), the
+  // record's u of the CTA's columns, and the caller's candidate rows
+  if (active) spec_stage_async<DK, ST>(stage, item_col0(cb0), r8, tid);
+  uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+  const int acc = B.n_accepted ? B.n_accepted[q.r] : -1;
+  const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
+  const IO* rec = reinterpret_cast<const IO*>(pg + G.record_off);
+  constexpr int RP = DK / VE;   // 16-byte pieces per q or k row
+  const int VP = VW / VE;
+  const int per_row = 2 * RP + VP;
+  for (int idx = tid; idx < 2 * G.Kc * RP; idx += kSpecThreads) {
+    const int st = idx / (G.Kc * RP), t = (idx / RP) % G.Kc, c = (idx % RP) * VE;
+    cp_async16(rawk + (size_t)(st * kSpecK + t) * DK + c,
+               rec + ((size_t)st * G.Kc + t) * G.rec_row + k_off + c);
+  }
+  for (int idx = tid; idx < 2 * 18; idx += kSpecThreads) {   // gam, rk of both slots
+    const int st = idx / 18, k = 4 + idx % 18;
+    const float* rc = reinterpret_cast<const float*>(pg + G.rcoef_off) +
+                      ((size_t)st * G.Hv + h) * kRunCoefFloats;
+    cp_async16(reinterpret_cast<float*>(&coef[st]) + spec_coef_piece(k), rc + 4 * k);
+  }
+  float* urec = reinterpret_cast<float*>(pg + G.ru_off) + (size_t)h * G.Kc * DV + cb0 * BVI;
   {
-    constexpr int Q4 = DK / 4;
-    const int nk = n_all * Q4;
-    for (int idx = tid; idx < nk + n_c * Q4; idx += kSpecThreads) {
-      float f[4];
-      if (idx < nk) {
-        const int r = idx / Q4, d = (idx % Q4) * 4;
-        const int row = (r < n_r) ? r : CR + (r - n_r);
-        load_f<IO, 4>(raw + (size_t)row * RW + DK + d, f);
-        *reinterpret_cast<float4*>(kx + row * DKP + spec_xpos<DK, ST>(d)) =
-            make_float4(f[0], f[1], f[2], f[3]);
-      } else {
-        const int t = (idx - nk) / Q4, d = ((idx - nk) % Q4) * 4;
-        load_f<IO, 4>(raw + (size_t)(CR + t) * RW + d, f);
-        *reinterpret_cast<float4*>(qx + t * DKP + spec_xpos<DK, ST>(d)) =
-            make_float4(f[0], f[1], f[2], f[3]);
-      }
+    const int UP = VW / 4;
+    for (int idx = tid; idx < G.Kc * UP; idx += kSpecThreads) {
+      const int s = idx / UP, c = (idx % UP) * 4;
+      cp_async16(ur + (size_t)s * VW + c, urec + (size_t)s * DV + c);
     }
   }
+  // where the candidates' piece p of row t goes, and where it comes from
+  auto cand_dst = [&](int t, int p) -> IO* {
+    return (p < RP) ? rawq + (size_t)t * DK + p * VE
+         : (p < 2 * RP) ? rawk + (size_t)(2 * kSpecK + t) * DK + (p - RP) * VE
+                        : rawv + (size_t)t * VW + (p - 2 * RP) * VE;
+  };
+  auto cand_src = [&](const IO* row, int p) -> const IO* {
+    return row + ((p < RP) ? q_off + p * VE : (p < 2 * RP) ? k_off + (p - RP) * VE
+                                                           : v_off + (p - 2 * RP) * VE);
+  };
+  if (rows_in && n_c <= G.Kc) {
+    for (int idx = tid; idx < n_c * per_row; idx += kSpecThreads) {
+      const int t = idx / per_row, p = idx % per_row;
+      cp_async16(cand_dst(t, p), cand_src(rows_in + (size_t)(q.start + t) * G.C, p));
+    }
+  }
+  cp_async_commit();
+  SpecState ss = spec_state_acc(G, q, flag, acc);
+  if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
+  if (ss.err) {
+    if (reporter) report(status, ss.err);
+    cp_async_wait_all();   // nothing lands after the CTA is gone
+    return;
+  }
+  const int n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
+  const int live = ss.live, parity = ss.parity;
+  const IO* cslot = rec + (size_t)(1 - live) * G.Kc * G.rec_row;
+  // what the coefficient kernel wrote: the candidates' coefficients and, in
+  // the fused step, their rows
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (!rows_in) {
+    for (int idx = tid; idx < n_c * per_row; idx += kSpecThreads) {
+      const int t = idx / per_row, p = idx % per_row;
+      cp_async16(cand_dst(t, p), cand_src(cslot + (size_t)t * G.rec_row, p));
+    }
+  }
+  if (n_c > 0) {
+    const float* rc = reinterpret_cast<const float*>(pg + G.rcoef_off) +
+                      ((size_t)(1 - live) * G.Hv + h) * kRunCoefFloats;
+    for (int i = tid; i < 36; i += kSpecThreads) {   // gk, gq, m, nq
+      const int k = (i < 4) ? i : 18 + i;
+      cp_async16(reinterpret_cast<float*>(&coef[2]) + spec_coef_piece(k), rc + 4 * k);
+    }
+  }
+  cp_async_commit();
+  cp_async_wait_all();
   __syncthreads();
 
-  // ---- 4. Gram products and norms (one per thread), gates ---------------
-  {
-    const int A = 0, Bc = n_c * (n_c + 1) / 2;   // (the replay's come from the record)
-    int k = tid;
-    if (k < A) {
-      int s, t;
-      spec_tri(k, s, t);
-      D.kkr[t][s] = spec_rowdot<DK>(kx + s * DKP, kx + t * DKP);
-    } else if ((k -= A) < Bc) {
-      int s, t;
-      spec_tri(k, s, t);
-      D.kkc[t][s] = spec_rowdot<DK>(kx + (CR + s) * DKP, kx + (CR + t) * DKP);
-    } else if ((k -= Bc) < Bc) {
-      int s, t;
-      spec_tri(k, s, t);
-      D.kqc[t][s] = spec_rowdot<DK>(kx + (CR + s) * DKP, qx + t * DKP);
-    } else if ((k -= Bc) < n_c) {
-      D.qqc[k] = spec_rowdot<DK>(qx + k * DKP, qx + k * DKP);
-    }
-    // gates of own heads for the candidates: thread -> (head, row); and the
-    // candidate run's coefficient blocks start from zero (the entries past
-    // the run stay zero wherever they are stored)
-    for (int idx = tid; idx < ng * n_c; idx += kSpecThreads) {
-      const int g = g_lo + idx / n_c, t = idx % n_c;
-      const int row = CR + t;
-      float alpha, beta;
-      gates(P, h0 + g, abs_[row * 2 * Gh + g], abs_[row * 2 * Gh + Gh + g], alpha, beta);
-      gts[((g * 2 + 1) * 2 + 0) * kSpecK + t] = alpha;
-      gts[((g * 2 + 1) * 2 + 1) * kSpecK + t] = beta;
-    }
-    for (int idx = tid; idx < ng * (int)(sizeof(RunCoef) / 16); idx += kSpecThreads) {
-      const int g = g_lo + idx / (int)(sizeof(RunCoef) / 16), k = idx % (int)(sizeof(RunCoef) / 16);
-      reinterpret_cast<float4*>(&coef[g * 2 + 1])[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
+  // ---- 2. fp32 copies of the rows, in the order the lanes read them: the
+  // live slot's replayed k rows at 0.., candidates' k rows at kSpecK.., q rows
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(kx, DKP, rawk + (size_t)live * kSpecK * DK, DK, n_r);
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(kx + kSpecK * DKP, DKP, rawk + 2 * kSpecK * DK, DK, n_c);
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(qx, DKP, rawq, DK, n_c);
   __syncthreads();
 
-  // ---- 5. run coefficients per own head and run --------------------------
-  {
-    // (a) thread -> (head, run, column s = -1..7): decay products R[.][s], G,
-    // and the columns of L, B and R/|k|. Loops run to kSpecK with guards, so
-    // every array index is a compile-time constant.
-    for (int idx = tid; idx < ng * (kSpecK + 1); idx += kSpecThreads) {
-      const int g = g_lo + idx / (kSpecK + 1);
-      const int run = 1;
-      const int s = idx % (kSpecK + 1) - 1;
-      const int n = run ? n_c : n_r;
-      if (s >= n) continue;
-      RunCoef& C = coef[g * 2 + run];
-      const float* al = gts + ((g * 2 + run) * 2 + 0) * kSpecK;
-      const float* be = gts + ((g * 2 + run) * 2 + 1) * kSpecK;
-      float ik[kSpecK], iq[kSpecK];
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t) {
-        ik[t] = (t < n) ? rsqrtf(__fadd_rn(run ? D.kkc[t][t] : D.kkr[t][t], P.eps)) : 0.0f;
-        iq[t] = (run && t < n) ? rsqrtf(__fadd_rn(D.qqc[t], P.eps)) : 0.0f;
+  // ---- 3. items: no block-wide barrier from here on. The next item's state
+  // starts copying once this one's is in registers.
+  const bool work = active && (n_r + n_c > 0);
+  float* dsc = reinterpret_cast<float*>(smem + L.scr) + warp * kSpecScr;
+  const int jw = 4 * cg + cown;                 // this lane's column in the warp
+  const bool writer = (r8 & 1) == 0;            // one of the column's two lanes
+  // the per-column phase maps lane -> (column jc of the warp, row half th)
+  const int jc = lane & 15, th = lane >> 4;
+  // the candidates' u replace the replayed rows' u (read above) in the record
+  float* uout = reinterpret_cast<float*>(pg + G.ru_off) + (size_t)h * G.Kc * DV;
+  for (int it = 0; it < per; ++it) {
+    const int cb = cb0 + it;
+    ST* col0 = item_col0(cb);
+    SpecS<DK> S;
+    bool ahead = !work || (it + 1 >= per);
+    auto prefetch = [&]() {
+      if (!ahead) {
+        spec_stage_async<DK, ST>(stage, item_col0(cb + 1), r8, tid);
+        ahead = true;
       }
-      if (s < 0) {
-        float r = 1.0f;
-#pragma unroll
-        for (int t = 0; t < kSpecK; ++t) {
-          if (t < n) {
-            r = __fmul_rn(r, al[t]);
-            C.gam[t] = r;
-            C.gk[t] = __fmul_rn(r, ik[t]);
-            C.gq[t] = __fmul_rn(r, iq[t]);
-            C.beta[t] = be[t];
-          }
-        }
-      } else {
-        float iks = 0.0f;
-#pragma unroll
-        for (int t = 0; t < kSpecK; ++t) iks = (t == s) ? ik[t] : iks;
-        float r = 1.0f;
-#pragma unroll
-        for (int t = 0; t < kSpecK; ++t) {
-          if (t >= s && t < n) {
-            if (t > s) r = __fmul_rn(r, al[t]);
-            C.rk[t][s] = __fmul_rn(r, iks);
-            if (t > s) {
-              const float kk = run ? D.kkc[t][s] : D.kkr[t][s];
-              C.l[t][s] = -__fmul_rn(be[t], __fmul_rn(r, __fmul_rn(__fmul_rn(kk, iks), ik[t])));
-            }
-            if (run) C.bco[t][s] = __fmul_rn(r, __fmul_rn(__fmul_rn(D.kqc[t][s], iks), iq[t]));
-          }
-        }
-      }
-    }
-    __syncthreads();
-    // (b) thread -> (head, run, column s): column s of (I - L)^-1 by forward
-    // substitution (rows in increasing order, terms r = s .. t-1), times beta_s
-    for (int idx = tid; idx < ng * kSpecK; idx += kSpecThreads) {
-      const int g = g_lo + idx / kSpecK;
-      const int run = 1;
-      const int s = idx % kSpecK;
-      const int n = run ? n_c : n_r;
-      if (s >= n) continue;
-      RunCoef& C = coef[g * 2 + run];
-      float Lr[kSpecK][kSpecK];
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t)
-#pragma unroll
-        for (int r = 0; r < t; ++r) Lr[t][r] = (t < n && r >= s) ? C.l[t][r] : 0.0f;
-      float col[kSpecK];   // col[t] = (I - L)^-1 [t][s]
-      const float bs = C.beta[s];
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t) {
-        if (t < s) {
-          col[t] = 0.0f;
-        } else if (t == s) {
-          col[t] = 1.0f;
-          C.m[t][s] = bs;
-        } else if (t < n) {
-          float acc = 0.0f;
-          bool first = true;
-#pragma unroll
-          for (int r = 0; r < t; ++r) {
-            if (r >= s) {
-              acc = first ? __fmul_rn(Lr[t][r], col[r]) : __fmaf_rn(Lr[t][r], col[r], acc);
-              first = false;
-            }
-          }
-          col[t] = acc;
-          C.m[t][s] = __fmul_rn(acc, bs);
-        }
-      }
-    }
-    __syncthreads();
-    // (c) thread -> (head, candidate row t, column s): N[t][s] = sum_r B[t][r] M[r][s]
-    for (int idx = tid; idx < ng * kSpecK * kSpecK; idx += kSpecThreads) {
-      const int g = g_lo + idx / (kSpecK * kSpecK);
-      const int t = (idx / kSpecK) % kSpecK, s = idx % kSpecK;
-      if (t >= n_c || s > t) continue;
-      RunCoef& C = coef[g * 2 + 1];
-      float acc = __fmul_rn(C.bco[t][s], C.m[s][s]);
-      for (int r = s + 1; r <= t; ++r) acc = __fmaf_rn(C.bco[t][r], C.m[r][s], acc);
-      C.nq[t][s] = acc;
-    }
-  }
-  __syncthreads();
-  if constexpr (MODE != SPEC_SLOTS) {
-    // the candidates' run coefficients go beside their rows in the other
-    // slot, for the next step's replay
-    if (n_c > 0) {
-      float* rc = reinterpret_cast<float*>(pg + G.rcoef_off) + (size_t)(1 - live) * G.Hv * kRunCoefFloats;
-      for (int idx = tid; idx < ng * 36; idx += kSpecThreads) {
-        const int g = g_lo + idx / 36, k = idx % 36;
-        if (!owns_head(g)) continue;
-        const float* src = reinterpret_cast<const float*>(&coef[g * 2 + 1]);
-        const int so = 4 * k;
-        const int sofs = (k < 2) ? so : (k < 4) ? 16 + (so - 8) : (k < 20) ? 160 + (so - 16) : 224 + (so - 80);
-        *reinterpret_cast<float4*>(rc + (size_t)(h0 + g) * kRunCoefFloats + so) =
-            *reinterpret_cast<const float4*>(src + sofs);
-      }
-    }
-  }
-
-  // ---- 6. items: no block-wide barrier from here on ---------------------
-  // An item's state comes from the stage (copied by this thread alone). The
-  // one-page modes request the next item's copy as soon as the first dot
-  // products have consumed the current one; the slot layout keeps the stage
-  // for the whole item (it rebuilds each candidate's state from it).
-  if (active && (n_all > 0 || MODE == SPEC_SLOTS)) {
-    const IO* vraw = raw + 2 * DK;
-    for (int it = it0; it < it1; ++it) {
-      const int g = it / nCB, cb = it % nCB, h = h0 + g;
-      ST* col0 = item_col0(it);
-      if (MODE == SPEC_SLOTS && it > it0) spec_stage_async<DK, ST>(stage, col0, r8, tid);
+    };
+    if (work) {
       spec_stage_wait();
-      SpecS<DK> S;
       spec_unstage<DK, ST>(S, stage, tid);
-      bool ahead = (MODE == SPEC_SLOTS) || (it + 1 >= it1);
-      auto prefetch = [&]() {
-        if (!ahead) {
-          spec_stage_async<DK, ST>(stage, item_col0(it + 1), r8, tid);
-          ahead = true;
-        }
-      };
-      // per-warp scratch: dsc[r][j] the dot products of row r (k rows 0..7,
-      // candidate q rows 8..15) with the warp's column j; usc[t][j] = u
-      float* dsc = reinterpret_cast<float*>(smem + L.scr) + warp * kSpecScr;
-      float* usc = dsc + 2 * kSpecK * 16;
-      const int jw = 4 * cg + cown;                 // this lane's column in the warp
-      const bool writer = (r8 & 1) == 0;            // one of the column's two lanes
-      // the scalar phase maps lane -> (column jc of the warp, row half th)
-      const int jc = lane & 15, th = lane >> 4;
-      const int vcol = g * DV + cb * BVI + 16 * warp + jc;   // v column of jc
-
-      if (n_r > 0) {
-        const RunCoef& C = coef[g * 2 + 0];
-#pragma unroll
-        for (int t = 0; t < kSpecK; t += 2) {
-          if (t < n_r) {
-            const float* xr[2] = {kx + t * DKP, kx + (t + 1) * DKP};
-            float out[2];
-            spec_dots<DK, ST, 2>(S, xr, r8, b2, b1, out);
-            if (writer) {
-              dsc[t * 16 + jw] = out[0];
-              dsc[(t + 1) * 16 + jw] = out[1];
-            }
-            if (t == 0) prefetch();
-          }
-        }
-        __syncwarp();
-        // c_t = v_t - G_t dk_t for column jc; u_t = sum_s M[t][s] c_s for
-        // the rows t of half th
-        {
-          float c[kSpecK];
-#pragma unroll
-          for (int t = 0; t < kSpecK; ++t)
-            c[t] = (t < n_r) ? __fmaf_rn(-C.gk[t], dsc[t * 16 + jc],
-                                         to_f(vraw[(size_t)t * RW + vcol])) : 0.0f;
-#pragma unroll
-          for (int tt = 0; tt < kSpecK / 2; ++tt) {
-            const int t = 2 * tt + th;
-            if (t < n_r) {
-              float acc = __fmul_rn(C.m[t][0], c[0]);
-#pragma unroll
-              for (int s = 1; s <= 2 * tt + 1; ++s)
-                if (s <= t) acc = __fmaf_rn(C.m[t][s], c[s], acc);
-              usc[t * 16 + jc] = acc;
-            }
-          }
-        }
-        __syncwarp();
-        spec_advance<DK, ST>(S, C, n_r - 1, kx, DKP, usc + 4 * cg, r8);
-        spec_store<DK, ST>(col0, S, r8);
-        // continue from exactly what was stored (a bf16 page rounds here)
-#pragma unroll
-        for (int m = 0; m < 4; ++m)
-#pragma unroll
-          for (int p = 0; p < M::P; ++p)
-            S.s[m][p] = make_float2(through<ST>(S.s[m][p].x), through<ST>(S.s[m][p].y));
-        __syncwarp();   // usc is read again only after this
-      }
-
-      if (n_c > 0) {
-        const RunCoef& C = coef[g * 2 + 1];
-        const float* kc = kx + CR * DKP;
-#pragma unroll
-        for (int t = 0; t < kSpecK; t += 2) {
-          if (t < n_c) {
-            const float* xr[4] = {kc + t * DKP, kc + (t + 1) * DKP, qx + t * DKP,
-                                  qx + (t + 1) * DKP};
-            float out[4];
-            spec_dots<DK, ST, 4>(S, xr, r8, b2, b1, out);
-            if (writer) {
-              dsc[t * 16 + jw] = out[0];
-              dsc[(t + 1) * 16 + jw] = out[1];
-              dsc[(kSpecK + t) * 16 + jw] = out[2];
-              dsc[(kSpecK + t + 1) * 16 + jw] = out[3];
-            }
-            if (t == 0) prefetch();
-          }
-        }
-        __syncwarp();
-        float c[kSpecK];
-#pragma unroll
-        for (int t = 0; t < kSpecK; ++t)
-          c[t] = (t < n_c) ? __fmaf_rn(-C.gk[t], dsc[t * 16 + jc],
-                                       to_f(vraw[(size_t)(CR + t) * RW + vcol])) : 0.0f;
-        // outputs o_t = scale (G_t S^T q^_t + sum_s N[t][s] c_s), column jc,
-        // the rows of half th
-        const size_t ocol = (size_t)h * DV + (size_t)cb * BVI + 16 * warp + jc;
-#pragma unroll
-        for (int tt = 0; tt < kSpecK / 2; ++tt) {
-          const int t = 2 * tt + th;
-          if (t < n_c) {
-            float acc = __fmul_rn(C.gq[t], dsc[(kSpecK + t) * 16 + jc]);
-#pragma unroll
-            for (int s = 0; s <= 2 * tt + 1; ++s)
-              if (s <= t) acc = __fmaf_rn(C.nq[t][s], c[s], acc);
-            store_out(o, out_f32, ((size_t)q.start + t) * G.Hv * DV + ocol,
-                      __fmul_rn(P.scale, acc));
-          }
-        }
-        if constexpr (MODE == SPEC_SLOTS) {
-          // u of the candidates, then the state after every candidate goes
-          // to its slot, each rebuilt from the staged starting state
-#pragma unroll
-          for (int tt = 0; tt < kSpecK / 2; ++tt) {
-            const int t = 2 * tt + th;
-            if (t < n_c) {
-              float acc = __fmul_rn(C.m[t][0], c[0]);
-#pragma unroll
-              for (int s = 1; s <= 2 * tt + 1; ++s)
-                if (s <= t) acc = __fmaf_rn(C.m[t][s], c[s], acc);
-              usc[t * 16 + jc] = acc;
-            }
-          }
-          __syncwarp();
-          const size_t off = (size_t)(col0 - Sbase);
-          for (int t = 0; t < n_c; ++t) {
-            SpecS<DK> T;
-            spec_unstage<DK, ST>(T, stage, tid);
-            spec_advance<DK, ST>(T, C, t, kc, DKP, usc + 4 * cg, r8);
-            ST* dst = reinterpret_cast<ST*>(pg + (size_t)t * SG.slot_bytes + SG.state_off) + off;
-            spec_store<DK, ST>(dst, T, r8);
-          }
-        }
-        __syncwarp();   // dsc / usc are written again only after this
-      }
-      prefetch();   // (a run with no rows never consumed the stage)
     }
+    if (work && n_r > 0) {
+      // the replay: S_a from the stored u of the accepted rows
+      spec_advance<DK, ST>(S, coef[live], n_r - 1, kx, DKP, ur + it * BVI + colw, VW, r8);
+      prefetch();
+      spec_store<DK, ST>(col0, S, r8);
+      // continue from exactly what was stored (a bf16 page rounds here)
+#pragma unroll
+      for (int m = 0; m < 4; ++m)
+#pragma unroll
+        for (int p = 0; p < M::P; ++p)
+          S.s[m][p] = make_float2(through<ST>(S.s[m][p].x), through<ST>(S.s[m][p].y));
+    }
+    if (work && n_c > 0) {
+      spec_candidate_dots<DK, ST>(S, kx + kSpecK * DKP, qx, DKP, n_c, r8, b2, b1, dsc, jw,
+                                  writer, prefetch);
+      __syncwarp();
+      const int col = cb * BVI + 16 * warp + jc;   // the column of jc in the head
+      spec_candidate_columns<IO>(
+          coef[2], dsc, jc, th, n_c, rawv + it * BVI + 16 * warp + jc, VW, P.scale, o, out_f32,
+          (size_t)q.start * G.Hv * DV + (size_t)h * DV + col, (size_t)G.Hv * DV,
+          [&](int t, float u) { uout[(size_t)t * DV + col] = u; });
+      __syncwarp();   // dsc is written again only after this
+    }
+    prefetch();   // (a run with no rows never consumed the stage)
   }
   spec_stage_wait();   // no copy outlives the CTA's shared memory
 
-  // ---- 7. the last CTA of the request publishes the new flag word -------
+  // ---- 4. the last CTA of the request publishes the new flag word -------
   // No fence orders the page data first: only later launches read it. The
   // counter needs none either: every CTA read the flag before its own
   // increment of the same word, so the publish follows every read.
-  if constexpr (MODE != SPEC_SLOTS) {
-    if (tid == 0) {
-      const uint32_t total = (uint32_t)(G.Hk * splits);
-      const uint32_t old = atomicAdd(flagp, 256u);
-      if ((old >> 8) == total - 1) {
-        const int nl = (n_c > 0) ? 1 - live : live;
-        atomicExch(flagp, make_flag(nl, 1 - parity, n_c));
-      }
+  if (tid == 0) {
+    const uint32_t total = (uint32_t)(G.Hv * nsplit);
+    const uint32_t old = atomicAdd(flagp, 256u);
+    if ((old >> 8) == total - 1) {
+      const int nl = (n_c > 0) ? 1 - live : live;
+      atomicExch(flagp, make_flag(nl, 1 - parity, n_c));
     }
   }
 }
 
-// Dynamic shared memory the spec kernel needs, and the most any launch may
-// ask for (the kernels' attribute is raised to it once per device).
+// ---------------------------------------------------------------------------
+// Slot-per-candidate layout. 2 CTAs per SM (240 registers): the per-candidate
+// rebuild keeps a second state in registers, and at 3 per SM it spilled 280
+// bytes and ran 294 us per 64-request step, against 244 us at 2.
+template <class IO, class ST, int DK>
+__global__ void __launch_bounds__(kSpecThreads, 2)
+spec_slots_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ rows_in,
+                  const IO* __restrict__ a_in, const IO* __restrict__ b_in, void* o,
+                  int out_f32, void* pools, int32_t* status, int splits) {
+  constexpr int DV = DK;
+  constexpr int VE = 16 / (int)sizeof(IO);
+  extern __shared__ __align__(16) uint8_t smem[];
+  pdl_begin();
+
+  const int Gh = G.Hv / G.Hk;
+  const int kh = blockIdx.x / splits, split = blockIdx.x % splits;
+  const int BVI = DV < kSpecBV ? DV : kSpecBV;     // columns per item
+  const int nCB = DV / BVI;
+  const int n_items = Gh * nCB;
+  const int per = (n_items + splits - 1) / splits;
+  const int it0 = split * per, it1 = min(n_items, it0 + per);
+  const int h0 = kh * Gh;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r8 = lane & 7, cg = lane >> 3;
+  const bool b2 = (r8 & 4) != 0, b1 = (r8 & 2) != 0;
+  const int colw = 16 * warp + 4 * cg;
+  const int cown = 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0);
+  const bool active = colw < BVI;
+  const bool reporter = (blockIdx.x == 0 && tid == 0);
+
+  const Req q = load_req(B, blockIdx.y);
+  if (q.err) {
+    if (reporter) report(status, q.err);
+    return;
+  }
+
+  const SpecSmem L = spec_smem(SPEC_SLOTS, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), 0);
+  IO* raw = reinterpret_cast<IO*>(smem + L.raw);
+  float* abs_ = reinterpret_cast<float*>(smem + L.ab);
+  float* kx = reinterpret_cast<float*>(smem + L.kx);
+  float* qx = reinterpret_cast<float*>(smem + L.qx);
+  RunCoef* coef = reinterpret_cast<RunCoef*>(smem + L.coef);
+  uint8_t* stage = smem + L.stage;
+  const int RW = L.RW, DKP = L.DKP;
+  const int g_lo = it0 / nCB, g_hi = (it1 > it0) ? (it1 - 1) / nCB + 1 : g_lo;  // own heads
+  const int ng = g_hi - g_lo;
+  const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK, v_off = 2 * G.Hk * DK + h0 * DV;
+  const int n_c = q.len;
+  auto chan = [&](int c) {
+    return (c < DK) ? q_off + c : (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
+  };
+  const int pieces = (2 * DK + Gh * DV) / VE;
+
+  // ---- 1. the candidates' rows start copying, then the source slot is checked
+  if (q.len <= G.Kc) {
+    for (int idx = tid; idx < n_c * pieces; idx += kSpecThreads) {
+      const int t = idx / pieces, c = (idx % pieces) * VE;
+      cp_async16(raw + (size_t)t * RW + c, rows_in + (size_t)(q.start + t) * G.C + chan(c));
+    }
+  }
+  cp_async_commit();
+  const int src = B.n_accepted ? B.n_accepted[q.r] : -1;
+  int err = 0;
+  if (src < 0 || src >= G.Kc) err = GDN_DEV_BAD_ACCEPTED;
+  else if (q.len > G.Kc) err = GDN_DEV_TOO_MANY_CANDIDATES;
+  if (err) {
+    if (reporter) report(status, err);
+    cp_async_wait_all();   // nothing lands after the CTA is gone
+    return;
+  }
+  char* pg = reinterpret_cast<char*>(pools) + (size_t)q.page * SG.pool_bytes;
+  ST* Sbase = reinterpret_cast<ST*>(pg + (size_t)src * SG.slot_bytes + SG.state_off);
+  auto item_col0 = [&](int it) -> ST* {
+    const int hh = h0 + it / nCB, cb = it % nCB;
+    return Sbase + ((size_t)hh * DV + (size_t)cb * BVI + colw) * DK;
+  };
+  if (active && it0 < it1) spec_stage_async<DK, ST>(stage, item_col0(it0), r8, tid);
+  else cp_async_commit();   // keep "all but the newest group" meaning the rows
+
+  // ---- 2. gate inputs and constants of own heads
+  float* hc = reinterpret_cast<float*>(smem + L.hc);
+  for (int idx = tid; idx < n_c * ng; idx += kSpecThreads) {
+    const int t = idx / ng, g = g_lo + idx % ng, hh = h0 + g;
+    const size_t rn = (size_t)q.start + t;
+    abs_[t * 2 * Gh + g] = to_f(a_in[rn * G.Hv + hh]);
+    abs_[t * 2 * Gh + Gh + g] = to_f(b_in[rn * G.Hv + hh]);
+  }
+  for (int g = g_lo + tid; g < g_hi; g += kSpecThreads) {
+    hc[2 * g] = P.A_log[h0 + g];
+    hc[2 * g + 1] = P.dt_bias[h0 + g];
+  }
+  cp_async_wait_all_but_one();   // the rows (not the state) have landed
+  __syncthreads();
+
+  // ---- 3. fp32 copies of the k and q rows, then the coefficients, with the
+  // one-page step's code
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(kx, DKP, raw + DK, RW, n_c);
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(qx, DKP, raw, RW, n_c);
+  __syncthreads();
+  spec_candidate_coefs<DK, kSpecThreads>(P, Gh, g_lo, ng, n_c, kx, qx, DKP, abs_, hc,
+                                         *reinterpret_cast<RunDots*>(smem + L.dots),
+                                         reinterpret_cast<float*>(smem + L.gates), coef);
+
+  // ---- 4. items: the candidates from the source slot's state, then the
+  // state after every candidate to its slot, each rebuilt from the staged
+  // starting state
+  if (active && n_c > 0) {
+    const IO* vraw = raw + 2 * DK;
+    float* dsc = reinterpret_cast<float*>(smem + L.scr) + warp * kSpecScr;
+    float* usc = dsc + 2 * kSpecK * 16;
+    const int jw = 4 * cg + cown;
+    const bool writer = (r8 & 1) == 0;
+    const int jc = lane & 15, th = lane >> 4;
+    for (int it = it0; it < it1; ++it) {
+      const int g = it / nCB, cb = it % nCB, hh = h0 + g;
+      ST* col0 = item_col0(it);
+      if (it > it0) spec_stage_async<DK, ST>(stage, col0, r8, tid);
+      spec_stage_wait();
+      SpecS<DK> S;
+      spec_unstage<DK, ST>(S, stage, tid);
+      const RunCoef& C = coef[g];
+      spec_candidate_dots<DK, ST>(S, kx, qx, DKP, n_c, r8, b2, b1, dsc, jw, writer, [] {});
+      __syncwarp();
+      const int col = cb * BVI + 16 * warp + jc;
+      spec_candidate_columns<IO>(C, dsc, jc, th, n_c, vraw + g * DV + col, RW, P.scale, o,
+                                 out_f32, (size_t)q.start * G.Hv * DV + (size_t)hh * DV + col,
+                                 (size_t)G.Hv * DV, [&](int t, float u) { usc[t * 16 + jc] = u; });
+      __syncwarp();
+      const size_t off = (size_t)(col0 - Sbase);
+      for (int t = 0; t < n_c; ++t) {
+        SpecS<DK> T;
+        spec_unstage<DK, ST>(T, stage, tid);
+        spec_advance<DK, ST>(T, C, t, kx, DKP, usc + 4 * cg, 16, r8);
+        ST* dst = reinterpret_cast<ST*>(pg + (size_t)t * SG.slot_bytes + SG.state_off) + off;
+        spec_store<DK, ST>(dst, T, r8);
+      }
+      __syncwarp();   // dsc / usc are written again only after this
+    }
+  }
+  spec_stage_wait();   // no copy outlives the CTA's shared memory
+}
+
+// Dynamic shared memory the spec kernels may ask for (their attribute is
+// raised to it once per device).
 constexpr int kSpecSmemMax = 200 * 1024;
+
+// Items per CTA of the item kernel: two (one CTA per value head at Dv = 128)
+// measured faster than one, whose setup (flag, record, coefficients) was
+// exposed as often as its item.
+#ifndef GDN_SPEC_ITEMS_PER_CTA
+#define GDN_SPEC_ITEMS_PER_CTA 2
+#endif
+
+// CTAs per value head of the item kernel.
+__host__ inline int spec_item_nsplit(int DV) {
+  const int bvi = DV < kSpecBV ? DV : kSpecBV;
+  const int ncb = DV / bvi;
+  const int ipc = GDN_SPEC_ITEMS_PER_CTA;
+  return (ipc >= 1 && ipc <= ncb && ncb % ipc == 0) ? ncb / ipc : ncb;
+}
+
+// The most shared memory any of the three kernels needs for a shape.
+__host__ inline uint32_t spec_smem_most(int DK, int Gh, int io_bytes, int st_bytes) {
+  const uint32_t a =
+      spec_smem(SPEC_VERIFY, DK, DK, Gh, io_bytes, st_bytes, DK / spec_item_nsplit(DK)).total;
+  const uint32_t b = spec_smem(SPEC_FUSED, DK, DK, Gh, io_bytes, st_bytes, 0).total;
+  const uint32_t c = spec_smem(SPEC_SLOTS, DK, DK, Gh, io_bytes, st_bytes, 0).total;
+  return a > b ? (a > c ? a : c) : (b > c ? b : c);
+}
 
 template <int DK>
 cudaError_t launch_spec_dk(int mode, const Geom& G, const Batch& B, const Params& P,
@@ -939,30 +1176,48 @@ cudaError_t launch_spec_dk(int mode, const Geom& G, const Batch& B, const Params
                            void* o, void* pages, int32_t* status, int splits,
                            cudaStream_t stream) {
   const int Gh = G.Hv / G.Hk;
-  const SpecSmem L = spec_smem(DK, DK, Gh, io_bf16 ? 2 : 4, state_bf16 ? 2 : 4);
-  if ((int)L.total > kSpecSmemMax) return cudaErrorInvalidConfiguration;
-  dim3 grid(G.Hk * splits, B.R);
-  dim3 block(kSpecThreads);
-#define GDN_SPEC_LAUNCH(IO, ST, MODE)                                                           \
+  const int iob = io_bf16 ? 2 : 4, stb = state_bf16 ? 2 : 4;
+  if ((int)spec_smem_most(DK, Gh, iob, stb) > kSpecSmemMax) return cudaErrorInvalidConfiguration;
+  const dim3 block(kSpecThreads);
+  const int nsplit = spec_item_nsplit(DK);
+  const SpecSmem Lc = spec_smem(SPEC_FUSED, DK, DK, Gh, iob, stb, 0);
+  const SpecSmem Li = spec_smem(SPEC_VERIFY, DK, DK, Gh, iob, stb, DK / nsplit);
+  const SpecSmem Ls = spec_smem(SPEC_SLOTS, DK, DK, Gh, iob, stb, 0);
+#define GDN_SPEC_ONE_PAGE(IO, ST, FUSED)                                                        \
   do {                                                                                          \
-    cudaError_t e = ensure_smem_limit<spec_kernel<IO, ST, DK, MODE>>(kSpecSmemMax);             \
+    cudaError_t e = ensure_smem_limit<spec_coef_kernel<IO, ST, DK, FUSED>>(kSpecSmemMax);       \
+    if (e == cudaSuccess) e = ensure_smem_limit<spec_item_kernel<IO, ST, DK>>(kSpecSmemMax);    \
     if (e != cudaSuccess) return e;                                                             \
-    return launch_pdl(spec_kernel<IO, ST, DK, MODE>, grid, block, L.total, stream, G, B, P, SG, \
-                      static_cast<const IO*>(rows), static_cast<const IO*>(conv_w),             \
-                      static_cast<const IO*>(a), static_cast<const IO*>(b), o, out_f32, pages,  \
-                      status, splits);                                                          \
+      e = launch_pdl(spec_coef_kernel<IO, ST, DK, FUSED>, dim3(G.Hk, B.R), block, Lc.total,       \
+                   stream, G, B, P, static_cast<const IO*>(rows),                               \
+                   static_cast<const IO*>(conv_w), static_cast<const IO*>(a),                   \
+                   static_cast<const IO*>(b), pages, status);                                   \
+    if (e != cudaSuccess) return e;                                                             \
+    return launch_pdl(spec_item_kernel<IO, ST, DK>, dim3(G.Hv * nsplit, B.R), block, Li.total,  \
+                      stream, G, B, P, FUSED ? nullptr : static_cast<const IO*>(rows), o,       \
+                      out_f32, pages, status, nsplit);                                          \
+  } while (0)
+#define GDN_SPEC_SLOTS(IO, ST)                                                                 \
+  do {                                                                                         \
+    cudaError_t e = ensure_smem_limit<spec_slots_kernel<IO, ST, DK>>(kSpecSmemMax);            \
+    if (e != cudaSuccess) return e;                                                            \
+    return launch_pdl(spec_slots_kernel<IO, ST, DK>, dim3(G.Hk * splits, B.R), block,          \
+                      Ls.total, stream, G, B, P, SG, static_cast<const IO*>(rows),             \
+                      static_cast<const IO*>(a), static_cast<const IO*>(b), o, out_f32, pages, \
+                      status, splits);                                                         \
   } while (0)
 #define GDN_SPEC_MODES(IO, ST)                                          \
-  if (mode == SPEC_VERIFY) GDN_SPEC_LAUNCH(IO, ST, SPEC_VERIFY);        \
-  else if (mode == SPEC_FUSED) GDN_SPEC_LAUNCH(IO, ST, SPEC_FUSED);     \
-  else GDN_SPEC_LAUNCH(IO, ST, SPEC_SLOTS);
+  if (mode == SPEC_VERIFY) GDN_SPEC_ONE_PAGE(IO, ST, false);            \
+  else if (mode == SPEC_FUSED) GDN_SPEC_ONE_PAGE(IO, ST, true);         \
+  else GDN_SPEC_SLOTS(IO, ST);
   if (io_bf16) {
     if (state_bf16) { GDN_SPEC_MODES(bf16, bf16) } else { GDN_SPEC_MODES(bf16, float) }
   } else {
     if (state_bf16) { GDN_SPEC_MODES(float, bf16) } else { GDN_SPEC_MODES(float, float) }
   }
 #undef GDN_SPEC_MODES
-#undef GDN_SPEC_LAUNCH
+#undef GDN_SPEC_SLOTS
+#undef GDN_SPEC_ONE_PAGE
 }
 
 }  // namespace gdn

@@ -56,8 +56,9 @@ def test_page_layout_full_shapes(lib):
     assert L.state_bytes == 32 * 128 * 128 * 4            # 2 MiB fp32 state
     assert L.window_bytes == (3 + 8) * 8192 * 2
     rec_row = (8192 + 64)                                  # already 16-byte aligned in bf16
-    # both slots' rows, then per slot and value head 144 fp32 run coefficients
-    assert L.record_bytes == 2 * 8 * rec_row * 2 + 2 * 32 * 144 * 4
+    # both slots' rows, per slot and value head 216 fp32 run coefficients, and
+    # per value head and candidate the fp32 u of every value column
+    assert L.record_bytes == 2 * 8 * rec_row * 2 + 2 * 32 * 216 * 4 + 32 * 8 * 128 * 4
     for off in (L.state_offset, L.window_offset, L.record_offset, L.flag_offset, L.page_bytes):
         assert off % 256 == 0
     assert L.window_offset >= L.state_offset + L.state_bytes
@@ -73,7 +74,7 @@ def test_record_rows_padded_to_16_bytes(lib):
     # Hv = 1, Hk = 1, Dk = 32: C = 96, + 2 = 98 floats -> padded to 100
     d = gdn.make_dims(1, 1, 32, 32, 4, 8, gdn.GDN_F32, gdn.GDN_F32, gdn.GDN_F32)
     L = gdn.gdn_page_layout(d)
-    assert L.record_bytes == 2 * 8 * 100 * 4 + 2 * 1 * 144 * 4
+    assert L.record_bytes == 2 * 8 * 100 * 4 + 2 * 1 * 216 * 4 + 1 * 8 * 32 * 4
 
 
 def test_slot_layout(lib):
