@@ -315,33 +315,33 @@ __device__ __forceinline__ void spec_advance(SpecS<DK>& S, const RunCoef& C, int
   for (int m = 0; m < 4; ++m)
 #pragma unroll
     for (int p = 0; p < M::P; ++p) S.s[m][p] = __fmul2_rn(g2, S.s[m][p]);
+  // a loop over the run's rows only (a fully unrolled loop to kSpecK would
+  // issue the rows past a as predicated-off instructions)
+#pragma unroll 1
+  for (int s = 0; s <= a; ++s) {
+    const float c = C.rk[a][s];
+    const float4 u4 = *reinterpret_cast<const float4*>(us + s * ustride);
+    const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+    float2 w2[4];
 #pragma unroll
-  for (int s = 0; s < kSpecK; ++s) {
-    if (s <= a) {
-      const float c = C.rk[a][s];
-      const float4 u4 = *reinterpret_cast<const float4*>(us + s * ustride);
-      const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
-      float2 w2[4];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float w = __fmul_rn(c, uu[m]);
-        w2[m] = make_float2(w, w);
-      }
-      const float* xr = kx + s * kstride;
-#pragma unroll
-      for (int i = 0; i < M::NI; ++i)
-#pragma unroll
-        for (int h = 0; h < M::VEC / 4; ++h) {
-          const int p = (i * M::VEC + 4 * h) / 2;
-          const float4 v = *reinterpret_cast<const float4*>(xr + M::xoff(r8, i, h));
-          const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            S.s[m][p] = __ffma2_rn(lo, w2[m], S.s[m][p]);
-            S.s[m][p + 1] = __ffma2_rn(hi, w2[m], S.s[m][p + 1]);
-          }
-        }
+    for (int m = 0; m < 4; ++m) {
+      const float w = __fmul_rn(c, uu[m]);
+      w2[m] = make_float2(w, w);
     }
+    const float* xr = kx + s * kstride;
+#pragma unroll
+    for (int i = 0; i < M::NI; ++i)
+#pragma unroll
+      for (int h = 0; h < M::VEC / 4; ++h) {
+        const int p = (i * M::VEC + 4 * h) / 2;
+        const float4 v = *reinterpret_cast<const float4*>(xr + M::xoff(r8, i, h));
+        const float2 lo = make_float2(v.x, v.y), hi = make_float2(v.z, v.w);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          S.s[m][p] = __ffma2_rn(lo, w2[m], S.s[m][p]);
+          S.s[m][p + 1] = __ffma2_rn(hi, w2[m], S.s[m][p + 1]);
+        }
+      }
   }
 }
 
