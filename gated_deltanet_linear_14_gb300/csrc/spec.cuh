@@ -140,6 +140,8 @@ struct RunDots {
   float kkc[kSpecK][kSpecK];   // [t][s]
   float kqc[kSpecK][kSpecK];   // k_s.q_t at [t][s]
   float qqc[kSpecK];
+  float ik[kSpecK];            // 1 / |k_t| = rsqrt(k_t.k_t + eps)
+  float iq[kSpecK];            // 1 / |q_t|
 };
 
 __host__ __device__ inline uint32_t spec_al16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -429,14 +431,18 @@ __device__ void spec_candidate_coefs(const Params& P, int Gh, int g_lo, int ng, 
       if (k < Bc) {
         int s, t;
         spec_tri(k, s, t);
-        D.kkc[t][s] = spec_rowdot<DK>(kx + s * DKP, kx + t * DKP);
+        const float kk = spec_rowdot<DK>(kx + s * DKP, kx + t * DKP);
+        D.kkc[t][s] = kk;
+        if (s == t) D.ik[t] = rsqrtf(__fadd_rn(kk, P.eps));
       } else if ((k -= Bc) < Bc) {
         int s, t;
         spec_tri(k, s, t);
         D.kqc[t][s] = spec_rowdot<DK>(kx + s * DKP, qx + t * DKP);
       } else {
         k -= Bc;
-        D.qqc[k] = spec_rowdot<DK>(qx + k * DKP, qx + k * DKP);
+        const float qq = spec_rowdot<DK>(qx + k * DKP, qx + k * DKP);
+        D.qqc[k] = qq;
+        D.iq[k] = rsqrtf(__fadd_rn(qq, P.eps));
       }
     }
     for (int idx = tid; idx < ng * n_c; idx += NT) {
@@ -454,51 +460,37 @@ __device__ void spec_candidate_coefs(const Params& P, int Gh, int g_lo, int ng, 
     }
   }
   __syncthreads();
-  // (a) thread -> (head, column s = -1..7): decay products R[.][s], G, and
-  // the columns of L, B and R/|k|
-  for (int idx = tid; idx < ng * (kSpecK + 1); idx += NT) {
-    const int g = g_lo + idx / (kSpecK + 1);
-    const int s = idx % (kSpecK + 1) - 1;
-    const int n = n_c;
-    if (s >= n) continue;
+  // (a) thread -> (head, task): task t < kSpecK forms G_t (the product
+  // alpha_0 ... alpha_t, left to right), G_t/|k_t| and G_t/|q_t|; the other
+  // tasks take one pair s <= t each: the decay product R[t][s] = alpha_{s+1}
+  // ... alpha_t (left to right) and the entries of L, B and R/|k| at [t][s]
+  constexpr int kTasks = kSpecK + kSpecK * (kSpecK + 1) / 2;
+  for (int idx = tid; idx < ng * kTasks; idx += NT) {
+    const int g = g_lo + idx / kTasks;
+    const int task = idx % kTasks;
     RunCoef& C = coef[g];
     const float* al = gts + (g * 2 + 0) * kSpecK;
     const float* be = gts + (g * 2 + 1) * kSpecK;
-    float ik[kSpecK], iq[kSpecK];
-#pragma unroll
-    for (int t = 0; t < kSpecK; ++t) {
-      ik[t] = (t < n) ? rsqrtf(__fadd_rn(D.kkc[t][t], P.eps)) : 0.0f;
-      iq[t] = (t < n) ? rsqrtf(__fadd_rn(D.qqc[t], P.eps)) : 0.0f;
-    }
-    if (s < 0) {
+    if (task < kSpecK) {
+      const int t = task;
+      if (t >= n_c) continue;
       float r = 1.0f;
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t) {
-        if (t < n) {
-          r = __fmul_rn(r, al[t]);
-          C.gam[t] = r;
-          C.gk[t] = __fmul_rn(r, ik[t]);
-          C.gq[t] = __fmul_rn(r, iq[t]);
-          C.beta[t] = be[t];
-        }
-      }
+      for (int q = 0; q <= t; ++q) r = __fmul_rn(r, al[q]);
+      C.gam[t] = r;
+      C.gk[t] = __fmul_rn(r, D.ik[t]);
+      C.gq[t] = __fmul_rn(r, D.iq[t]);
+      C.beta[t] = be[t];
     } else {
-      float iks = 0.0f;
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t) iks = (t == s) ? ik[t] : iks;
+      int s, t;
+      spec_tri(task - kSpecK, s, t);
+      if (t >= n_c) continue;
       float r = 1.0f;
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t) {
-        if (t >= s && t < n) {
-          if (t > s) r = __fmul_rn(r, al[t]);
-          C.rk[t][s] = __fmul_rn(r, iks);
-          if (t > s) {
-            const float kk = D.kkc[t][s];
-            C.l[t][s] = -__fmul_rn(be[t], __fmul_rn(r, __fmul_rn(__fmul_rn(kk, iks), ik[t])));
-          }
-          C.bco[t][s] = __fmul_rn(r, __fmul_rn(__fmul_rn(D.kqc[t][s], iks), iq[t]));
-        }
-      }
+      for (int q = s + 1; q <= t; ++q) r = __fmul_rn(r, al[q]);
+      const float iks = D.ik[s];
+      C.rk[t][s] = __fmul_rn(r, iks);
+      if (t > s)
+        C.l[t][s] = -__fmul_rn(be[t], __fmul_rn(r, __fmul_rn(__fmul_rn(D.kkc[t][s], iks), D.ik[t])));
+      C.bco[t][s] = __fmul_rn(r, __fmul_rn(__fmul_rn(D.kqc[t][s], iks), D.iq[t]));
     }
   }
   __syncthreads();
