@@ -156,10 +156,14 @@ typedef struct {
  *   record  [2][Kc][R_w] io dtype: two slots of candidate rows, each row
  *           = conv'd q|k|v (C) then a (Hv) then b (Hv), padded to R_w
  *           elements so that every row starts on a 16-byte boundary; then
- *           [2][Hv][144] fp32: per slot and value head, the run coefficients
- *           the verify derived for that slot's rows (G_t/|k_t| [8], G_t [8],
- *           R[t][s]/|k_s| [8][8], M = (I - L)^-1 diag(beta) [8][8]; see
- *           gdn_spec_verify), which the next step's replay uses as stored.
+ *           [2][Hv][216] fp32: per slot and value head, the run coefficients
+ *           the verify derived for that slot's rows (G_t [8] and
+ *           R[t][s]/|k_s| [8][8], which the next step's replay uses as
+ *           stored; then G_t/|k_t| [8], G_t/|q_t| [8], M = (I - L)^-1
+ *           diag(beta) [8][8] and N [8][8]; see gdn_spec_verify); then
+ *           [Hv][Kc][Dv] fp32: the live slot's u_t per value column, which
+ *           the next step's replay applies as stored (and then overwrites
+ *           with its own candidates' u).
  *   flag    uint32: bit 0 live slot, bit 1 step parity, bits 2..7 number of
  *           rows in the live slot, bits 8..31 done counter (0 between calls).
  * A zero-filled page is a valid empty page (zero state, zero window, closed
@@ -240,8 +244,9 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch,
  *   1. P must equal the request's GDN_REQ_PARITY bit (else
  *      GDN_DEV_STALE_STEP, request untouched);
  *   2. if n > 0: replay rows 0..a (a = n_accepted, 0 <= a < n) of record
- *      slot L through the rule into the page state and store it (the new
- *      checkpoint); a and b of those rows come from the record;
+ *      slot L into the page state and store it (the new checkpoint): the
+ *      rank-(a+1) update with the rows' G, R/|k| and u as the previous step
+ *      stored them;
  *   3. run this step's row_len candidates (qkv rows, a, b) from the
  *      checkpoint, writing o for each; no per-candidate state is kept;
  *   4. write the candidates' a/b into record slot 1-L (gdn_conv wrote their
@@ -256,24 +261,29 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch,
  *   u_t = beta_t (v_t - G_t S^T k^_t - sum_{s<t} R[t][s] (k^_s.k^_t) u_s),
  *   o_t = scale (G_t S^T q^_t + sum_{s<=t} R[t][s] (k^_s.q^_t) u_s),
  *   checkpoint S_a = G_a S + sum_{s<=a} R[a][s] k^_s u_s^T,
- * which equals the token-by-token rule in exact arithmetic. Returns
- * GDN_ERR_UNSUPPORTED when a q/k head's group of value heads is too wide for
- * the kernel's shared memory (about (Hv/Hk) Dv > 4000 at bf16 rows). */
+ * which equals the token-by-token rule in exact arithmetic. Two launches on
+ * `stream`: the candidates' coefficients per (request, q/k head), written to
+ * record slot 1-L, then the items per (request, value head), which also
+ * store the candidates' u for the next step. Returns GDN_ERR_UNSUPPORTED
+ * when a q/k head's group of value heads is too wide for the kernels'
+ * shared memory (about (Hv/Hk) Dv > 4000 at bf16 rows). */
 gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch,
                            const gdn_params* params, const void* qkv,
                            const void* a, const void* b, void* o, void* pages,
                            int32_t* status, gdn_stream_t stream);
 
 /* Fused speculative step: gdn_conv (io-dtype output) followed by
- * gdn_spec_verify for the SPEC requests of the batch, in one launch, with the
- * same results bit for bit (outputs, states, conv windows, record slots and
- * flag words; the conv'd rows are written only into the record, as the next
- * step's replay needs them). Plain requests are skipped. This is the one
- * launch per layer step that the r9700-stack v0.2.3 notes (section 1) credit
- * for the short-step speed-up, applied to the verify of v0.2.4 ("What it
- * does"): per (request, q/k head) one CTA convolves the group's q, k and v
- * channels for this step's candidates, rolls the window by the accepted
- * count, replays, checkpoints and runs the candidates.
+ * gdn_spec_verify for the SPEC requests of the batch, without a separate
+ * conv launch, with the same results bit for bit (outputs, states, conv
+ * windows, record slots and flag words; the conv'd rows are written only
+ * into the record, as the next step's replay needs them). Plain requests
+ * are skipped. This is the fewer-launches-per-layer-step design that the
+ * r9700-stack v0.2.3 notes (section 1) credit for the short-step speed-up,
+ * applied to the verify of v0.2.4 ("What it does"): per (request, q/k head)
+ * the coefficient kernel's CTA convolves the group's q, k and v channels for
+ * this step's candidates and rolls the window by the accepted count; the
+ * item kernel then replays, checkpoints and runs the candidates. Two
+ * launches, against three for gdn_conv + gdn_spec_verify.
  *   x       device [num_rows][C] io dtype (raw conv inputs, candidate rows)
  *   conv_w  device [C][W];  a, b, o, pages, status as gdn_spec_verify.
  * Returns GDN_ERR_UNSUPPORTED where gdn_spec_verify does. */
