@@ -347,20 +347,20 @@ __device__ __forceinline__ void spec_advance(SpecS<DK>& S, const RunCoef& C, int
   }
 }
 
-// Plain dot product of two fp32 rows in shared memory, in a fixed order.
+// Plain dot product of two fp32 rows in shared memory, in a fixed order:
+// four running sums (entries d = 0, 1, 2, 3 mod 4, as two packed pairs), then
+// (x + y) + (z + w).
 template <int DK>
 __device__ __forceinline__ float spec_rowdot(const float* a, const float* b) {
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float2 lo = make_float2(0.f, 0.f), hi = make_float2(0.f, 0.f);
 #pragma unroll 8
   for (int d = 0; d < DK; d += 4) {
     const float4 x = *reinterpret_cast<const float4*>(a + d);
     const float4 y = *reinterpret_cast<const float4*>(b + d);
-    acc.x = __fmaf_rn(x.x, y.x, acc.x);
-    acc.y = __fmaf_rn(x.y, y.y, acc.y);
-    acc.z = __fmaf_rn(x.z, y.z, acc.z);
-    acc.w = __fmaf_rn(x.w, y.w, acc.w);
+    lo = __ffma2_rn(make_float2(x.x, x.y), make_float2(y.x, y.y), lo);
+    hi = __ffma2_rn(make_float2(x.z, x.w), make_float2(y.z, y.w), hi);
   }
-  return __fadd_rn(__fadd_rn(acc.x, acc.y), __fadd_rn(acc.z, acc.w));
+  return __fadd_rn(__fadd_rn(lo.x, lo.y), __fadd_rn(hi.x, hi.y));
 }
 
 // fp32 copies of n rows (io dtype, DK apart from src, q/k entries at column
