@@ -553,6 +553,41 @@ def test_fused_step_bit_identical_to_conv_verify_and_slots_20_steps(state):
         assert int(L3.pool.flag(r).item()) & 0xFC == 0
 
 
+@pytest.mark.parametrize("state", [gdn.GDN_F32, gdn.GDN_BF16])
+def test_fused_and_two_launch_steps_alternate_on_the_same_pages(state):
+    """A step's record (the candidates' rows, run coefficients and u) is what
+    the next step's replay reads, whichever entry wrote it: the same pages
+    driven by gdn_spec_step on even steps and gdn_conv + gdn_spec_verify on
+    odd ones, over 12 steps and a final commit, give outputs bit-identical to
+    the slot layout at every step and checkpoints equal to the accepted
+    slots."""
+    d = synth.spec()
+    R, n, steps = d["R"], d["n"], 12
+    start, ln = d["row_start"], d["row_len"]
+    L1, L2, _ = make_layers(d, R, state)
+    for s in range(steps):
+        x, a, b = step_rows(d, s, R, n)
+        acc = d["accepted"][s]
+        if s % 2 == 0:
+            B1 = L1.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc)
+            o1 = L1.spec_step(B1, x, a, b)
+        else:
+            _, o1 = one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        B2 = L2.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc)
+        _, o2 = L2.spec_slots(B2, x, a, b)
+        L1.ok()
+        L2.ok()
+        assert np.array_equal(bits(o1), bits(o2)), f"outputs differ from the slots at step {s}"
+    acc = d["accepted"][steps]
+    zero = np.zeros(R, np.int32)
+    B = L1.batch(start, zero, flags=spec_flags(steps, R), n_accepted=acc,
+                 num_rows=int(start[-1]) + n)
+    L1.verify(B, x, a, b)   # the commit: replay, checkpoint, close the record
+    L1.ok()
+    for r in range(R):
+        assert np.array_equal(bits(L1.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
+
+
 @pytest.mark.parametrize("io", [synth.BF16, synth.F32])
 @pytest.mark.parametrize("hk,hv,dk", OTHER_SHAPES)
 def test_fused_step_equals_conv_verify_other_shapes_ragged(hk, hv, dk, io):
