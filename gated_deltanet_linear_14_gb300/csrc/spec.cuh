@@ -45,14 +45,14 @@
 //   Gram products and gates once, derives the run coefficients of every
 //   value head of the group, and stores them in the record slot the
 //   candidates go to.
-// - spec_item_kernel, one CTA per (request, value head, block of 64 value
-//   columns): copies its part of the state while it reads the flag word and
-//   the replay's inputs, then (after the coefficient kernel, which it follows
-//   as a programmatic dependent launch) the candidates' rows and
-//   coefficients; replays and stores the checkpoint; runs the candidates and
-//   stores their outputs and u. The last CTA of a request publishes the new
-//   flag word. Small CTAs of one item each keep the SMs evenly loaded to the
-//   end of the launch.
+// - spec_item_kernel, one CTA per (request, value head) with the head's
+//   items of 64 value columns (two at Dv = 128): copies the first item's
+//   state while it reads the flag word and the replay's inputs, then (after
+//   the coefficient kernel, which it follows as a programmatic dependent
+//   launch) the candidates' rows and coefficients; per item replays and
+//   stores the checkpoint, runs the candidates and stores their outputs and
+//   u, with the next item's state copied meanwhile. The last CTA of a
+//   request publishes the new flag word.
 // - spec_slots_kernel, one CTA per (request, q/k head, split): the slot
 //   layout. It forms the coefficients with the coefficient kernel's code,
 //   then per item runs the candidates from the source slot and rebuilds and
@@ -782,8 +782,8 @@ spec_coef_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in,
 // them from the record slot they went to (the fused step). nsplit CTAs per
 // value head, each with Dv / (BVI nsplit) items of BVI columns.
 //
-// 3 CTAs per SM (at most 168 registers): the items are bound by latency,
-// not by a pipe, and a fourth CTA would spill.
+// 3 CTAs per SM (150 registers at fp32 state, 70 KB of shared memory; at bf16
+// state a fourth CTA, at 128 registers with small spills, ran no faster).
 template <class IO, class ST, int DK>
 __global__ void __launch_bounds__(kSpecThreads, 3)
 spec_item_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in, void* o, int out_f32,
