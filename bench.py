@@ -628,7 +628,7 @@ def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
     torch.cuda.synchronize()
     evs = [_events(torch, 3) for _ in range(K)]
     el = time_steps(lambda i: launch(W + i, evs[i]), K, torch)
-    # the same steps with the conv fused into the coefficient kernel; the
+    # the same steps as one fused launch each (gdn_spec_step); the
     # pools' parities carry on from the two-launch steps
     for i in range(W):
         launch_fused(W + K + i)
@@ -662,7 +662,7 @@ def bench_spec(device, peaks, state, K=40, W=8, pools=POOLS):
             "verify_tflops_fp32": flops / (ver_ms / 1e3) / 1e12,
             "verify_frac_of_fp32": flops / (ver_ms / 1e3) / 1e12 / FP32_PEAK_TFLOPS,
             "fp32_peak_tflops": FP32_PEAK_TFLOPS,
-            "fused_step": {"entry": "gdn_spec_step (conv in the coefficient kernel: two launches)",
+            "fused_step": {"entry": "gdn_spec_step (conv, coefficients and items in one launch)",
                            "ms_per_step": el_f_plain / K * 1e3,
                            "ms_per_step_event_bracketed": fused_ms,
                            "tokens_per_s": T * K / el_f_plain, "bytes": state_bytes + fused_other,

@@ -55,7 +55,7 @@ cudaError_t launch_handover(const Geom& G, const SlotGeom& SG, int dir, int n, c
 // Speculative decode in closed form (spec.cuh). mode: 0 = one-page verify
 // (rows = conv'd qkv), 1 = the same with the conv fused in (rows = raw x),
 // 2 = slot-per-candidate layout (rows = conv'd qkv, pages = slot pools).
-// Modes 0 and 1 launch two kernels (run coefficients, then items); mode 2
+// Mode 0 launches two kernels (run coefficients, then items); modes 1 and 2
 // one. splits: CTAs per (request, q/k head) of mode 2.
 cudaError_t launch_spec_d32(int mode, const Geom&, const Batch&, const Params&, const SlotGeom&,
                             int, int, int, const void*, const void*, const void*, const void*,

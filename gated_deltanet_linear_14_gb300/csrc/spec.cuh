@@ -40,11 +40,9 @@
 //
 // Kernels.
 // - spec_coef_kernel, one CTA per (request, q/k head kh): stages the
-//   candidates' q and k rows of kh (the fused step convolves the group's
-//   q, k and v channels first and writes them into the record), forms their
-//   Gram products and gates once, derives the run coefficients of every
-//   value head of the group, and stores them in the record slot the
-//   candidates go to.
+//   candidates' q and k rows of kh, forms their Gram products and gates
+//   once, derives the run coefficients of every value head of the group,
+//   and stores them in the record slot the candidates go to.
 // - spec_item_kernel, one CTA per (request, value head) with the head's
 //   items of 64 value columns (two at Dv = 128): copies the first item's
 //   state while it reads the flag word and the replay's inputs, then (after
@@ -53,6 +51,11 @@
 //   stores the checkpoint, runs the candidates and stores their outputs and
 //   u, with the next item's state copied meanwhile. The last CTA of a
 //   request publishes the new flag word.
+// - spec_step_kernel (gdn_spec_step), one CTA per (request, q/k head kh):
+//   the conv of the group's q, k and v channels for this step's candidates
+//   (rows into the record, the window rolled), the coefficient kernel's work
+//   for the group, then the item kernel's work for every item of the group,
+//   in one launch.
 // - spec_slots_kernel, one CTA per (request, q/k head, split): the slot
 //   layout. It forms the coefficients with the coefficient kernel's code,
 //   then per item runs the candidates from the source slot and rebuilds and
@@ -74,6 +77,8 @@
 namespace gdn {
 
 enum SpecMode { SPEC_VERIFY = 0, SPEC_FUSED = 1, SPEC_SLOTS = 2 };
+// Shared memory layouts of spec_smem (see there).
+enum SpecLayout { LAYOUT_ITEMS = 0, LAYOUT_COEF = 1, LAYOUT_SLOTS = 2 };
 
 constexpr int kSpecThreads = 128;
 constexpr int kSpecBV = 64;   // value columns per item
@@ -167,15 +172,15 @@ struct SpecSmem {
   int RW, DKP, VW;
 };
 
-// kind: SPEC_VERIFY = the item kernel (VW value columns per CTA),
-// SPEC_FUSED = the coefficient kernel, SPEC_SLOTS = the slot kernel.
+// kind: LAYOUT_ITEMS = the item kernel (VW value columns per CTA),
+// LAYOUT_COEF = the coefficient kernel, LAYOUT_SLOTS = the slot kernel.
 __host__ __device__ inline SpecSmem spec_smem(int kind, int DK, int DV, int Gh, int io_bytes,
                                                int st_bytes, int VW) {
   SpecSmem L;
   L.DKP = DK + 4;
-  L.RW = (kind == SPEC_SLOTS) ? (2 * DK + Gh * DV + 7) / 8 * 8 : 2 * DK;
+  L.RW = (kind == LAYOUT_SLOTS) ? (2 * DK + Gh * DV + 7) / 8 * 8 : 2 * DK;
   L.VW = VW;
-  const bool items = (kind == SPEC_VERIFY), coef = (kind == SPEC_FUSED);
+  const bool items = (kind == LAYOUT_ITEMS), coef = (kind == LAYOUT_COEF);
   const uint32_t K = kSpecK;
   uint32_t off = 0;
   auto take = [&](uint32_t& at, uint32_t bytes) {
@@ -305,9 +310,10 @@ __device__ __forceinline__ void spec_dots(const SpecS<DK>& S, const float* const
 // S <- the state after row a of a run that started from S:
 //   G_a S + sum_{s<=a} k_s (R[a][s] / |k_s|) u_s^T,
 // k rows (raw, fp32, stored by spec_xpos) at kx + s * kstride; us[s * ustride
-// + m] holds u_s of the lane's column m.
-template <int DK, class ST>
-__device__ __forceinline__ void spec_advance(SpecS<DK>& S, const RunCoef& C, int a,
+// + m] holds u_s of the lane's column m; C is any block with gam and rk laid
+// out as in RunCoef (a RunCoef, or the replay's RepCoef).
+template <int DK, class ST, class CT>
+__device__ __forceinline__ void spec_advance(SpecS<DK>& S, const CT& C, int a,
                                              const float* kx, int kstride, const float* us,
                                              int ustride, int r8) {
   using M = SpecMap<DK, ST>;
@@ -614,11 +620,11 @@ __device__ __forceinline__ void spec_candidate_columns(const RunCoef& C, const f
 
 // ---------------------------------------------------------------------------
 // One-page step, part 1: the candidates' run coefficients per value head.
-template <class IO, class ST, int DK, bool FUSED>
+template <class IO, class ST, int DK>
 __global__ void __launch_bounds__(kSpecThreads)
 spec_coef_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in,
-                 const IO* __restrict__ conv_w, const IO* __restrict__ a_in,
-                 const IO* __restrict__ b_in, void* pages, int32_t* status) {
+                 const IO* __restrict__ a_in, const IO* __restrict__ b_in, void* pages,
+                 int32_t* status) {
   constexpr int NT = kSpecThreads;
   constexpr int DV = DK;
   constexpr int VE = 16 / (int)sizeof(IO);
@@ -636,22 +642,20 @@ spec_coef_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in,
   }
   if (!q.spec) return;
 
-  const SpecSmem L = spec_smem(SPEC_FUSED, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), 0);
+  const SpecSmem L = spec_smem(LAYOUT_COEF, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), 0);
   IO* raw = reinterpret_cast<IO*>(smem + L.raw);
   float* abs_ = reinterpret_cast<float*>(smem + L.ab);
   float* hc = reinterpret_cast<float*>(smem + L.hc);
   const int RW = L.RW;
-  const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK, v_off = 2 * G.Hk * DK + h0 * DV;
+  const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK;
   const int n_c = (q.len <= G.Kc) ? q.len : 0;   // (more is an error, found below)
-  // channel of group element c (q | k | v of the group's heads)
-  auto chan = [&](int c) {
-    return (c < DK) ? q_off + c : (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
-  };
+  // channel of row element c (q | k of the group)
+  auto chan = [&](int c) { return (c < DK) ? q_off + c : k_off + (c - DK); };
 
   // ---- the candidates' q and k rows start copying; the flag word, the gate
   // inputs and the heads' constants are loaded together (none depends on
   // another), then the page is checked
-  if constexpr (!FUSED) {
+  {
     constexpr int pieces = 2 * DK / VE;
     for (int idx = tid; idx < n_c * pieces; idx += NT) {
       const int t = idx / pieces, c = (idx % pieces) * VE;
@@ -679,72 +683,8 @@ spec_coef_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in,
     cp_async_wait_all();   // nothing lands after the CTA is gone
     return;
   }
-  const int n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
   IO* rec_out = reinterpret_cast<IO*>(pg + G.record_off) + (size_t)(1 - ss.live) * G.Kc * G.rec_row;
 
-  if constexpr (FUSED) {
-    // the conv of the group's channels for this step's candidates, exactly
-    // as gdn_conv computes it for a spec request: history = window columns
-    // n_r .. n_r+W-2 (the record's accepted rows rolled out), taps oldest
-    // first, own SiLU, rounded to the io dtype; the rows go to the record.
-    // Every load of a channel vector is issued before its arithmetic.
-    const int nvec = (2 * DK + Gh * DV) / 4;
-    IO* win = reinterpret_cast<IO*>(pg + G.window_off);
-    for (int vi = tid; vi < nvec; vi += NT) {
-      const int c4 = 4 * vi;
-      const int ch = chan(c4);
-      float wt[4][4], hcol[3][4], h0c[3][4], xr[kSpecK][4];
-      {
-        float tmp[16];
-        load_f<IO, 16>(conv_w + (size_t)ch * 4, tmp);
-#pragma unroll
-        for (int v = 0; v < 4; ++v)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) wt[j][v] = tmp[v * 4 + j];
-      }
-#pragma unroll
-      for (int j = 0; j < 3; ++j) load_f<IO, 4>(win + (size_t)(n_r + j) * G.C + ch, hcol[j]);
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t)
-        if (t < n_c) load_f<IO, 4>(rows_in + (size_t)(q.start + t) * G.C + ch, xr[t]);
-#pragma unroll
-      for (int j = 0; j < 3; ++j)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) h0c[j][v] = hcol[j][v];
-#pragma unroll
-      for (int t = 0; t < kSpecK; ++t) {
-        if (t < n_c) {
-          float yv[4];
-#pragma unroll
-          for (int v = 0; v < 4; v += 2) {
-            float2 acc = P.conv_bias ? make_float2(P.conv_bias[ch + v], P.conv_bias[ch + v + 1])
-                                     : make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int j = 0; j < 3; ++j)
-              acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]),
-                               make_float2(hcol[j][v], hcol[j][v + 1]), acc);
-            acc = __ffma2_rn(make_float2(wt[3][v], wt[3][v + 1]),
-                             make_float2(xr[t][v], xr[t][v + 1]), acc);
-            const float2 y2 = own_silu2(acc);
-            yv[v] = y2.x;
-            yv[v + 1] = y2.y;
-          }
-          if (c4 < 2 * DK) store_f<IO, 4>(raw + (size_t)t * RW + c4, yv);
-          store_f<IO, 4>(rec_out + (size_t)t * G.rec_row + ch, yv);
-          store_f<IO, 4>(win + (size_t)(3 + t) * G.C + ch, xr[t]);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            hcol[0][v] = hcol[1][v];
-            hcol[1][v] = hcol[2][v];
-            hcol[2][v] = xr[t][v];
-          }
-        }
-      }
-      // window columns 0..2: the history this step started from
-#pragma unroll
-      for (int j = 0; j < 3; ++j) store_f<IO, 4>(win + (size_t)j * G.C + ch, h0c[j]);
-    }
-  }
   // the candidates' gate inputs go next to their conv'd rows in the record slot
   for (int idx = tid; idx < n_c * Gh; idx += NT) {
     const int t = idx / Gh, g = idx % Gh, h = h0 + g;
@@ -778,9 +718,8 @@ spec_coef_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in,
 
 // ---------------------------------------------------------------------------
 // One-page step, part 2: replay, checkpoint and the candidates, per item.
-// rows_in: the candidates' conv'd rows (gdn_spec_verify), or null to read
-// them from the record slot they went to (the fused step). nsplit CTAs per
-// value head, each with Dv / (BVI nsplit) items of BVI columns.
+// rows_in: the candidates' conv'd rows. nsplit CTAs per value head, each
+// with Dv / (BVI nsplit) items of BVI columns.
 //
 // 3 CTAs per SM (150 registers at fp32 state, 70 KB of shared memory; at bf16
 // state a fourth CTA, at 128 registers with small spills, ran no faster).
@@ -818,7 +757,7 @@ spec_item_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in, void
   }
   if (!q.spec) return;
 
-  const SpecSmem L = spec_smem(SPEC_VERIFY, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), per * BVI);
+  const SpecSmem L = spec_smem(LAYOUT_ITEMS, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), per * BVI);
   IO* rawk = reinterpret_cast<IO*>(smem + L.rawk);
   IO* rawq = reinterpret_cast<IO*>(smem + L.rawq);
   IO* rawv = reinterpret_cast<IO*>(smem + L.rawv);
@@ -879,7 +818,7 @@ spec_item_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in, void
     return row + ((p < RP) ? q_off + p * VE : (p < 2 * RP) ? k_off + (p - RP) * VE
                                                            : v_off + (p - 2 * RP) * VE);
   };
-  if (rows_in && n_c <= G.Kc) {
+  if (n_c <= G.Kc) {
     for (int idx = tid; idx < n_c * per_row; idx += kSpecThreads) {
       const int t = idx / per_row, p = idx % per_row;
       cp_async16(cand_dst(t, p), cand_src(rows_in + (size_t)(q.start + t) * G.C, p));
@@ -895,17 +834,9 @@ spec_item_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in, void
   }
   const int n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
   const int live = ss.live, parity = ss.parity;
-  const IO* cslot = rec + (size_t)(1 - live) * G.Kc * G.rec_row;
-  // what the coefficient kernel wrote: the candidates' coefficients and, in
-  // the fused step, their rows
+  // what the coefficient kernel wrote: the candidates' coefficients
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (!rows_in) {
-    for (int idx = tid; idx < n_c * per_row; idx += kSpecThreads) {
-      const int t = idx / per_row, p = idx % per_row;
-      cp_async16(cand_dst(t, p), cand_src(cslot + (size_t)t * G.rec_row, p));
-    }
-  }
   if (n_c > 0) {
     const float* rc = reinterpret_cast<const float*>(pg + G.rcoef_off) +
                       ((size_t)(1 - live) * G.Hv + h) * kRunCoefFloats;
@@ -992,6 +923,326 @@ spec_item_kernel(Geom G, Batch B, Params P, const IO* __restrict__ rows_in, void
 }
 
 // ---------------------------------------------------------------------------
+// The fused step (gdn_spec_step) in one launch: one CTA per (request, q/k
+// head kh) convolves the group's channels for this step's candidates (as the
+// coefficient kernel's fused form does), forms the group's run coefficients,
+// and then runs every item of the group as the item kernel does, with the
+// same helpers: the same bits as gdn_conv + gdn_spec_verify, pages included.
+
+// The replay's G and R/|k| of one value head, as the record keeps them
+// (floats 16 .. 87 of its coefficient block).
+struct RepCoef {
+  float gam[kSpecK];
+  float rk[kSpecK][kSpecK];
+};
+static_assert(sizeof(RepCoef) == 72 * 4, "record floats 16..87");
+
+struct StepSmem {
+  uint32_t raw;     // [Kc][RW] io dtype: the candidates' conv'd q | k | v of the group
+  uint32_t ab;      // [Kc][2 Gh] float: a then b per head
+  uint32_t hc;      // [Gh][2] float: A_log, dt_bias per head
+  uint32_t kx;      // [2 Kc][DKP] float: replayed k rows 0.., candidates' k rows kSpecK..
+  uint32_t qx;      // [Kc][DKP] float: candidates' q rows
+  uint32_t dots;    // RunDots
+  uint32_t gates;   // [Gh][2][Kc] float
+  uint32_t coef;    // [Gh] RunCoef: the candidates'
+  uint32_t rep;     // [Gh] RepCoef: the replay's
+  uint32_t rawr;    // [Kc][DK] io dtype: the replayed k rows
+  uint32_t ur;      // [Gh][Kc][DV] float: the replayed rows' u
+  uint32_t stage;   // [NC][threads] 16-byte chunks of one item's state
+  uint32_t scr;     // per warp [2 Kc][16] dot products
+  uint32_t total;
+  int RW, DKP;
+};
+
+__host__ __device__ inline StepSmem step_smem(int DK, int DV, int Gh, int io_bytes, int st_bytes) {
+  StepSmem L;
+  const uint32_t K = kSpecK;
+  L.DKP = DK + 4;
+  L.RW = (2 * DK + Gh * DV + 7) / 8 * 8;
+  uint32_t off = 0;
+  auto take = [&](uint32_t& at, uint32_t bytes) {
+    at = off;
+    off = spec_al16(off + bytes);
+  };
+  take(L.raw, K * L.RW * io_bytes);
+  take(L.ab, K * 2 * Gh * 4);
+  take(L.hc, Gh * 2 * 4);
+  take(L.kx, 2 * K * L.DKP * 4);
+  take(L.qx, K * L.DKP * 4);
+  take(L.dots, (uint32_t)sizeof(RunDots));
+  take(L.gates, Gh * 2 * K * 4);
+  take(L.coef, (uint32_t)Gh * (uint32_t)sizeof(RunCoef));
+  take(L.rep, (uint32_t)Gh * (uint32_t)sizeof(RepCoef));
+  take(L.rawr, K * DK * io_bytes);
+  take(L.ur, Gh * K * DV * 4);
+  take(L.stage, (uint32_t)(DK / 2 * st_bytes * kSpecThreads));
+  take(L.scr, (uint32_t)((kSpecThreads / 32) * 2 * kSpecK * 16 * 4));
+  L.total = off;
+  return L;
+}
+
+// 3 CTAs per SM at Dk = Dv = 128 with Gh = 2 (about 72 KB of shared memory).
+template <class IO, class ST, int DK>
+__global__ void __launch_bounds__(kSpecThreads, 3)
+spec_step_kernel(Geom G, Batch B, Params P, const IO* __restrict__ x_in,
+                 const IO* __restrict__ conv_w, const IO* __restrict__ a_in,
+                 const IO* __restrict__ b_in, void* o, int out_f32, void* pages,
+                 int32_t* status) {
+  using M = SpecMap<DK, ST>;
+  constexpr int DV = DK;
+  constexpr int VE = 16 / (int)sizeof(IO);
+  constexpr int BVI = DV < kSpecBV ? DV : kSpecBV;   // columns per item
+  constexpr int nCB = DV / BVI;
+  extern __shared__ __align__(16) uint8_t smem[];
+  pdl_begin();
+
+  const int Gh = G.Hv / G.Hk;
+  const int kh = blockIdx.x, h0 = kh * Gh;
+  const int n_items = Gh * nCB;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r8 = lane & 7, cg = lane >> 3;
+  const bool b2 = (r8 & 4) != 0, b1 = (r8 & 2) != 0;
+  const int colw = 16 * warp + 4 * cg;             // the lane's first column in an item
+  const int cown = 2 * (b2 ? 1 : 0) + (b1 ? 1 : 0);
+  const bool active = colw < BVI;
+  const bool reporter = (blockIdx.x == 0 && tid == 0);
+  const Req q = load_req(B, blockIdx.y);
+  if (q.err) {
+    if (reporter) report(status, q.err);
+    return;
+  }
+  if (!q.spec) return;
+
+  const StepSmem L = step_smem(DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST));
+  IO* raw = reinterpret_cast<IO*>(smem + L.raw);
+  float* abs_ = reinterpret_cast<float*>(smem + L.ab);
+  float* hc = reinterpret_cast<float*>(smem + L.hc);
+  float* kx = reinterpret_cast<float*>(smem + L.kx);
+  float* qx = reinterpret_cast<float*>(smem + L.qx);
+  RunCoef* coef = reinterpret_cast<RunCoef*>(smem + L.coef);
+  RepCoef* rep = reinterpret_cast<RepCoef*>(smem + L.rep);
+  IO* rawr = reinterpret_cast<IO*>(smem + L.rawr);
+  float* ur = reinterpret_cast<float*>(smem + L.ur);
+  uint8_t* stage = smem + L.stage;
+  const int RW = L.RW, DKP = L.DKP;
+  const int q_off = kh * DK, k_off = G.Hk * DK + kh * DK, v_off = 2 * G.Hk * DK + h0 * DV;
+  // channel of group element c (q | k | v of the group's heads)
+  auto chan = [&](int c) {
+    return (c < DK) ? q_off + c : (c < 2 * DK) ? k_off + (c - DK) : v_off + (c - 2 * DK);
+  };
+
+  char* pg = page_ptr(G, pages, q.page);
+  ST* Sbase = reinterpret_cast<ST*>(pg + G.state_off);
+  auto item_col0 = [&](int it) -> ST* {
+    return Sbase + ((size_t)(h0 + it / nCB) * DV + (size_t)(it % nCB) * BVI + colw) * DK;
+  };
+  // ---- 1. the first item's state starts copying; the flag word and the
+  // heads' constants are loaded, then the page is checked
+  if (active) spec_stage_async<DK, ST>(stage, item_col0(0), r8, tid);
+  uint32_t* flagp = reinterpret_cast<uint32_t*>(pg + G.flag_off);
+  const uint32_t flag = *reinterpret_cast<volatile uint32_t*>(flagp);
+  for (int g = tid; g < Gh; g += kSpecThreads) {
+    hc[2 * g] = P.A_log[h0 + g];
+    hc[2 * g + 1] = P.dt_bias[h0 + g];
+  }
+  SpecState ss = spec_state(G, B, q, flag);
+  if (q.fresh) ss.err = GDN_DEV_BAD_FLAG;
+  if (ss.err) {
+    if (reporter) report(status, ss.err);
+    cp_async_wait_all();   // nothing lands after the CTA is gone
+    return;
+  }
+  const int n_r = (ss.width > 0) ? ss.accepted + 1 : 0;
+  const int n_c = q.len;
+  const int live = ss.live, parity = ss.parity;
+  IO* rec = reinterpret_cast<IO*>(pg + G.record_off);
+  const IO* rslot = rec + (size_t)live * G.Kc * G.rec_row;
+  IO* rec_out = rec + (size_t)(1 - live) * G.Kc * G.rec_row;
+
+  // ---- 2. the replay's inputs from the live record slot: its k rows, per
+  // head G and R/|k|, and the u of the accepted rows
+  constexpr int RP = DK / VE;   // 16-byte pieces per k row
+  for (int idx = tid; idx < n_r * RP; idx += kSpecThreads) {
+    const int t = idx / RP, c = (idx % RP) * VE;
+    cp_async16(rawr + (size_t)t * DK + c, rslot + (size_t)t * G.rec_row + k_off + c);
+  }
+  if (n_r > 0) {
+    constexpr int RQ = (int)sizeof(RepCoef) / 16;
+    for (int idx = tid; idx < Gh * RQ; idx += kSpecThreads) {
+      const int g = idx / RQ, k = idx % RQ;
+      const float* rc = reinterpret_cast<const float*>(pg + G.rcoef_off) +
+                        ((size_t)live * G.Hv + h0 + g) * kRunCoefFloats;
+      cp_async16(reinterpret_cast<float*>(&rep[g]) + 4 * k, rc + 16 + 4 * k);
+    }
+    constexpr int UP = DV / 4;
+    const float* us = reinterpret_cast<const float*>(pg + G.ru_off) + (size_t)h0 * G.Kc * DV;
+    for (int idx = tid; idx < Gh * n_r * UP; idx += kSpecThreads) {
+      const int g = idx / (n_r * UP), s = (idx / UP) % n_r, c = (idx % UP) * 4;
+      cp_async16(ur + ((size_t)g * kSpecK + s) * DV + c, us + ((size_t)g * G.Kc + s) * DV + c);
+    }
+  }
+  cp_async_commit();
+
+  // ---- 3. the conv of the group's channels for this step's candidates,
+  // exactly as gdn_conv computes it for a spec request: history = window
+  // columns n_r .. n_r+W-2, taps oldest first, own SiLU, rounded to the io
+  // dtype; the rows go to shared memory and the record slot, the window rolls
+  {
+    const int nvec = (2 * DK + Gh * DV) / 4;
+    IO* win = reinterpret_cast<IO*>(pg + G.window_off);
+    for (int vi = tid; vi < nvec; vi += kSpecThreads) {
+      const int c4 = 4 * vi;
+      const int ch = chan(c4);
+      float wt[4][4], hcol[3][4], h0c[3][4], xr[kSpecK][4];
+      {
+        float tmp[16];
+        load_f<IO, 16>(conv_w + (size_t)ch * 4, tmp);
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) wt[j][v] = tmp[v * 4 + j];
+      }
+#pragma unroll
+      for (int j = 0; j < 3; ++j) load_f<IO, 4>(win + (size_t)(n_r + j) * G.C + ch, hcol[j]);
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t)
+        if (t < n_c) load_f<IO, 4>(x_in + (size_t)(q.start + t) * G.C + ch, xr[t]);
+#pragma unroll
+      for (int j = 0; j < 3; ++j)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) h0c[j][v] = hcol[j][v];
+#pragma unroll
+      for (int t = 0; t < kSpecK; ++t) {
+        if (t < n_c) {
+          float yv[4];
+#pragma unroll
+          for (int v = 0; v < 4; v += 2) {
+            float2 acc = P.conv_bias ? make_float2(P.conv_bias[ch + v], P.conv_bias[ch + v + 1])
+                                     : make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int j = 0; j < 3; ++j)
+              acc = __ffma2_rn(make_float2(wt[j][v], wt[j][v + 1]),
+                               make_float2(hcol[j][v], hcol[j][v + 1]), acc);
+            acc = __ffma2_rn(make_float2(wt[3][v], wt[3][v + 1]),
+                             make_float2(xr[t][v], xr[t][v + 1]), acc);
+            const float2 y2 = own_silu2(acc);
+            yv[v] = y2.x;
+            yv[v + 1] = y2.y;
+          }
+          store_f<IO, 4>(raw + (size_t)t * RW + c4, yv);
+          store_f<IO, 4>(rec_out + (size_t)t * G.rec_row + ch, yv);
+          store_f<IO, 4>(win + (size_t)(3 + t) * G.C + ch, xr[t]);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            hcol[0][v] = hcol[1][v];
+            hcol[1][v] = hcol[2][v];
+            hcol[2][v] = xr[t][v];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 3; ++j) store_f<IO, 4>(win + (size_t)j * G.C + ch, h0c[j]);
+    }
+  }
+  // gate inputs per candidate and head; they also go next to the
+  // candidates' conv'd rows in the record slot
+  for (int idx = tid; idx < n_c * Gh; idx += kSpecThreads) {
+    const int t = idx / Gh, g = idx % Gh, h = h0 + g;
+    const size_t rn = ((size_t)q.start + t) * G.Hv + h;
+    abs_[t * 2 * Gh + g] = to_f(a_in[rn]);
+    abs_[t * 2 * Gh + Gh + g] = to_f(b_in[rn]);
+    IO* rr = rec_out + (size_t)t * G.rec_row;
+    rr[G.C + h] = a_in[rn];
+    rr[G.C + G.Hv + h] = b_in[rn];
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- 4. fp32 rows in the lanes' order (replayed k rows at 0.., the
+  // candidates' k rows at kSpecK.., their q rows), then the candidates'
+  // coefficients, which also go to the record slot they are written to
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(kx, DKP, rawr, DK, n_r);
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(kx + kSpecK * DKP, DKP, raw + DK, RW, n_c);
+  spec_rows_f32<DK, ST, IO, kSpecThreads>(qx, DKP, raw, RW, n_c);
+  __syncthreads();
+  if (n_c > 0) {
+    spec_candidate_coefs<DK, kSpecThreads>(P, Gh, 0, Gh, n_c, kx + kSpecK * DKP, qx, DKP, abs_,
+                                           hc, *reinterpret_cast<RunDots*>(smem + L.dots),
+                                           reinterpret_cast<float*>(smem + L.gates), coef);
+    float* rc = reinterpret_cast<float*>(pg + G.rcoef_off) + (size_t)(1 - live) * G.Hv * kRunCoefFloats;
+    for (int idx = tid; idx < Gh * kCoefPieces; idx += kSpecThreads) {
+      const int g = idx / kCoefPieces, k = idx % kCoefPieces;
+      *reinterpret_cast<float4*>(rc + (size_t)(h0 + g) * kRunCoefFloats + 4 * k) =
+          *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(&coef[g]) +
+                                           spec_coef_piece(k));
+    }
+  }
+
+  // ---- 5. items (value head g, column block cb): no block-wide barrier
+  // from here on. The next item's state starts copying once this one's is in
+  // registers.
+  if (active && n_r + n_c > 0) {
+    float* dsc = reinterpret_cast<float*>(smem + L.scr) + warp * 2 * kSpecK * 16;
+    const int jw = 4 * cg + cown;
+    const bool writer = (r8 & 1) == 0;
+    const int jc = lane & 15, th = lane >> 4;
+    for (int it = 0; it < n_items; ++it) {
+      const int g = it / nCB, cb = it % nCB, h = h0 + g;
+      ST* col0 = item_col0(it);
+      spec_stage_wait();
+      SpecS<DK> S;
+      spec_unstage<DK, ST>(S, stage, tid);
+      bool ahead = (it + 1 >= n_items);
+      auto prefetch = [&]() {
+        if (!ahead) {
+          spec_stage_async<DK, ST>(stage, item_col0(it + 1), r8, tid);
+          ahead = true;
+        }
+      };
+      if (n_r > 0) {
+        // the replay: S_a from the stored u of the accepted rows
+        spec_advance<DK, ST>(S, rep[g], n_r - 1, kx, DKP,
+                             ur + (size_t)g * kSpecK * DV + cb * BVI + colw, DV, r8);
+        prefetch();
+        spec_store<DK, ST>(col0, S, r8);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+#pragma unroll
+          for (int p = 0; p < M::P; ++p)
+            S.s[m][p] = make_float2(through<ST>(S.s[m][p].x), through<ST>(S.s[m][p].y));
+      }
+      if (n_c > 0) {
+        spec_candidate_dots<DK, ST>(S, kx + kSpecK * DKP, qx, DKP, n_c, r8, b2, b1, dsc, jw,
+                                    writer, prefetch);
+        __syncwarp();
+        const int col = cb * BVI + 16 * warp + jc;   // the column of jc in the head
+        float* uout = reinterpret_cast<float*>(pg + G.ru_off) + (size_t)h * G.Kc * DV;
+        spec_candidate_columns<IO>(coef[g], dsc, jc, th, n_c, raw + 2 * DK + g * DV + col, RW,
+                                   P.scale, o, out_f32,
+                                   (size_t)q.start * G.Hv * DV + (size_t)h * DV + col,
+                                   (size_t)G.Hv * DV,
+                                   [&](int t, float u) { uout[(size_t)t * DV + col] = u; });
+        __syncwarp();   // dsc is written again only after this
+      }
+      prefetch();
+    }
+  }
+  spec_stage_wait();   // no copy outlives the CTA's shared memory
+
+  // ---- 6. the last CTA of the request publishes the new flag word (every
+  // CTA read the flag before its own increment of the same word)
+  if (tid == 0) {
+    const uint32_t total = (uint32_t)G.Hk;
+    const uint32_t old = atomicAdd(flagp, 256u);
+    if ((old >> 8) == total - 1) {
+      const int nl = (n_c > 0) ? 1 - live : live;
+      atomicExch(flagp, make_flag(nl, 1 - parity, n_c));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Slot-per-candidate layout. 2 CTAs per SM (240 registers): the per-candidate
 // rebuild keeps a second state in registers, and at 3 per SM it spilled 280
 // bytes and ran 294 us per 64-request step, against 244 us at 2.
@@ -1027,7 +1278,7 @@ spec_slots_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__
     return;
   }
 
-  const SpecSmem L = spec_smem(SPEC_SLOTS, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), 0);
+  const SpecSmem L = spec_smem(LAYOUT_SLOTS, DK, DV, Gh, (int)sizeof(IO), (int)sizeof(ST), 0);
   IO* raw = reinterpret_cast<IO*>(smem + L.raw);
   float* abs_ = reinterpret_cast<float*>(smem + L.ab);
   float* kx = reinterpret_cast<float*>(smem + L.kx);
@@ -1152,13 +1403,15 @@ __host__ inline int spec_item_nsplit(int DV) {
   return (ipc >= 1 && ipc <= ncb && ncb % ipc == 0) ? ncb / ipc : ncb;
 }
 
-// The most shared memory any of the three kernels needs for a shape.
+// The most shared memory any of the four kernels needs for a shape.
 __host__ inline uint32_t spec_smem_most(int DK, int Gh, int io_bytes, int st_bytes) {
   const uint32_t a =
-      spec_smem(SPEC_VERIFY, DK, DK, Gh, io_bytes, st_bytes, DK / spec_item_nsplit(DK)).total;
-  const uint32_t b = spec_smem(SPEC_FUSED, DK, DK, Gh, io_bytes, st_bytes, 0).total;
-  const uint32_t c = spec_smem(SPEC_SLOTS, DK, DK, Gh, io_bytes, st_bytes, 0).total;
-  return a > b ? (a > c ? a : c) : (b > c ? b : c);
+      spec_smem(LAYOUT_ITEMS, DK, DK, Gh, io_bytes, st_bytes, DK / spec_item_nsplit(DK)).total;
+  const uint32_t b = spec_smem(LAYOUT_COEF, DK, DK, Gh, io_bytes, st_bytes, 0).total;
+  const uint32_t c = spec_smem(LAYOUT_SLOTS, DK, DK, Gh, io_bytes, st_bytes, 0).total;
+  const uint32_t d = step_smem(DK, DK, Gh, io_bytes, st_bytes).total;
+  const uint32_t ab = a > b ? a : b, cd = c > d ? c : d;
+  return ab > cd ? ab : cd;
 }
 
 template <int DK>
@@ -1172,22 +1425,31 @@ cudaError_t launch_spec_dk(int mode, const Geom& G, const Batch& B, const Params
   if ((int)spec_smem_most(DK, Gh, iob, stb) > kSpecSmemMax) return cudaErrorInvalidConfiguration;
   const dim3 block(kSpecThreads);
   const int nsplit = spec_item_nsplit(DK);
-  const SpecSmem Lc = spec_smem(SPEC_FUSED, DK, DK, Gh, iob, stb, 0);
-  const SpecSmem Li = spec_smem(SPEC_VERIFY, DK, DK, Gh, iob, stb, DK / nsplit);
-  const SpecSmem Ls = spec_smem(SPEC_SLOTS, DK, DK, Gh, iob, stb, 0);
-#define GDN_SPEC_ONE_PAGE(IO, ST, FUSED)                                                        \
-  do {                                                                                          \
-    cudaError_t e = ensure_smem_limit<spec_coef_kernel<IO, ST, DK, FUSED>>(kSpecSmemMax);       \
-    if (e == cudaSuccess) e = ensure_smem_limit<spec_item_kernel<IO, ST, DK>>(kSpecSmemMax);    \
-    if (e != cudaSuccess) return e;                                                             \
-      e = launch_pdl(spec_coef_kernel<IO, ST, DK, FUSED>, dim3(G.Hk, B.R), block, Lc.total,       \
-                   stream, G, B, P, static_cast<const IO*>(rows),                               \
-                   static_cast<const IO*>(conv_w), static_cast<const IO*>(a),                   \
-                   static_cast<const IO*>(b), pages, status);                                   \
-    if (e != cudaSuccess) return e;                                                             \
-    return launch_pdl(spec_item_kernel<IO, ST, DK>, dim3(G.Hv * nsplit, B.R), block, Li.total,  \
-                      stream, G, B, P, FUSED ? nullptr : static_cast<const IO*>(rows), o,       \
-                      out_f32, pages, status, nsplit);                                          \
+  const SpecSmem Lc = spec_smem(LAYOUT_COEF, DK, DK, Gh, iob, stb, 0);
+  const SpecSmem Li = spec_smem(LAYOUT_ITEMS, DK, DK, Gh, iob, stb, DK / nsplit);
+  const SpecSmem Ls = spec_smem(LAYOUT_SLOTS, DK, DK, Gh, iob, stb, 0);
+  const StepSmem Lf = step_smem(DK, DK, Gh, iob, stb);
+#define GDN_SPEC_ONE_PAGE(IO, ST)                                                              \
+  do {                                                                                         \
+    cudaError_t e = ensure_smem_limit<spec_coef_kernel<IO, ST, DK>>(kSpecSmemMax);             \
+    if (e == cudaSuccess) e = ensure_smem_limit<spec_item_kernel<IO, ST, DK>>(kSpecSmemMax);   \
+    if (e != cudaSuccess) return e;                                                            \
+    e = launch_pdl(spec_coef_kernel<IO, ST, DK>, dim3(G.Hk, B.R), block, Lc.total, stream, G,  \
+                   B, P, static_cast<const IO*>(rows), static_cast<const IO*>(a),              \
+                   static_cast<const IO*>(b), pages, status);                                  \
+    if (e != cudaSuccess) return e;                                                            \
+    return launch_pdl(spec_item_kernel<IO, ST, DK>, dim3(G.Hv * nsplit, B.R), block, Li.total, \
+                      stream, G, B, P, static_cast<const IO*>(rows), o, out_f32, pages,        \
+                      status, nsplit);                                                         \
+  } while (0)
+#define GDN_SPEC_STEP(IO, ST)                                                                  \
+  do {                                                                                         \
+    cudaError_t e = ensure_smem_limit<spec_step_kernel<IO, ST, DK>>(kSpecSmemMax);             \
+    if (e != cudaSuccess) return e;                                                            \
+    return launch_pdl(spec_step_kernel<IO, ST, DK>, dim3(G.Hk, B.R), block, Lf.total, stream,  \
+                      G, B, P, static_cast<const IO*>(rows), static_cast<const IO*>(conv_w),   \
+                      static_cast<const IO*>(a), static_cast<const IO*>(b), o, out_f32, pages, \
+                      status);                                                                 \
   } while (0)
 #define GDN_SPEC_SLOTS(IO, ST)                                                                 \
   do {                                                                                         \
@@ -1199,8 +1461,8 @@ cudaError_t launch_spec_dk(int mode, const Geom& G, const Batch& B, const Params
                       status, splits);                                                         \
   } while (0)
 #define GDN_SPEC_MODES(IO, ST)                                          \
-  if (mode == SPEC_VERIFY) GDN_SPEC_ONE_PAGE(IO, ST, false);            \
-  else if (mode == SPEC_FUSED) GDN_SPEC_ONE_PAGE(IO, ST, true);         \
+  if (mode == SPEC_VERIFY) GDN_SPEC_ONE_PAGE(IO, ST);                   \
+  else if (mode == SPEC_FUSED) GDN_SPEC_STEP(IO, ST);                   \
   else GDN_SPEC_SLOTS(IO, ST);
   if (io_bf16) {
     if (state_bf16) { GDN_SPEC_MODES(bf16, bf16) } else { GDN_SPEC_MODES(bf16, float) }
@@ -1209,6 +1471,7 @@ cudaError_t launch_spec_dk(int mode, const Geom& G, const Batch& B, const Params
   }
 #undef GDN_SPEC_MODES
 #undef GDN_SPEC_SLOTS
+#undef GDN_SPEC_STEP
 #undef GDN_SPEC_ONE_PAGE
 }
 

@@ -279,11 +279,12 @@ gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch,
  * into the record, as the next step's replay needs them). Plain requests
  * are skipped. This is the fewer-launches-per-layer-step design that the
  * r9700-stack v0.2.3 notes (section 1) credit for the short-step speed-up,
- * applied to the verify of v0.2.4 ("What it does"): per (request, q/k head)
- * the coefficient kernel's CTA convolves the group's q, k and v channels for
- * this step's candidates and rolls the window by the accepted count; the
- * item kernel then replays, checkpoints and runs the candidates. Two
- * launches, against three for gdn_conv + gdn_spec_verify.
+ * applied to the verify of v0.2.4 ("What it does"): one launch, one CTA
+ * per (request, q/k head), which convolves the group's q, k and v channels
+ * for this step's candidates and rolls the window by the accepted count,
+ * forms the group's run coefficients, then replays, checkpoints and runs the
+ * candidates for every value column of the group. One launch, against three
+ * for gdn_conv + gdn_spec_verify.
  *   x       device [num_rows][C] io dtype (raw conv inputs, candidate rows)
  *   conv_w  device [C][W];  a, b, o, pages, status as gdn_spec_verify.
  * Returns GDN_ERR_UNSUPPORTED where gdn_spec_verify does. */
