@@ -28,6 +28,21 @@ __global__ void wait_check_kernel(uint64_t limit_ns, int32_t* status) {
   }
 }
 
+// SMs of the current device (looked up once per device; declared in kernels.h).
+int device_sms() {
+  static int sms[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev < 0 || dev >= 64) return 152;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    sms[dev] = n;
+  }
+  return sms[dev];
+}
+
 }  // namespace gdn
 
 namespace {
@@ -169,21 +184,6 @@ cudaError_t rule(const Geom& G, const Batch& B, const Params& P, const gdn_dims*
     case 64: return launch_rule_d64(G, B, P, io, st, of, qkv, a, b, o, pages, status, s);
     default: return launch_rule_d128(G, B, P, io, st, of, qkv, a, b, o, pages, status, s);
   }
-}
-
-// SMs of the current device (looked up once per device).
-int device_sms() {
-  static int sms[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev < 0 || dev >= 64) return 152;
-  if (sms[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 152;
-    sms[dev] = n;
-  }
-  return sms[dev];
 }
 
 // CTAs per (request, q/k head) for the slot-layout kernel: one unless the

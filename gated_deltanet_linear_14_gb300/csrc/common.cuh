@@ -269,13 +269,14 @@ __device__ __forceinline__ float through(float x) { return to_f(from_f<T>(x)); }
 // within 0.90 ulp of e^{-a} where that is a normal float and within 0.86 of
 // the subnormal spacing below.
 //
-// 1/d: the quadratic of least maximum relative error to 1/d on [1, 2],
-// 70/33 - (16/11) d + (32/99) d^2 (relative error at most 1/99,
-// equioscillating at 1, 5/4, 7/4 and 2), one Newton-Raphson step r <- r + r (1 - d r)
-// (error about 1e-4), then the quotient t r corrected once,
-// q <- q + r (t - d q) (about 1e-8 before rounding). Over every float z with
-// |z| <= 104 the SiLU is within 3.32 ulp where |z| <= 87 and the result is a
-// normal float of at least 2^-124, and within 2^-142 absolutely elsewhere.
+// t/d: the hardware's approximate reciprocal r of d (rcp.approx), the
+// quotient t r, then one correction with the exact residual,
+// q <- q + r (t - d q) (Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34, 1990). For every
+// float t in [0, 1] and d = fl(1 + t) this gives the correctly rounded t/d:
+// silu_negquot below was run over all of them on sm_103a against the IEEE
+// division, with no difference. The SiLU is therefore c - a fl(t/d), with
+// t the exp above.
 //
 // c = max(z, 0) is taken on the bit pattern (a signed-integer maximum with
 // 0): it is z for z > 0 and +0 for every z with the sign bit set. A NaN z
@@ -287,7 +288,6 @@ constexpr float kLn2Lo = 0x1.0bfbe8p-15f;       // float(ln 2 - kLn2Hi)
 constexpr float kRound = 12582912.0f;           // 1.5 2^23
 constexpr float kC2 = 0x1.fffffcp-2f, kC3 = 0x1.55548cp-3f, kC4 = 0x1.555858p-5f,
                 kC5 = 0x1.123e26p-7f, kC6 = 0x1.6ace9ap-10f;   // c0 = c1 = 1
-constexpr float kS0 = (float)(70.0 / 33.0), kS1 = (float)(16.0 / 11.0), kS2 = (float)(32.0 / 99.0);
 }  // namespace silu_consts
 
 __device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
@@ -297,6 +297,20 @@ __device__ __forceinline__ float silu_arg(float z) {
   float r;
   asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(z)), "f"(104.0f));
   return r;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// -t/d, correctly rounded, from nt = -t and nd = -d = -fl(1 + t), t in [0, 1]
+// (the method above), on two values.
+__device__ __forceinline__ float2 silu_negquot(float2 nt, float2 nd) {
+  const float2 rc = make_float2(rcp_approx(-nd.x), rcp_approx(-nd.y));   // ~ 1/d
+  const float2 nq = __fmul2_rn(nt, rc);
+  return __ffma2_rn(rc, __ffma2_rn(nd, nq, nt), nq);
 }
 
 // SiLU on two values (the method above), the floating-point steps in packed
@@ -322,10 +336,7 @@ __device__ __forceinline__ float2 own_silu2(float2 z) {
                                   __uint_as_float((__float_as_uint(m.y) << 23) + (447u << 23)));
   const float2 nt = __fmul2_rn(p, negs);           // -t
   const float2 nd = __fadd2_rn(nt, splat2(-1.0f));  // -d
-  float2 rc = __ffma2_rn(__ffma2_rn(splat2(kS2), nd, splat2(kS1)), nd, splat2(kS0));
-  rc = __ffma2_rn(rc, __ffma2_rn(nd, rc, splat2(1.0f)), rc);
-  float2 nq = __fmul2_rn(nt, rc);                  // -t/d
-  nq = __ffma2_rn(rc, __ffma2_rn(nd, nq, nt), nq);
+  const float2 nq = silu_negquot(nt, nd);           // -t/d
   const float2 c = make_float2(__int_as_float(max(__float_as_int(z.x), 0)),
                                __int_as_float(max(__float_as_int(z.y), 0)));
   return __ffma2_rn(a, nq, c);

@@ -19,15 +19,14 @@
 //     window and another writes the final one).
 //   * accumulation is fp32 in a fixed order: bias (or 0), then taps
 //     j = 0..W-1 oldest first, each a fused multiply-add; SiLU uses the
-//     library's own exp and Newton reciprocal (additions, multiplications
-//     and fused multiply-adds only). The CPU fp32 conv reproduces this bit
-//     for bit.
+//     library's own exp and the correctly rounded quotient t / (1 + t)
+//     (common.cuh). The CPU fp32 conv reproduces this bit for bit.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace gdn {
 
-// The exact SiLU (own exp and reciprocal per element) keeps the conv's
+// The exact SiLU (own exp and quotient per element) keeps the conv's
 // floating-point pipe busier than its HBM traffic, so the kernel is built to
 // keep that pipe fed: channel pairs in packed f32x2 form, 8-byte vectors, 4
 // CTAs of 256 threads per SM (32 warps), and the input rows staged into
@@ -35,8 +34,13 @@ namespace gdn {
 // arithmetic of a batch never waits for its loads.
 constexpr int kConvThreads = 256;
 constexpr int kConvVecBytes = 8;
-constexpr int kConvRows = 32;   // rows per tile (>= W-1)
-constexpr int kConvBatch = 4;   // rows per ring stage
+// Rows per tile (TILE): 64 where the launch has rows for several waves of
+// CTAs (fewer tiles: less per-tile setup, fewer halo rows, and rows in ring
+// stages of 8), else 32 (more CTAs for batches of short requests, stages of
+// 4: the 24 KB ring of the short tile leaves the shared memory the kernels
+// after it in a mixed step want).
+constexpr int kConvRowsLong = 64;
+constexpr int kConvRowsShort = 32;
 constexpr int kConvStages = 3;  // ring stages: the batch in use and two in flight
 
 __device__ __forceinline__ void conv_cp8(void* smem, const void* gmem) {
@@ -49,13 +53,14 @@ __device__ __forceinline__ void conv_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(kConvStages - 1) : "memory");
 }
 
-template <class IO, class YT, int W, bool SLOTS>
+template <class IO, class YT, int W, bool SLOTS, int TILE>
 __global__ void __launch_bounds__(kConvThreads, 4)
 conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
             const IO* __restrict__ w, YT* __restrict__ y, void* pages, int32_t* status) {
   pdl_begin();
   constexpr int V = kConvVecBytes / (int)sizeof(IO);  // channels per thread
   constexpr int H = W - 1;
+  constexpr int kConvBatch = TILE / 8;   // rows per ring stage
   const bool reporter = (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0);
 
   Batch Bi = B;
@@ -65,7 +70,7 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
     if (reporter) report(status, q.err);
     return;
   }
-  const int t0 = blockIdx.y * kConvRows;
+  const int t0 = blockIdx.y * TILE;
   if (t0 > 0 && t0 >= q.len) return;
 
   char* pg = nullptr;
@@ -116,7 +121,7 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
   // the only ordering needed (no block-wide barrier). Every copy is issued
   // here, after the last early return, and waited for before the end.
   __shared__ uint2 ring[kConvStages][kConvBatch][kConvThreads];
-  const int t_end = min(q.len, t0 + kConvRows);
+  const int t_end = min(q.len, t0 + TILE);
   const int nb = (t_end - t0 + kConvBatch - 1) / kConvBatch;
   const IO* xr = x + (size_t)q.start * G.C + c0;  // row t at xr + t C
   auto issue = [&](int b) {
@@ -205,7 +210,10 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
 
   // one row: taps, SiLU, stores, then the window slides by one. rec is a
   // constant at each call, so the full-batch path below has no branch
-  // between its rows and their arithmetic interleaves.
+  // between its rows and their arithmetic interleaves. The output row moves
+  // by one row stride per row (an address add, not a 64-bit product).
+  YT* yrow = y + ((size_t)q.start + t0) * G.C + c0;
+  const size_t ystride = (size_t)G.C;
   auto row = [&](const uint2 raw, int t, bool rec) {
     float xv[V];
     {
@@ -227,7 +235,8 @@ conv_kernel(Geom G, Batch B, Params P, SlotGeom SG, const IO* __restrict__ x,
       yv[v] = y2.x;
       yv[v + 1] = y2.y;
     }
-    store_f<YT, V>(y + (size_t)(q.start + t) * G.C + c0, yv);
+    store_f<YT, V>(yrow, yv);
+    yrow += ystride;
 #pragma unroll
     for (int j = 0; j < H - 1; ++j)
 #pragma unroll
@@ -269,10 +278,15 @@ static cudaError_t launch_conv_t(const Geom& G, const Batch& B, const Params& P,
                                  int32_t* status, cudaStream_t stream) {
   constexpr int V = kConvVecBytes / (int)sizeof(IO);
   const int ctiles = (G.C + kConvThreads * V - 1) / (kConvThreads * V);
-  const int rtiles = B.max_rows > 0 ? (B.max_rows + kConvRows - 1) / kConvRows : 1;
-  return launch_pdl(conv_kernel<IO, YT, 4, SLOTS>, dim3(ctiles, rtiles, B.R), dim3(kConvThreads),
-                    0, stream, G, B, P, SG, static_cast<const IO*>(x), static_cast<const IO*>(w),
-                    static_cast<YT*>(y), pages, status);
+  // several waves (4 CTAs per SM) of long tiles, counting the rows present
+  const long long long_ctas = (long long)ctiles * (B.num_rows / kConvRowsLong);
+  const int tile = (long_ctas >= 4LL * 4 * device_sms()) ? kConvRowsLong : kConvRowsShort;
+  const int rtiles = B.max_rows > 0 ? (B.max_rows + tile - 1) / tile : 1;
+  auto kern = (tile == kConvRowsLong) ? conv_kernel<IO, YT, 4, SLOTS, kConvRowsLong>
+                                      : conv_kernel<IO, YT, 4, SLOTS, kConvRowsShort>;
+  return launch_pdl(kern, dim3(ctiles, rtiles, B.R), dim3(kConvThreads), 0, stream, G, B, P, SG,
+                    static_cast<const IO*>(x), static_cast<const IO*>(w), static_cast<YT*>(y),
+                    pages, status);
 }
 
 cudaError_t launch_conv(const Geom& G, const Batch& B, const Params& P, int io_bf16, int y_f32,

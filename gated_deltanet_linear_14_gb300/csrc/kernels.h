@@ -7,6 +7,9 @@
 
 namespace gdn {
 
+// SMs of the current device.
+int device_sms();
+
 cudaError_t launch_conv(const Geom& G, const Batch& B, const Params& P, int io_bf16, int y_f32,
                         const void* x, const void* w, void* y, void* pages, int32_t* status,
                         cudaStream_t stream);

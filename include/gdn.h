@@ -184,9 +184,10 @@ gdn_status gdn_page_layout(const gdn_dims* dims, gdn_page_layout_t* out);
  *   y_t[c] = SiLU( bias[c] + sum_{j=0..W-1} w[c][j] * x_{t-(W-1)+j}[c] )
  * accumulated in fp32 in exactly that order (fused multiply-adds, taps
  * oldest first), SiLU(z) = z / (1 + e^{-z}) = z sigmoid(z), evaluated from
- * the library's own exp of -|z| and a Newton reciprocal of 1 + e^{-|z|}
- * (IEEE additions, multiplications and fused multiply-adds only, so a plain
- * CPU program reproduces every output bit; within 4 ulp of the exact value).
+ * the library's own exp of -|z| and the correctly rounded quotient
+ * e^{-|z|} / (1 + e^{-|z|}) (each step one rounding of a plain operation, so
+ * a plain CPU program reproduces every output bit; within 4 ulp of the
+ * exact value).
  * History before a request's first row comes from its page window (zero for
  * FRESH requests). Per request:
  *   plain:  window columns 0..W-2 <- last W-1 columns of [history; rows];

@@ -32,9 +32,9 @@
 // oracle_conv_f64 is IEEE double. oracle_conv_f32 is the one deliberate
 // exception: it is the fp32-accumulate conv that the GPU conv must match bit
 // for bit, so it fixes the accumulation order (bias, then taps j = 0..W-1,
-// each a fused multiply-add) and evaluates SiLU with its own exp and
-// reciprocal (below), from IEEE additions, multiplications and fused
-// multiply-adds only.
+// each a fused multiply-add) and evaluates SiLU with its own exp and an
+// IEEE quotient (below), from IEEE additions, multiplications, divisions and
+// fused multiply-adds only.
 // Build with -ffp-contract=off so the compiler adds no contractions.
 
 #include <cfloat>
@@ -187,15 +187,16 @@ void parallel_for(long n, int threads, F f) {
 
 // ------------------------------------------------------- fp32 conv mirror
 //
-// SiLU(z) = z sigmoid(z), evaluated as the GPU conv does, step for step.
-// With a = |z| (raised to at most 104), t = e^{-a} in [0, 1] and
-// d = 1 + t in [1, 2], sigmoid(z) = t/d for z < 0 and 1 - t/d for z >= 0, so
-// with c = max(z, 0):
+// SiLU(z) = z sigmoid(z) in fp32, with the exp of the GPU conv. With
+// a = |z| (lowered to at most 104), t = e^{-a} in [0, 1] and d = 1 + t in
+// [1, 2], sigmoid(z) = t/d for z < 0 and 1 - t/d for z >= 0, so with
+// c = max(z, 0):
 //     SiLU(z) = c - a (t/d)
-// for both signs: exp is only taken of a non-positive argument and the
-// reciprocal only of a number in [1, 2]. The chain below carries -t, -d and
-// -t/d (negation is exact, so each value has the roundings of its positive
-// form).
+// for both signs: exp is only taken of a non-positive argument. Each step is
+// one fp32 rounding: t (the exp below), d = fl(1 + t), the quotient
+// fl(t / d) as an IEEE division, and c - a q as one fused multiply-add. The
+// chain carries -t, -d and -t/d (negation is exact, so each value has the
+// roundings of its positive form).
 //
 // e^{-a}: Cody & Waite argument reduction (W. J. Cody and W. Waite,
 // "Software Manual for the Elementary Functions", 1980): -a = n ln2 + r with
@@ -209,15 +210,9 @@ void parallel_for(long n, int threads, F f) {
 // coefficients), by Horner's rule with fused multiply-adds, the coefficients
 // scaled by 2^-64 (exactly); then one product with -2^(n+64), which rounds
 // once, and only where e^{-a} is subnormal. At a = 104 the result is 0.
-//
-// 1/d: the quadratic of least maximum relative error to 1/d on [1, 2]
-// (70/33 - (16/11) d + (32/99) d^2, error at most 1/99), one Newton-Raphson
-// step r <- r + r (1 - d r) (error about 1e-4), then the quotient q = t r
-// corrected once, q <- q + r (t - d q) (about 1e-8 before rounding).
 struct OwnExpConsts {
   float log2e, ln2_hi, ln2_lo;
   float c[7];     // e^r ~ sum c_k r^k, |r| <= ln2/2
-  float seed[3];  // 70/33, 16/11, 32/99
   OwnExpConsts() {
     const double ln2 = std::log(2.0);
     log2e = (float)(1.0 / ln2);
@@ -233,9 +228,6 @@ struct OwnExpConsts {
     const float fit[7] = {1.0f, 1.0f, 0x1.fffffcp-2f, 0x1.55548cp-3f, 0x1.555858p-5f,
                           0x1.123e26p-7f, 0x1.6ace9ap-10f};
     for (int k = 0; k < 7; ++k) c[k] = fit[k];
-    seed[0] = (float)(70.0 / 33.0);
-    seed[1] = (float)(16.0 / 11.0);
-    seed[2] = (float)(32.0 / 99.0);
   }
 };
 const OwnExpConsts kExp;
@@ -269,11 +261,7 @@ float silu_own_f32(float z) {
   const float a = silu_arg(z);
   const float negt = std::isnan(a) ? a : own_negexp_f32(a);
   const float N = negt - 1.0f;                         // -d
-  // 70/33 - (16/11) d + (32/99) d^2 in -d
-  float r = std::fma(std::fma(kExp.seed[2], N, kExp.seed[1]), N, kExp.seed[0]);
-  r = std::fma(r, std::fma(N, r, 1.0f), r);            // one Newton-Raphson step
-  float nq = negt * r;                                 // -t/d
-  nq = std::fma(r, std::fma(N, nq, negt), nq);         // corrected once
+  const float nq = negt / -N;                          // -t/d, correctly rounded
   int32_t zb;
   std::memcpy(&zb, &z, 4);
   const int32_t cb = zb > 0 ? zb : 0;                  // max(z, 0) on the bit pattern

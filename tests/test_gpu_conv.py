@@ -96,7 +96,7 @@ def test_conv_long_request_with_initial_window_is_race_free():
 
 
 def test_own_exp_silu_against_cuda_expf():
-    """SiLU of the conv (own exp, Newton reciprocal) on the GPU: bit-identical
+    """SiLU of the conv (own exp, correctly rounded quotient) on the GPU: bit-identical
     to the CPU mirror, within 4 ulp of the exact value (2^-140 absolutely
     where e^x is subnormal), and within 8 ulp of torch's CUDA-exp SiLU on the
     same values (the two methods' bounds added: neither need match the

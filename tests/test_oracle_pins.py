@@ -254,7 +254,7 @@ def test_own_exp_within_one_ulp():
 
 
 def test_own_silu_within_four_ulp():
-    """SiLU(x) = x sigmoid(x) through the own exp and the Newton reciprocal:
+    """SiLU(x) = x sigmoid(x) through the own exp and an IEEE quotient:
     within 4 ulp of the exact value where it is a normal float of at least
     2^-124, and within 2^-140 absolutely below that (x < -87, where e^x is
     subnormal)."""
