@@ -588,18 +588,20 @@ def test_fused_and_two_launch_steps_alternate_on_the_same_pages(state):
         assert np.array_equal(bits(L1.pool.state(r)), bits(L2.slots.state(r, int(acc[r]))))
 
 
-@pytest.mark.parametrize("io", [synth.BF16, synth.F32])
+@pytest.mark.parametrize("io,state", [(synth.BF16, gdn.GDN_F32), (synth.F32, gdn.GDN_F32),
+                                      (synth.BF16, gdn.GDN_BF16)])
 @pytest.mark.parametrize("hk,hv,dk", OTHER_SHAPES)
-def test_fused_step_equals_conv_verify_other_shapes_ragged(hk, hv, dk, io):
+def test_fused_step_equals_conv_verify_other_shapes_ragged(hk, hv, dk, io, state):
     """1..8 candidates per request and step in a shuffled row order, the
-    three head dimensions and groups of 1, 3 and 8 value heads: gdn_spec_step
-    leaves every page and output exactly as gdn_conv + gdn_spec_verify."""
+    three head dimensions and groups of 1, 3 and 8 value heads, fp32 and
+    bf16 state: gdn_spec_step leaves every page and output exactly as
+    gdn_conv + gdn_spec_verify."""
     sh = synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk)
     rng = np.random.default_rng(300 + hk * 1000 + hv * 10 + dk)
     R, Kc, steps = 6, 8, 5
     d = synth.spec(seed=int(rng.integers(1 << 30)), R=R, steps=1, n=1, sh=sh, io=io)
-    L1, _, _ = make_layers(d, R, gdn.GDN_F32, slots=False, Kc=Kc)
-    L3, _, _ = make_layers(d, R, gdn.GDN_F32, slots=False, Kc=Kc)
+    L1, _, _ = make_layers(d, R, state, slots=False, Kc=Kc)
+    L3, _, _ = make_layers(d, R, state, slots=False, Kc=Kc)
     prev_len = np.zeros(R, np.int64)
     for s in range(steps):
         ln = rng.integers(1, Kc + 1, size=R)
