@@ -26,7 +26,10 @@ def _layer(d, R):
     return L
 
 
-def test_spec_steps_graph_replay_equals_eager():
+@pytest.mark.parametrize("fused", [False, True])
+def test_spec_steps_graph_replay_equals_eager(fused):
+    """Captured conv + verify (or the fused gdn_spec_step) replayed over 6
+    steps: outputs and pages equal the eager conv + verify steps."""
     R, n, steps = 8, 8, 6
     d = synth.spec(R=R, steps=steps)
     start, ln = d["row_start"], d["row_len"]
@@ -56,6 +59,9 @@ def test_spec_steps_graph_replay_equals_eager():
     B = gdn.make_batch(R, T, n, R, rs, rl, pg, flags_t, acc_t)
 
     def step():
+        if fused:
+            gdn.gdn_spec_step(Lg.dims, B, Lg.params, x, Lg.conv_w, a, b, o, Lg.pool.buf, Lg.status)
+            return
         gdn.gdn_conv(Lg.dims, B, Lg.params, x, Lg.conv_w, y, gdn.GDN_BF16, Lg.pool.buf, Lg.status)
         gdn.gdn_spec_verify(Lg.dims, B, Lg.params, y, a, b, o, Lg.pool.buf, Lg.status)
 
