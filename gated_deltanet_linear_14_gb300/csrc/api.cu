@@ -202,11 +202,11 @@ int spec_splits(const gdn_dims* d, int R, int mode) {
   return s;
 }
 
-// The shared memory the spec kernel needs fits (else the shape is not
-// supported: a very wide group of value heads).
-bool spec_fits(const gdn_dims* d) {
+// The shared memory the entry point's spec kernels need fits (else the
+// shape is not supported: a very wide group of value heads).
+bool spec_fits(const gdn_dims* d, int mode) {
   const int Gh = d->num_v_heads / d->num_k_heads;
-  return (int)spec_smem_most(d->head_k_dim, Gh, (int)dsize(d->io_dtype),
+  return (int)spec_smem_need(mode, d->head_k_dim, Gh, (int)dsize(d->io_dtype),
                              (int)dsize(d->state_dtype)) <= kSpecSmemMax;
 }
 
@@ -394,7 +394,7 @@ gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch, const g
   if ((e = check_batch(batch, false)) != GDN_OK) return e;
   if ((e = check_params(params, true)) != GDN_OK) return e;
   if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
-  if (!spec_fits(dims)) return GDN_ERR_UNSUPPORTED;
+  if (!spec_fits(dims, SPEC_VERIFY)) return GDN_ERR_UNSUPPORTED;
   if (batch->num_requests == 0) return GDN_OK;
   if (!status || !pages) return GDN_ERR_INVALID_ARG;
   if (batch->num_rows > 0 && (!qkv || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
@@ -416,7 +416,7 @@ gdn_status gdn_spec_step(const gdn_dims* dims, const gdn_batch* batch, const gdn
   if ((e = check_batch(batch, false)) != GDN_OK) return e;
   if ((e = check_params(params, true)) != GDN_OK) return e;
   if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
-  if (!spec_fits(dims)) return GDN_ERR_UNSUPPORTED;
+  if (!spec_fits(dims, SPEC_FUSED)) return GDN_ERR_UNSUPPORTED;
   if (batch->num_requests == 0) return GDN_OK;
   if (!status || !pages || !conv_w) return GDN_ERR_INVALID_ARG;
   if (batch->num_rows > 0 && (!x || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
@@ -438,7 +438,7 @@ gdn_status gdn_spec_slots(const gdn_dims* dims, const gdn_batch* batch, const gd
   if ((e = check_batch(batch, false)) != GDN_OK) return e;
   if ((e = check_params(params, true)) != GDN_OK) return e;
   if (dims->max_candidates == 0) return GDN_ERR_UNSUPPORTED;
-  if (!spec_fits(dims)) return GDN_ERR_UNSUPPORTED;
+  if (!spec_fits(dims, SPEC_SLOTS)) return GDN_ERR_UNSUPPORTED;
   if (batch->num_requests == 0) return GDN_OK;
   if (!status || !slots || !conv_w) return GDN_ERR_INVALID_ARG;
   if (batch->num_rows > 0 && (!x || !y || !a || !b || !o)) return GDN_ERR_INVALID_ARG;

@@ -1403,15 +1403,16 @@ __host__ inline int spec_item_nsplit(int DV) {
   return (ipc >= 1 && ipc <= ncb && ncb % ipc == 0) ? ncb / ipc : ncb;
 }
 
-// The most shared memory any of the four kernels needs for a shape.
-__host__ inline uint32_t spec_smem_most(int DK, int Gh, int io_bytes, int st_bytes) {
+// The shared memory an entry point's kernels need for a shape: the
+// coefficient and item kernels (SPEC_VERIFY), the one-launch step
+// (SPEC_FUSED) or the slot kernel (SPEC_SLOTS).
+__host__ inline uint32_t spec_smem_need(int mode, int DK, int Gh, int io_bytes, int st_bytes) {
+  if (mode == SPEC_FUSED) return step_smem(DK, DK, Gh, io_bytes, st_bytes).total;
+  if (mode == SPEC_SLOTS) return spec_smem(LAYOUT_SLOTS, DK, DK, Gh, io_bytes, st_bytes, 0).total;
   const uint32_t a =
       spec_smem(LAYOUT_ITEMS, DK, DK, Gh, io_bytes, st_bytes, DK / spec_item_nsplit(DK)).total;
   const uint32_t b = spec_smem(LAYOUT_COEF, DK, DK, Gh, io_bytes, st_bytes, 0).total;
-  const uint32_t c = spec_smem(LAYOUT_SLOTS, DK, DK, Gh, io_bytes, st_bytes, 0).total;
-  const uint32_t d = step_smem(DK, DK, Gh, io_bytes, st_bytes).total;
-  const uint32_t ab = a > b ? a : b, cd = c > d ? c : d;
-  return ab > cd ? ab : cd;
+  return a > b ? a : b;
 }
 
 template <int DK>
@@ -1422,7 +1423,7 @@ cudaError_t launch_spec_dk(int mode, const Geom& G, const Batch& B, const Params
                            cudaStream_t stream) {
   const int Gh = G.Hv / G.Hk;
   const int iob = io_bf16 ? 2 : 4, stb = state_bf16 ? 2 : 4;
-  if ((int)spec_smem_most(DK, Gh, iob, stb) > kSpecSmemMax) return cudaErrorInvalidConfiguration;
+  if ((int)spec_smem_need(mode, DK, Gh, iob, stb) > kSpecSmemMax) return cudaErrorInvalidConfiguration;
   const dim3 block(kSpecThreads);
   const int nsplit = spec_item_nsplit(DK);
   const SpecSmem Lc = spec_smem(LAYOUT_COEF, DK, DK, Gh, iob, stb, 0);

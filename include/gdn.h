@@ -267,7 +267,8 @@ gdn_status gdn_decode(const gdn_dims* dims, const gdn_batch* batch,
  * record slot 1-L, then the items per (request, value head), which also
  * store the candidates' u for the next step. Returns GDN_ERR_UNSUPPORTED
  * when a q/k head's group of value heads is too wide for the kernels'
- * shared memory (about (Hv/Hk) Dv > 4000 at bf16 rows). */
+ * shared memory (more than 124 value heads per q/k head at Dk = Dv = 128
+ * with bf16 rows and fp32 state). */
 gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch,
                            const gdn_params* params, const void* qkv,
                            const void* a, const void* b, void* o, void* pages,
@@ -288,7 +289,10 @@ gdn_status gdn_spec_verify(const gdn_dims* dims, const gdn_batch* batch,
  * for gdn_conv + gdn_spec_verify.
  *   x       device [num_rows][C] io dtype (raw conv inputs, candidate rows)
  *   conv_w  device [C][W];  a, b, o, pages, status as gdn_spec_verify.
- * Returns GDN_ERR_UNSUPPORTED where gdn_spec_verify does. */
+ * Returns GDN_ERR_UNSUPPORTED when the group's rows and replay u do not fit
+ * in shared memory (more than 18 value heads per q/k head at Dk = Dv = 128
+ * with bf16 rows and fp32 state; gdn_conv + gdn_spec_verify take such
+ * shapes). */
 gdn_status gdn_spec_step(const gdn_dims* dims, const gdn_batch* batch,
                          const gdn_params* params, const void* x,
                          const void* conv_w, const void* a, const void* b,
@@ -303,7 +307,10 @@ gdn_status gdn_spec_step(const gdn_dims* dims, const gdn_batch* batch,
  * resumes request r from slot n_accepted[r] (0 <= n_accepted < Kc; the
  * caller seeds slot 0 before the first step), runs its row_len candidates
  * through conv and rule, and stores the state and window after candidate i
- * into slot i. Two launches (conv, then rule) on `stream`.
+ * into slot i. Two launches (conv, then the closed-form run per candidate)
+ * on `stream`. Returns GDN_ERR_UNSUPPORTED when the group's rows do not fit
+ * in shared memory (more than 42 value heads per q/k head at Dk = Dv = 128
+ * with bf16 rows and fp32 state).
  *   x     device [num_rows][C] raw candidate rows (io dtype)
  *   y     device [num_rows][C] io dtype, receives the conv'd rows
  *   a, b, o, conv_w, status as gdn_conv / gdn_seq.                       */

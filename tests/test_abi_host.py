@@ -177,3 +177,37 @@ def test_bounded_wait_check_validates_arguments(lib):
     assert lib.gdn_check_bounded_wait(0, 8, None) == -1                 # limit <= 0
     assert lib.gdn_check_bounded_wait(-5, 8, None) == -1
     assert lib.gdn_check_bounded_wait(10 ** 10 + 1, 8, None) == -1      # above 10 s
+
+
+def _widest_group(lib, entry, io, state):
+    """Largest number of value heads per q/k head (Dk = Dv = 128) that the
+    entry accepts: the shared-memory fit is checked on the host before any
+    launch (an empty batch then returns GDN_OK)."""
+    params = gdn.make_params(8, 8)
+    b = _batch(R=0, rows=0)
+    widest = 0
+    for gh in range(1, 200):
+        d = gdn.make_dims(1, gh, 128, 128, 4, 8, io, state, gdn.GDN_BF16)
+        D, B, P = ctypes.byref(d), ctypes.byref(b), ctypes.byref(params)
+        if entry == "verify":
+            rc = lib.gdn_spec_verify(D, B, P, 8, 8, 8, 8, 8, 8, None)
+        elif entry == "step":
+            rc = lib.gdn_spec_step(D, B, P, 8, 8, 8, 8, 8, 8, 8, None)
+        else:
+            rc = lib.gdn_spec_slots(D, B, P, 8, 8, 8, 8, 8, 8, 8, 8, None)
+        if rc != 0:
+            assert rc == gdn.CODES["GDN_ERR_UNSUPPORTED"], (entry, gh, rc)
+            break
+        widest = gh
+    return widest
+
+
+def test_each_spec_entry_checks_only_its_own_kernels(lib):
+    """gdn_spec_verify is limited only by its coefficient and item kernels,
+    not by the wider shared-memory needs of the one-launch step (which stages
+    the group's rows and u) or of the slot kernel (the group's rows). The
+    figures are the ones include/gdn.h quotes."""
+    bf, f32 = gdn.GDN_BF16, gdn.GDN_F32
+    assert _widest_group(lib, "verify", bf, f32) == 124
+    assert _widest_group(lib, "step", bf, f32) == 18
+    assert _widest_group(lib, "slots", bf, f32) == 42
