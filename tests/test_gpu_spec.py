@@ -383,6 +383,24 @@ def test_one_page_bit_identical_to_slots_other_shapes_bf16_state(hk, hv, dk):
                      200 + hk * 1000 + hv * 10 + dk, state=gdn.GDN_BF16)
 
 
+def test_wide_group_verify_bit_identical_to_slots_step_refused():
+    """32 value heads on one q/k head at Dk = Dv = 128: the one-page verify
+    (bounded only by its own kernels) stays bit-identical to the slot layout,
+    and the one-launch step, whose CTA stages the whole group's rows and u,
+    refuses the shape on the host with GDN_ERR_UNSUPPORTED."""
+    sh = synth.Shapes(Hk=1, Hv=32, Dk=128, Dv=128)
+    _ragged_vs_slots(sh, synth.BF16, 4242, R=3, steps=3)
+    d = synth.spec(seed=1, R=2, steps=1, n=1, sh=sh, io=synth.BF16)
+    L, _, _ = make_layers(d, 2, gdn.GDN_F32, slots=False)
+    rows = synth.rows(np.random.default_rng(0), 2, sh, synth.BF16)
+    B = L.batch(np.arange(2, dtype=np.int32), np.ones(2, np.int32), flags=spec_flags(0, 2),
+                n_accepted=np.zeros(2, np.int32), max_rows=1)
+    with pytest.raises(gdn.GdnError) as e:
+        L.spec_step(B, to_dev(rows["x"]), to_dev(rows["a"]), to_dev(rows["b"]))
+    assert e.value.code == gdn.CODES["GDN_ERR_UNSUPPORTED"]
+    L.ok()
+
+
 @pytest.mark.parametrize("Kc", [1, 3])
 def test_one_page_bit_identical_to_slots_small_record(Kc):
     """A record of 1 row (no drafts: every step verifies one token, so the
