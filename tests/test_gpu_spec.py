@@ -640,6 +640,38 @@ def test_fused_step_equals_conv_verify_other_shapes_ragged(hk, hv, dk, io, state
         prev_len = ln
 
 
+@pytest.mark.parametrize("gate_mode", [0, 1])
+def test_fused_step_bf16_outputs_and_gate_modes(gate_mode):
+    """gdn_spec_step with bf16 outputs (the benchmark's configuration) and
+    with raw or precomputed gates (a = g <= 0, b = beta): outputs, record,
+    coefficients, u, windows and states equal gdn_conv + gdn_spec_verify bit
+    for bit over 6 steps."""
+    d = synth.spec(R=8, steps=6)
+    R, n, steps, sh = d["R"], d["n"], d["steps"], d["shapes"]
+    start, ln = d["row_start"][:R], d["row_len"][:R]
+    rng = np.random.default_rng(77 + gate_mode)
+    Ls = []
+    for _ in range(2):
+        L = Layer(sh, d["io"], d["A_log"], d["dt_bias"], d["conv_w"], Kc=8, num_pages=R,
+                  out=gdn.GDN_BF16, gate_mode=gate_mode)
+        L.seed(range(R), S0=d["S0"][:R], hist=to_dev(d["hist0"])[:R])
+        Ls.append(L)
+    L1, L3 = Ls
+    for s in range(steps):
+        x, a, b = step_rows(d, s, R, n)
+        if gate_mode == 1:
+            a = to_dev(synth.as_io(-np.abs(rng.standard_normal((R * n, sh.Hv))) * 0.7, synth.BF16))
+            b = to_dev(synth.as_io(rng.uniform(0, 1, (R * n, sh.Hv)), synth.BF16))
+        acc = d["accepted"][s][:R]
+        _, o1 = one_page_step(L1, start, ln, spec_flags(s, R), acc, x, a, b)
+        o3 = L3.spec_step(L3.batch(start, ln, flags=spec_flags(s, R), n_accepted=acc), x, a, b)
+        L1.ok()
+        L3.ok()
+        assert o3.dtype == torch.bfloat16
+        assert np.array_equal(bits(o3), bits(o1)), f"outputs differ at step {s}"
+        assert torch.equal(L3.pool.buf, L1.pool.buf), f"pages differ at step {s}"
+
+
 def test_fused_step_device_errors_leave_the_page_alone():
     d = synth.spec(R=4, steps=2)
     n = d["n"]
