@@ -614,9 +614,20 @@ def test_fused_step_equals_conv_verify_other_shapes_ragged(hk, hv, dk, io, state
     three head dimensions and groups of 1, 3 and 8 value heads, fp32 and
     bf16 state: gdn_spec_step leaves every page and output exactly as
     gdn_conv + gdn_spec_verify."""
-    sh = synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk)
-    rng = np.random.default_rng(300 + hk * 1000 + hv * 10 + dk)
-    R, Kc, steps = 6, 8, 5
+    _fused_vs_conv_verify(synth.Shapes(Hk=hk, Hv=hv, Dk=dk, Dv=dk), io, state,
+                          300 + hk * 1000 + hv * 10 + dk)
+
+
+@pytest.mark.parametrize("Kc", [1, 3])
+def test_fused_step_equals_conv_verify_small_record(Kc):
+    """Records of 1 and 3 rows (the window then holds 3 + Kc columns)."""
+    _fused_vs_conv_verify(synth.Shapes(Hk=2, Hv=4, Dk=64, Dv=64), synth.BF16, gdn.GDN_F32,
+                          900 + Kc, Kc=Kc)
+
+
+def _fused_vs_conv_verify(sh, io, state, seed, Kc=8):
+    rng = np.random.default_rng(seed)
+    R, steps = 6, 5
     d = synth.spec(seed=int(rng.integers(1 << 30)), R=R, steps=1, n=1, sh=sh, io=io)
     L1, _, _ = make_layers(d, R, state, slots=False, Kc=Kc)
     L3, _, _ = make_layers(d, R, state, slots=False, Kc=Kc)
